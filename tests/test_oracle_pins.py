@@ -1,0 +1,300 @@
+"""Pins of the fp64 oracle against facts the pages and the mathematics fix.
+
+Nothing here re-types the oracle's own formula: the score is checked against
+a brute-force recomputation of attention with each token deleted (the
+definition the DropKV page derives its closed form from), against a hand
+closed form for two keys, and against invariants (softmax rows sum to one,
+causality).  Selection is checked against a brute-force sort and its
+invariants; budgets against the sums and ratios RippleKV and PyramidKV state.
+A final group compiles mutated copies of the oracle (a dropped factor, a
+squared norm, a lost causal mask, a wrong tie-break) and checks that some pin
+rejects each.
+"""
+import math
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def _bf16(rng, shape, scale=1.0):
+    return synth.f32_to_bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+def _f64(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _softmax_out(qv, K, V, keys, scale):
+    s = np.array([scale * float(qv @ K[j]) for j in keys])
+    e = np.exp(s - s.max())
+    p = e / e.sum()
+    return p @ V[list(keys)], dict(zip(keys, p))
+
+
+def brute_force_scores(q, k, v, G, w, scale=None):
+    """sum over rows of || attention without j  -  attention with all keys ||, per j.
+
+    DropKV, "Methodology in Plain English": deleting a token renormalises the
+    softmax over the survivors; the score is the size of the resulting output
+    shift.  Computed by literally deleting the token and recomputing.
+    """
+    Q, K, V = _f64(q).reshape(G * w, -1), _f64(k), _f64(v)
+    n, d = K.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    S = np.zeros(n)
+    for i in range(G * w):
+        pos = n - w + i % w
+        keys = list(range(pos + 1))
+        a_full, _ = _softmax_out(Q[i], K, V, keys, scale)
+        for j in keys:
+            rest = [t for t in keys if t != j]
+            a_minus, _ = _softmax_out(Q[i], K, V, rest, scale)
+            S[j] += np.linalg.norm(a_minus - a_full)
+    return S
+
+
+# --------------------------------------------------------------------------
+# score pins
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("n,d", [(5, 4), (17, 8), (64, 16)])
+def test_single_query_removal_identity(n, d):
+    """One query: the closed-form score equals the brute-force removal shift."""
+    rng = np.random.default_rng(n * 31 + d)
+    q, k, v = _bf16(rng, (1, d)), _bf16(rng, (n, d)), _bf16(rng, (n, d))
+    S = oracle.unit_scores(q, k, v, G=1, w=1)
+    ref = brute_force_scores(q, k, v, 1, 1)
+    np.testing.assert_allclose(S, ref, rtol=1e-11, atol=0)
+
+
+@pytest.mark.parametrize("G,w,n", [(2, 3, 11), (4, 4, 24), (3, 5, 9)])
+def test_window_and_group_removal_identity(G, w, n):
+    """Sum over the window rows and GQA heads, each causal, of the removal shift."""
+    rng = np.random.default_rng(G * 100 + w * 10 + n)
+    d = 8
+    q, k, v = _bf16(rng, (G * w, d)), _bf16(rng, (n, d)), _bf16(rng, (n, d))
+    S = oracle.unit_scores(q, k, v, G=G, w=w)
+    ref = brute_force_scores(q, k, v, G, w)
+    np.testing.assert_allclose(S, ref, rtol=1e-11, atol=0)
+
+
+def test_two_key_closed_form():
+    """n=2, one query: S_0 = p_0 * ||v_1 - v_0||, S_1 = p_1 * ||v_1 - v_0||.
+
+    Derivation: a - v_0 = p_1 (v_1 - v_0), so p_0/(1-p_0) * ||a - v_0||
+    = (p_0/p_1) * p_1 ||v_1 - v_0||.
+    """
+    rng = np.random.default_rng(5)
+    d = 16
+    q, k, v = _bf16(rng, (1, d)), _bf16(rng, (2, d)), _bf16(rng, (2, d))
+    Q, K, V = _f64(q)[0], _f64(k), _f64(v)
+    s0, s1 = (Q @ K[0]) / 4.0, (Q @ K[1]) / 4.0
+    p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    p1 = 1.0 - p0
+    gap = math.sqrt(sum((V[1, c] - V[0, c]) ** 2 for c in range(d)))
+    S = oracle.unit_scores(q, k, v, G=1, w=1)
+    assert S[0] == pytest.approx(p0 * gap, rel=1e-12)
+    assert S[1] == pytest.approx(p1 * gap, rel=1e-12)
+
+
+def test_softmax_rows_sum_to_one():
+    """With every value row equal to ones, a = sum_j p_j = 1 for each row."""
+    rng = np.random.default_rng(6)
+    G, w, n, d = 4, 8, 300, 32
+    q, k = _bf16(rng, (G * w, d), 3.0), _bf16(rng, (n, d), 3.0)
+    ones = synth.f32_to_bf16_bits(np.ones((n, d), np.float32))
+    m, l, a = oracle.window_attention(q, k, ones, G, w)
+    np.testing.assert_allclose(a, 1.0, rtol=0, atol=1e-13)
+    assert np.all(l >= 1.0 - 1e-15)
+    # m is the largest causal logit of the row
+    Q, K = _f64(q), _f64(k)
+    for i in range(G * w):
+        pos = n - w + i % w
+        assert m[i] == pytest.approx((K[:pos + 1] @ Q[i]).max() / math.sqrt(d), rel=1e-14)
+
+
+def test_attention_is_causal():
+    """Row at window slot t never sees keys after position n - w + t."""
+    rng = np.random.default_rng(7)
+    G, w, n, d = 2, 6, 40, 8
+    q, k, v = _bf16(rng, (G * w, d)), _bf16(rng, (n, d)), _bf16(rng, (n, d))
+    _, _, a1 = oracle.window_attention(q, k, v, G, w)
+    k2, v2 = k.copy(), v.copy()
+    k2[n - w + 1:] = _bf16(rng, (w - 1, d), 5.0)
+    v2[n - w + 1:] = _bf16(rng, (w - 1, d), 5.0)
+    _, _, a2 = oracle.window_attention(q, k2, v2, G, w)
+    slot0 = [i for i in range(G * w) if i % w == 0]
+    np.testing.assert_array_equal(a1[slot0], a2[slot0])
+    assert not np.allclose(a1, a2)
+
+
+def test_attention_matches_definition():
+    rng = np.random.default_rng(8)
+    G, w, n, d = 3, 4, 50, 16
+    q, k, v = _bf16(rng, (G * w, d)), _bf16(rng, (n, d)), _bf16(rng, (n, d))
+    m, l, a = oracle.window_attention(q, k, v, G, w)
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    for i in range(G * w):
+        pos = n - w + i % w
+        ref, _ = _softmax_out(Q[i], K, V, list(range(pos + 1)), 1.0 / math.sqrt(d))
+        np.testing.assert_allclose(a[i], ref, rtol=1e-12, atol=1e-15)
+
+
+def test_single_visible_key_is_rejected():
+    """w = n: the first window row sees one key, p = 1, the shift is unbounded."""
+    rng = np.random.default_rng(9)
+    q, k, v = _bf16(rng, (3, 4)), _bf16(rng, (3, 4)), _bf16(rng, (3, 4))
+    with pytest.raises(ValueError):
+        oracle.unit_scores(q, k, v, G=1, w=3)
+
+
+# --------------------------------------------------------------------------
+# selection pins
+# --------------------------------------------------------------------------
+def brute_select(S, w, sinks, b):
+    n = len(S)
+    mid = sorted(range(sinks, n - w), key=lambda j: (-S[j], j))[: b - sinks - w]
+    return sorted(list(range(sinks)) + mid + list(range(n - w, n)))
+
+
+@pytest.mark.parametrize("n,w,sinks,b", [(100, 8, 4, 30), (50, 4, 4, 8), (50, 4, 4, 50),
+                                         (9, 5, 4, 9), (64, 16, 4, 20), (33, 1, 0, 7)])
+def test_select_matches_brute_force(n, w, sinks, b):
+    rng = np.random.default_rng(n + b)
+    S = rng.integers(0, 6, n).astype(np.float64)  # many ties
+    got = oracle.select(S, w, sinks, b)
+    assert list(got) == brute_select(S, w, sinks, b)
+    assert len(got) == b and np.all(np.diff(got) > 0)
+    assert set(range(sinks)) <= set(got) and set(range(n - w, n)) <= set(got)
+
+
+def test_select_tie_break_lower_index():
+    S = np.zeros(20)
+    S[[6, 9, 12]] = 1.0
+    got = oracle.select(S, w=2, sinks=4, b=4 + 2 + 5)
+    # three ones, then the two lowest-index zeros of the middle [4, 18)
+    assert list(got) == [0, 1, 2, 3, 4, 5, 6, 9, 12, 18, 19]
+
+
+def test_select_rejects_small_budget():
+    with pytest.raises(ValueError):
+        oracle.select(np.zeros(40), w=8, sinks=4, b=11)
+    with pytest.raises(ValueError):
+        oracle.select(np.zeros(40), w=8, sinks=4, b=41)
+
+
+# --------------------------------------------------------------------------
+# budget pins
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("L,B", [(32, 13107), (28, 6553), (1, 256), (2, 100), (80, 999)])
+def test_budgets_sum_to_L_times_B(L, B):
+    """RippleKV Eq. (5): the layer budgets sum to the global budget."""
+    prof = synth.ripple_profile(synth.QWEN7B_128K.scaled(num_layers=L))
+    for b in (oracle.budgets_uniform(L, B), oracle.budgets_pyramid(L, B),
+              oracle.budgets_ripple(L, B, prof, 2.0), oracle.budgets_ripple(L, B, prof, 0.7, 1.5)):
+        assert sum(b) == L * B and len(b) == L
+
+
+def test_pyramid_is_linear_from_1p8_to_0p2():
+    m = oracle.pyramid_multipliers(32)
+    assert m[0] == pytest.approx(1.8, rel=1e-14) and m[-1] == pytest.approx(0.2, rel=1e-13)
+    assert sum(m) / 32 == pytest.approx(1.0, rel=1e-15)
+    steps = np.diff(m)
+    np.testing.assert_allclose(steps, -1.6 / 31, rtol=1e-12)
+    b = oracle.budgets_pyramid(32, 13107)
+    assert all(x > y for x, y in zip(b, b[1:]))
+    assert abs(b[0] - 1.8 * 13107) < 1 and abs(b[-1] - 0.2 * 13107) < 1
+
+
+def test_ripple_ratio_is_r():
+    """RippleKV after Eq. (10): max/min multiplier before clipping is exactly r = e^beta."""
+    prof = synth.ripple_profile(synth.QWEN7B_128K)
+    for beta in (0.5, 2.0, math.log(1.5)):
+        m = oracle.ripple_multipliers(prof, beta)
+        assert max(m) / min(m) == pytest.approx(math.exp(beta), rel=1e-13)
+        assert sum(m) / len(m) == pytest.approx(1.0, rel=1e-14)
+        # monotone in the profile
+        order = np.argsort(prof)
+        assert np.all(np.diff(np.asarray(m)[order]) >= -1e-15)
+
+
+def test_ripple_special_cases():
+    """Eq. (9): constant profile -> uniform; r = 1 -> uniform; invariant to s -> a*s + c."""
+    L, B = 28, 6553
+    assert oracle.budgets_ripple(L, B, [0.3] * L, 2.0) == [B] * L
+    prof = synth.ripple_profile(synth.QWEN7B_128K)
+    assert oracle.budgets_ripple(L, B, prof, 0.0) == [B] * L
+    np.testing.assert_allclose(oracle.ripple_multipliers(prof * 3.5 + 7.0, 2.0),
+                               oracle.ripple_multipliers(prof, 2.0), rtol=1e-13)
+
+
+def test_ripple_clip_bounds():
+    """Eq. (11): with gamma finite, pre-normalisation multipliers lie in [1/gamma, gamma]."""
+    prof = synth.ripple_profile(synth.QWEN7B_128K)
+    m = oracle.ripple_multipliers(prof, 3.0, gamma=4.0)
+    scale = max(m) / 4.0   # the largest was clipped to gamma
+    assert min(m) / scale >= 1.0 - 1e-12
+
+
+def test_ripple_profile_is_non_monotonic():
+    s = synth.ripple_profile(synth.QWEN7B_128K)
+    interior_max = any(s[i] > s[i - 1] and s[i] > s[i + 1] for i in range(1, len(s) - 1))
+    assert interior_max and np.argmax(s) not in (0, len(s) - 1)
+
+
+def test_largest_remainder_close_to_real():
+    mult = oracle.pyramid_multipliers(32)
+    b = oracle.largest_remainder(32, 1638, mult)
+    assert all(abs(bi - 1638 * m) < 1 for bi, m in zip(b, mult))
+
+
+def test_offsets_is_exclusive_scan():
+    o = oracle.offsets(np.array([[3, 4], [5, 6]]))
+    assert list(o) == [0, 3, 7, 12, 18]
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each mutated oracle must fail one of the pins above
+# --------------------------------------------------------------------------
+MUTATIONS = {
+    "drop_1_minus_p": ("S[j] += p / (1.0 - p) * sqrt(dist2);", "S[j] += p * sqrt(dist2);"),
+    "squared_norm": ("S[j] += p / (1.0 - p) * sqrt(dist2);", "S[j] += p / (1.0 - p) * dist2;"),
+    "not_causal": ("const int pos = n - w + (i % w);\n        const uint16_t *qrow = q + (size_t)i * d;\n        const double mx = row_logits(pos, d, scale, qrow, k, s);\n        double sum = 0.0;\n        for (int j = 0; j <= pos; ++j) {\n            s[j] = exp(s[j] - mx);\n            sum += s[j];\n        }\n        for (int c = 0; c < d; ++c) a[c] = 0.0;",
+                   "const int pos = n - 1;\n        const uint16_t *qrow = q + (size_t)i * d;\n        const double mx = row_logits(pos, d, scale, qrow, k, s);\n        double sum = 0.0;\n        for (int j = 0; j <= pos; ++j) {\n            s[j] = exp(s[j] - mx);\n            sum += s[j];\n        }\n        for (int c = 0; c < d; ++c) a[c] = 0.0;"),
+    "tie_to_higher_index": ("return (a->idx > b->idx) - (a->idx < b->idx);",
+                            "return (a->idx < b->idx) - (a->idx > b->idx);"),
+    "sign_of_v": ("const double diff = a[c] - bf16_value(vj[c]);",
+                  "const double diff = a[c] + bf16_value(vj[c]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_reject_planted_mistake(name, tmp_path, monkeypatch):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) == 1, name
+    bad = tmp_path / "oracle.c"
+    bad.write_text(src.replace(old, new))
+    so = tmp_path / "_liboracle.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-o", str(so), str(bad), "-lm"])
+    monkeypatch.setattr(oracle, "_LIB_PATH", str(so))
+    monkeypatch.setattr(oracle, "_SRC", str(bad))
+    monkeypatch.setattr(oracle, "_lib", None)
+    pins = [lambda: test_single_query_removal_identity(17, 8),
+            lambda: test_window_and_group_removal_identity(2, 3, 11),
+            lambda: test_two_key_closed_form(),
+            lambda: test_select_tie_break_lower_index()]
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            failed += 1
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert failed >= 1, "planted mistake %r passed every pin" % name
