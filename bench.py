@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Throughput of the KV-cache eviction hot path on one GB300 (or N, weak scaling).
+
+One step = kv_score (window attention + rescoring) + kv_select_topk +
+kv_compact over the whole workload, inputs resident in HBM.  The default
+workload is the long-context configuration at n = 131072 (32 layers, 8 KV
+heads, 32 query heads, d = 128, w = 64, pyramid budgets averaging 10%).
+
+Prints one JSON line.  `value` counts unit-tokens (tokens x layers x KV heads,
+each scored, selected and compacted) per second over all ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference arm: the
+pages ship no code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens scored+selected+compacted/s at n=128K; achieved HBM GB/s vs GB300 peak"
+UNIT = "unit-tokens/s"
+DEFAULT_WORKLOAD = "long_32L_8kv_32q_d128_n131072_pyramid10"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 FMA ceiling of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-units", type=int, default=0, help="oracle sample size (0: one per core)")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+def kv_cache_bytes(layers, kv_heads, head_dim, tokens, bytes_per_elem=2):
+    """K and V bytes of a cache: 2 (K,V) x bytes x L x H x D x N (PyramidKV guide,
+    "The Long-Context Memory Wall")."""
+    return 2 * bytes_per_elem * layers * kv_heads * head_dim * tokens
+
+
+def algorithmic_bytes(wl, budgets):
+    """Bytes the path must move at least once: K+V read, the window queries read,
+    the compacted K/V and int32 indices written, the offsets table."""
+    L, H, d = wl.num_layers, wl.num_kv_heads, wl.head_dim
+    n_tot = sum(wl.seq_lengths())
+    kv_read = kv_cache_bytes(L, H, d, n_tot)
+    q_read = wl.num_requests * L * wl.num_q_heads * wl.window * d * 2
+    rows = int(np.asarray(budgets).sum())
+    out = rows * (2 * d * 2 + 4)
+    offsets = 8 * (wl.num_units + 1)
+    return kv_read + q_read + out + offsets
+
+
+def pass_pairs(wl):
+    """(row, key) pairs one scoring pass visits: each window row sees keys 0..pos."""
+    G, w = wl.group, wl.window
+    tot = 0
+    for n in wl.seq_lengths():
+        per_unit = G * sum(n - w + t + 1 for t in range(w))
+        tot += per_unit * wl.num_layers * wl.num_kv_heads
+    return tot
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the fp64 oracle on host cores
+# ---------------------------------------------------------------------------
+def oracle_inputs(wl, budgets, units, rows_per_unit=None):
+    """Host-regenerated inputs of `units` for the oracle (not timed)."""
+    import synth
+    outl = synth.outlier_channels(wl)
+    hp = synth.heavy_positions(wl)
+    qh = synth.q_window(wl)
+    hv = synth.heavy_rows(wl, qh) if wl.num_heavy else None
+    G, R = wl.group, wl.rows
+    rows = rows_per_unit or R
+    inputs = []
+    for u in units:
+        r, l, h = wl.unit_coords(u)
+        q = qh[r, l, h * G:(h + 1) * G].reshape(R, wl.head_dim)[:rows]
+        k, v = synth.kv_unit(wl, r, l, h, outl=outl, heavy_pos=hp, heavy_vec=hv)
+        inputs.append((q, k, v, int(budgets.reshape(-1)[u])))
+    return inputs
+
+
+def oracle_time(wl, inputs, threads):
+    """Times the oracle (score + select + gather) over prepared inputs, one unit per
+    thread; returns (seconds, unit-token equivalents).  An input with fewer than
+    G*w query rows counts as that fraction of a unit."""
+    import oracle
+    w = wl.window
+
+    def one(args):
+        q, k, v, b = args
+        S = oracle.unit_scores(q, k, v, max(1, q.shape[0] // w), w)
+        idx = oracle.select(S, w, wl.num_sinks, b)
+        oracle.compact(k, v, idx)
+        return k.shape[0] * q.shape[0] / wl.rows
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        work = sum(ex.map(one, inputs))
+    return time.perf_counter() - t0, work
+
+
+def run_reference(args, wl, budgets):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synth
+    cores = os.cpu_count() or 1
+    units = list(range(min(cores, wl.num_units)))
+    rows = wl.window   # one query head's window rows per unit per step
+    inputs = oracle_inputs(wl, budgets, units, rows_per_unit=rows)
+    times = []
+    work = 0.0
+    for s in range(args.warmup + args.steps):
+        dt, work = oracle_time(wl, inputs, cores)
+        if s >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    value = work / t
+    sample = ("%d units x %d of %d window rows (one query head), full n=%d, per step; "
+              "work counted as %.4f units" % (len(units), rows, wl.rows, wl.seq_lengths()[0],
+                                              work / wl.seq_lengths()[0]))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+# Kernels of one step and how many launches each makes (the timed region
+# launches only these).  The score passes run on the CUDA cores in fp32.
+STAGES = ["attention", "rescore", "select", "compact"]
+LAUNCHES_PER_STEP = {"attention": 2, "rescore": 1, "select": 1, "compact": 1}
+STAGE_KERNELS = {"attention": "attn_partial_kernel+attn_merge_kernel",
+                 "rescore": "rescore_kernel", "select": "select_kernel",
+                 "compact": "compact_kernel"}
+SCORE_ENGINE = "alu"
+# DRAM bytes per launch from an ncu capture of the current kernels (None: not taken)
+TRAFFIC = {}
+
+
+def product_budgets(kv, wl):
+    import synth
+    L, H = wl.num_layers, wl.num_kv_heads
+    prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
+    rows = []
+    for B in wl.mean_budgets():
+        if wl.budget_policy == "uniform":
+            bl = kv.kv_budgets_uniform(L, B)
+        elif wl.budget_policy == "pyramid":
+            bl = kv.kv_budgets_pyramid(L, B, wl.pyramid_max, wl.pyramid_min)
+        else:
+            bl = kv.kv_budgets_ripple(L, B, prof, wl.ripple_beta)
+        rows.append(np.repeat(np.asarray(bl, np.int32)[:, None], H, axis=1))
+    return np.asarray(rows, dtype=np.int32)
+
+
+def stage_roofline(stage, ms, wl, budgets, peaks):
+    d = wl.head_dim
+    units = wl.num_units
+    n_tot = sum(wl.seq_lengths())
+    rows = int(np.asarray(budgets).sum())
+    if stage in ("attention", "rescore"):
+        flops = pass_pairs(wl) * 4 * d       # two d-long dot products per (row, key)
+        achieved = flops / (ms * 1e-3) / 1e12
+        if SCORE_ENGINE == "tensor":
+            peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+            bound = "tensor"
+        else:
+            peak = ALU_FP32_TFLOPS
+            bound = "alu"
+        return {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "algorithmic": flops}
+    if stage == "select":
+        nbytes = n_tot * wl.num_layers * wl.num_kv_heads * 4 + rows * 4 + 8 * (units + 1) * 2
+    else:
+        nbytes = rows * (2 * d * 2) * 2 + rows * 4 + 8 * (units + 1)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "algorithmic": nbytes}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    import synth
+    wl = synth.BY_NAME[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
+        return run_reference(args, wl, oracle.segment_budgets(wl, prof))
+
+    import torch
+    import kv_cache_eviction_split_gb300 as kv
+    from synth.device import DeviceWorkload
+    kv.load()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+
+    budgets = product_budgets(kv, wl)
+    dw = DeviceWorkload(wl, device=dev)
+    prob = kv.Problem.for_workload(wl, device=dev)
+    bufs = kv.Buffers(prob, budgets)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        kv.kv_score_attention(prob, dw.q, dw.k, dw.v, bufs.score_ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        kv.kv_score_rescore(prob, dw.q, dw.k, dw.v, bufs.scores, bufs.score_ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        kv.kv_select_topk(prob, bufs.scores, bufs.budgets, bufs.offsets, bufs.sel,
+                          bufs.select_ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        kv.kv_compact(prob, dw.k, dw.v, bufs.sel, bufs.offsets, bufs.total_rows, bufs.k_out,
+                      bufs.v_out, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    for _ in range(max(args.warmup, 0)):
+        step()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st = (kv.kv_check_status(bufs.score_ws, stream), kv.kv_check_status(bufs.select_ws, stream))
+    if st != (0, 0):
+        raise SystemExit("device status after the timed region: %s" % (st,))
+    stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
+                                   for i in range(args.steps)) for j, s in enumerate(STAGES)}
+    ms_per_step = total_ms / args.steps
+    n_tot = sum(wl.seq_lengths())
+    unit_tokens = n_tot * wl.num_layers * wl.num_kv_heads
+    value = unit_tokens * world / (ms_per_step * 1e-3)
+    alg_bytes = algorithmic_bytes(wl, budgets)
+    hbm_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
+
+    dominant = max(("attention", "rescore", "select", "compact"), key=lambda s: stage_ms[s])
+    roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks)
+    roof.update({"kernel": STAGE_KERNELS[dominant], "peak_source": peak_src,
+                 "traffic": TRAFFIC.get(STAGE_KERNELS[dominant])})
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if SCORE_ENGINE == "alu" else "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "layers": wl.num_layers,
+                       "kv_heads": wl.num_kv_heads, "q_heads": wl.num_q_heads,
+                       "head_dim": wl.head_dim, "n": wl.seq_lengths(), "window": wl.window,
+                       "budget": "%s, mean %s tokens/head" % (wl.budget_policy,
+                                                              wl.mean_budgets()),
+                       "units": wl.num_units, "parallelism": "replicas x%d" % world,
+                       "l2": "no flush: the K+V inputs (%.1f GB) exceed L2 every step"
+                             % (kv_cache_bytes(wl.num_layers, wl.num_kv_heads, wl.head_dim,
+                                               n_tot) / 1e9)},
+            "seq_tokens_per_s": n_tot * world / (ms_per_step * 1e-3),
+            "hbm": {"alg_bytes_per_step": alg_bytes, "achieved_gbs": hbm_gbs,
+                    "peak_gbs": peaks["hbm_gbs"], "frac": hbm_gbs / peaks["hbm_gbs"],
+                    "peak_source": peak_src},
+            "stages_ms": stage_ms,
+            "roofline": roof,
+            "gpu_launches": args.steps * sum(LAUNCHES_PER_STEP.values()),
+            "clocks": clocks}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens * world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
+        ob = oracle.segment_budgets(wl, prof)
+        cores = os.cpu_count() or 1
+        n_units = args.cpu_units or min(cores, 16, wl.num_units)
+        thr = min(cores, n_units)
+        dt, work = oracle_time(wl, oracle_inputs(wl, ob, list(range(n_units))), thr)
+        line["cpu_baseline"] = {"value": work / dt, "unit": UNIT,
+                                "cores": thr, "kind": "oracle",
+                                "sample": "%d full units (of %d) of the same workload, one "
+                                          "thread each, fp64 score + select + gather"
+                                          % (n_units, wl.num_units)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens):
+    """Same metric through the public API with host buffers: pinned host Q/K/V
+    copied in, the three calls, the kept indices and packed K/V copied out."""
+    try:
+        qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)
+        kh = torch.empty(dw.k.shape, dtype=dw.k.dtype, pin_memory=True)
+        vh = torch.empty(dw.v.shape, dtype=dw.v.dtype, pin_memory=True)
+        qh.copy_(dw.q)
+        kh.copy_(dw.k)
+        vh.copy_(dw.v)
+        rows = bufs.total_rows
+        selh = torch.empty(rows, dtype=torch.int32, pin_memory=True)
+        koh = torch.empty((rows, wl.head_dim), dtype=torch.bfloat16, pin_memory=True)
+        voh = torch.empty_like(koh, pin_memory=True)
+    except RuntimeError as e:
+        return {"value": None, "unit": UNIT, "error": "pinned host allocation failed: %s" % e}
+
+    def one():
+        dw.q.copy_(qh, non_blocking=True)
+        dw.k.copy_(kh, non_blocking=True)
+        dw.v.copy_(vh, non_blocking=True)
+        sel, ko, vo, _ = kv.evict(prob, dw.q, dw.k, dw.v, bufs, stream)
+        selh.copy_(sel, non_blocking=True)
+        koh.copy_(ko, non_blocking=True)
+        voh.copy_(vo, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = selh.numel() * 4 + (koh.numel() + voh.numel()) * 2
+    return {"value": unit_tokens / dt, "unit": UNIT, "ms_per_step": dt * 1e3,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

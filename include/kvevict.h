@@ -1,0 +1,188 @@
+/*
+ * kvevict.h -- C ABI of the GB300 KV-cache eviction hot path.
+ *
+ * Three steps run on one GPU, each asynchronous on the caller's stream:
+ *
+ *   kv_score        per-token DropKV removal score of every cached key
+ *   kv_select_topk  budgeted per-(request, layer, KV head) selection
+ *   kv_compact      ragged gather of the kept K/V rows
+ *
+ * Definitions (the pages these steps follow):
+ *
+ *  - Score.  "DropKV: Decoupling Residual-Output Perturbation for Near-Optimal
+ *    KV-Cache Eviction", Key Contributions item 1 and "Methodology in Plain
+ *    English": deleting token j alone shifts an attention output a by
+ *    p_j / (1 - p_j) * ||a - v_j||_2.  Here the score of key j is that shift
+ *    summed, unsquared, over the last w query positions of the request (the
+ *    observation window) and the G query heads that share the KV head, each
+ *    query attending causally.  It is computed in two streaming passes
+ *    (window attention with split-K and a merge, then a rescoring pass that
+ *    expands ||a - v||^2 = ||a||^2 - 2 a.v + ||v||^2, the expansion the same
+ *    section describes), never materialising the n x w attention matrix.
+ *  - Selection.  Same page, "Methodology in Plain English" (keep the highest
+ *    scores, pin the recent w) and the PyramidKV guide, "Observation Window
+ *    and Aggregated Attention Eviction" (always keep the first 4 sinks).
+ *  - Compaction.  GraceKV project page, section 05 "physical cache packing":
+ *    each layer-KV-head pair gets a cache of its own length.
+ *  - Layer budgets.  RippleKV, Eq. (9)-(12) and PyramidKV guide,
+ *    "Layer-Adaptive Dynamic Budget Allocation".
+ *
+ * Shapes.  R requests with lengths n_r (tokens packed, cu_seqlens
+ * seq_offsets[r] .. seq_offsets[r+1]), L layers, H KV heads, H_q = G*H query
+ * heads, head dim d in {64, 128}, window w, sinks s.  A "unit" (also
+ * "segment") is one (request, layer, KV head); units are ordered request-major,
+ * then layer, then head: u = (r*L + l)*H + h.
+ *
+ * Layouts (row-major; bf16 = IEEE bfloat16):
+ *   q_win   bf16 [R][L][H_q][w][d]   queries at positions n_r - w .. n_r - 1
+ *   k, v    bf16 [L][H][N_tot][d]    N_tot = seq_offsets[R]
+ *   scores  f32  [L][H][N_tot]
+ *   budgets i32  [R][L][H]           kept tokens per unit, sinks and window included
+ *   offsets i64  [R*L*H + 1]         exclusive scan of budgets (rows)
+ *   sel_idx i32  [offsets[R*L*H]]    kept token indices, local to the request, ascending
+ *   k_out, v_out bf16 [offsets[R*L*H]][d]
+ *
+ * Ownership.  The caller allocates and owns every buffer, host or device.
+ * The library allocates nothing and keeps no state between calls; the
+ * scratch it needs is the caller's workspace, sized by *_workspace_size.
+ * Functions are re-entrant; calls that share a workspace must be ordered on
+ * one stream.
+ *
+ * Errors.  Argument checks run on the host before anything is launched and
+ * return KV_ERR_INVALID_ARG / KV_ERR_BUDGET / KV_ERR_WORKSPACE /
+ * KV_ERR_UNSUPPORTED.  A failed launch returns KV_ERR_CUDA.  Conditions only
+ * the device can see (a budget in device memory out of range, an offsets table
+ * that disagrees with the budgets) are written to a status word in the
+ * workspace; kv_check_status reads it.
+ *
+ * Pointers: device pointers must be 16-byte aligned.  `stream` is a
+ * cudaStream_t (NULL = legacy default stream).
+ */
+#ifndef KVEVICT_H
+#define KVEVICT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kv_status {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or shape */
+    KV_ERR_BUDGET = 2,       /* a budget outside [sinks + w, n_r] */
+    KV_ERR_WORKSPACE = 3,    /* workspace smaller than *_workspace_size */
+    KV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    KV_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired */
+    KV_ERR_UNSUPPORTED = 6   /* shape outside what the kernels handle */
+} kv_status;
+
+typedef struct kv_problem {
+    int32_t num_requests;            /* R >= 0 (0: every call is a no-op) */
+    int32_t num_layers;              /* L >= 1 */
+    int32_t num_kv_heads;            /* H >= 1 */
+    int32_t num_q_heads;             /* H_q, a multiple of H; G = H_q / H */
+    int32_t head_dim;                /* d: 64 or 128 */
+    int32_t window;                  /* w >= 1 */
+    int32_t num_sinks;               /* s >= 0 (4 in the method) */
+    int32_t reserved;                /* must be 0 */
+    const int64_t *seq_offsets_host; /* [R+1] cu_seqlens, host memory; n_r >= s + w, n_r < 2^31 */
+    const int64_t *seq_offsets_dev;  /* the same [R+1] values, device memory */
+    float softmax_scale;             /* logit scale, normally 1/sqrt(d); > 0 */
+} kv_problem;
+
+/* Bytes of workspace kv_score / kv_score_attention / kv_score_rescore need. */
+kv_status kv_score_workspace_size(const kv_problem *p, size_t *bytes);
+
+/*
+ * Full scoring step: kv_score_attention then kv_score_rescore on one stream.
+ * scores receives one fp32 score per key of every unit, >= 0 (or +inf when a
+ * window row puts all of its attention on one key).
+ */
+kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const void *v,
+                   float *scores, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Pass 1: causal window attention of every unit with split-K over the keys and
+ * a merge of the splits (row max, row sum and a = sum p v); leaves them in the
+ * workspace for pass 2.
+ */
+kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void *k,
+                             const void *v, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Pass 2: rescoring of every key from the pass-1 results in the workspace. */
+kv_status kv_score_rescore(const kv_problem *p, const void *q_win, const void *k,
+                           const void *v, float *scores, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * Host helper: offsets[u+1] = offsets[u] + budgets[u] for the R*L*H units,
+ * offsets[0] = 0, after checking every budget lies in [s + w, n_r].
+ * budgets_host [R*L*H] and offsets_host [R*L*H + 1] are host memory.
+ */
+kv_status kv_make_offsets(const kv_problem *p, const int32_t *budgets_host,
+                          int64_t *offsets_host);
+
+/* Bytes of workspace kv_select_topk needs. */
+kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes);
+
+/*
+ * Per unit: keep the s sinks and the w window tokens, and from the middle
+ * candidates [s, n_r - w) the budget - s - w highest scores, equal scores
+ * going to the lower index.  Writes the kept indices, ascending, to
+ * sel_idx[offsets[u] .. offsets[u+1]).  scores as written by kv_score (the
+ * ordering compares the fp32 bit patterns, exact for values >= 0).
+ * budgets_dev / offsets_dev: device copies of the tables above.  A budget
+ * that is out of range, or disagrees with offsets, leaves its unit untouched
+ * and posts KV_ERR_BUDGET to the workspace status word.
+ */
+kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
+                         const int64_t *offsets_dev, int32_t *sel_idx, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * k_out[offsets[u] + i] = k[row of unit u, token sel_idx[offsets[u] + i]],
+ * the same for v: a bit copy of the kept rows into one packed ragged cache.
+ * total_rows = offsets[R*L*H] (the caller knows it from kv_make_offsets).
+ * Indices must be in [0, n_r); out-of-range ones are skipped and their output
+ * rows left untouched.
+ */
+kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const int32_t *sel_idx,
+                     const int64_t *offsets_dev, int64_t total_rows, void *k_out, void *v_out,
+                     void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of a
+ * kv_score or kv_select_topk workspace.  *device_status receives the kv_status
+ * a kernel posted (KV_OK if none).  Returns KV_ERR_CUDA if the stream itself
+ * reports an error.
+ */
+kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status);
+
+/* Static, human-readable name of a status code. */
+const char *kv_status_string(kv_status s);
+
+/*
+ * Host helpers: per-layer budgets b_l (tokens per KV head) whose sum is
+ * exactly L*B.  Real targets B*m_l are rounded by largest remainder: floor
+ * each, then one more token to the layers with the largest fractional parts,
+ * ties to the lower layer.
+ *   pyramid: m_l proportional to lo + (hi - lo) * (1 - l/(L-1))^curve, mean 1
+ *            (PyramidKV guide; hi = 1.8, lo = 0.2, curve = 1 is linear).
+ *   ripple:  s_hat = min-max normalised profile (all 0 if constant), m_l
+ *            proportional to exp(beta * s_hat_l) clipped to [1/gamma, gamma]
+ *            (gamma = +inf: no clip), then mean 1 (RippleKV Eq. (9)-(11)).
+ * budgets_out: host [L].
+ */
+kv_status kv_budgets_pyramid(int32_t num_layers, int32_t mean_budget, double hi, double lo,
+                             double curve, int32_t *budgets_out);
+kv_status kv_budgets_ripple(int32_t num_layers, int32_t mean_budget, const double *profile,
+                            double beta, double gamma, int32_t *budgets_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVEVICT_H */

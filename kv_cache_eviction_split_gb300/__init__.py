@@ -1,0 +1,285 @@
+"""GB300-native KV-cache eviction: DropKV removal scores, budgeted top-k, ragged compaction.
+
+A thin ctypes binding over ``libkvevict.so`` (the C ABI in ``include/kvevict.h``).
+Every step of the path runs in the library's CUDA kernels; this module only
+marshals arguments (torch tensors -> pointers, sizes, the caller's stream)
+and allocates outputs and workspaces with torch.  There is no CPU fallback:
+if the library is missing, ``load()`` raises.
+
+Names follow the C ABI: ``kv_score``, ``kv_score_attention``,
+``kv_score_rescore``, ``kv_make_offsets``, ``kv_select_topk``, ``kv_compact``,
+``kv_check_status``, ``kv_budgets_pyramid``, ``kv_budgets_ripple``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import _build
+
+__all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attention",
+           "kv_score_rescore", "kv_make_offsets", "kv_select_topk", "kv_compact",
+           "kv_check_status", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
+           "EXPORTED_SYMBOLS", "evict"]
+
+KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
+    KV_ERR_UNSUPPORTED = range(7)
+
+EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
+                    "kv_score_rescore", "kv_make_offsets", "kv_select_workspace_size",
+                    "kv_select_topk", "kv_compact", "kv_check_status", "kv_status_string",
+                    "kv_budgets_pyramid", "kv_budgets_ripple")
+
+
+class KvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s" % (where, status_string(code)))
+
+
+class _KvProblem(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("num_sinks", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("seq_offsets_host", ctypes.POINTER(ctypes.c_int64)),
+                ("seq_offsets_dev", ctypes.c_void_p), ("softmax_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def load(path: Optional[str] = None):
+    """Load ``libkvevict.so``; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError("libkvevict.so not found at %s: run "
+                           "kv_cache_eviction_split_gb300.build() (needs nvcc)" % path)
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(_KvProblem)
+    vp, sz, i32, i64, f64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64, \
+        ctypes.c_double
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "kv_score_workspace_size": [P, szp],
+        "kv_score": [P, vp, vp, vp, vp, vp, sz, vp],
+        "kv_score_attention": [P, vp, vp, vp, vp, sz, vp],
+        "kv_score_rescore": [P, vp, vp, vp, vp, vp, sz, vp],
+        "kv_make_offsets": [P, ctypes.POINTER(i32), ctypes.POINTER(i64)],
+        "kv_select_workspace_size": [P, szp],
+        "kv_select_topk": [P, vp, vp, vp, vp, vp, sz, vp],
+        "kv_compact": [P, vp, vp, vp, vp, i64, vp, vp, vp],
+        "kv_check_status": [vp, vp, ctypes.POINTER(i32)],
+        "kv_budgets_pyramid": [i32, i32, f64, f64, f64, ctypes.POINTER(i32)],
+        "kv_budgets_ripple": [i32, i32, ctypes.POINTER(f64), f64, f64, ctypes.POINTER(i32)],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.kv_status_string.argtypes = [ctypes.c_int]
+    lib.kv_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().kv_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != KV_OK:
+        raise KvError(code, where)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+@dataclass
+class Problem:
+    """Shapes of one eviction problem; owns the host and device cu_seqlens."""
+    lengths: Sequence[int]
+    num_layers: int
+    num_kv_heads: int
+    num_q_heads: int
+    head_dim: int
+    window: int
+    num_sinks: int = 4
+    softmax_scale: Optional[float] = None
+    device: object = "cuda"
+
+    def __post_init__(self):
+        import torch
+        self.cu_host = np.concatenate([[0], np.cumsum(np.asarray(self.lengths, dtype=np.int64))]
+                                      ).astype(np.int64)
+        self.cu_dev = torch.from_numpy(self.cu_host).to(self.device) if len(self.lengths) else \
+            torch.zeros(1, dtype=torch.int64, device=self.device)
+        scale = self.softmax_scale if self.softmax_scale is not None else 1.0 / math.sqrt(self.head_dim)
+        self._c = _KvProblem(len(self.lengths), self.num_layers, self.num_kv_heads,
+                             self.num_q_heads, self.head_dim, self.window, self.num_sinks, 0,
+                             self.cu_host.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                             self.cu_dev.data_ptr(), float(scale))
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+    @property
+    def num_requests(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def num_units(self) -> int:
+        return self.num_requests * self.num_layers * self.num_kv_heads
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_host[-1])
+
+    @classmethod
+    def for_workload(cls, wl, device="cuda") -> "Problem":
+        return cls(wl.seq_lengths(), wl.num_layers, wl.num_kv_heads, wl.num_q_heads,
+                   wl.head_dim, wl.window, wl.num_sinks, device=device)
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+def kv_score_workspace_size(prob: Problem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().kv_score_workspace_size(prob.c, ctypes.byref(n)), "kv_score_workspace_size")
+    return n.value
+
+
+def kv_select_workspace_size(prob: Problem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().kv_select_workspace_size(prob.c, ctypes.byref(n)), "kv_select_workspace_size")
+    return n.value
+
+
+def kv_score(prob, q, k, v, scores, workspace, stream=None):
+    _check(load().kv_score(prob.c, _ptr(q), _ptr(k), _ptr(v), _ptr(scores), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "kv_score")
+
+
+def kv_score_attention(prob, q, k, v, workspace, stream=None):
+    _check(load().kv_score_attention(prob.c, _ptr(q), _ptr(k), _ptr(v), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream)), "kv_score_attention")
+
+
+def kv_score_rescore(prob, q, k, v, scores, workspace, stream=None):
+    _check(load().kv_score_rescore(prob.c, _ptr(q), _ptr(k), _ptr(v), _ptr(scores),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "kv_score_rescore")
+
+
+def kv_make_offsets(prob, budgets_host: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(-1)
+    out = np.zeros(b.size + 1, dtype=np.int64)
+    _check(load().kv_make_offsets(prob.c, b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                  out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))),
+           "kv_make_offsets")
+    return out
+
+
+def kv_select_topk(prob, scores, budgets_dev, offsets_dev, sel_idx, workspace, stream=None):
+    _check(load().kv_select_topk(prob.c, _ptr(scores), _ptr(budgets_dev), _ptr(offsets_dev),
+                                 _ptr(sel_idx), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "kv_select_topk")
+
+
+def kv_compact(prob, k, v, sel_idx, offsets_dev, total_rows: int, k_out, v_out, stream=None):
+    _check(load().kv_compact(prob.c, _ptr(k), _ptr(v), _ptr(sel_idx), _ptr(offsets_dev),
+                             int(total_rows), _ptr(k_out), _ptr(v_out), _stream(stream)),
+           "kv_compact")
+
+
+def kv_check_status(workspace, stream=None) -> int:
+    st = ctypes.c_int32()
+    _check(load().kv_check_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
+           "kv_check_status")
+    return st.value
+
+
+def kv_budgets_uniform(num_layers: int, mean_budget: int) -> np.ndarray:
+    return np.full(num_layers, int(mean_budget), dtype=np.int32)
+
+
+def kv_budgets_pyramid(num_layers: int, mean_budget: int, hi: float = 1.8, lo: float = 0.2,
+                       curve: float = 1.0) -> np.ndarray:
+    out = np.zeros(num_layers, dtype=np.int32)
+    _check(load().kv_budgets_pyramid(num_layers, mean_budget, hi, lo, curve,
+                                     out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "kv_budgets_pyramid")
+    return out
+
+
+def kv_budgets_ripple(num_layers: int, mean_budget: int, profile, beta: float = 2.0,
+                      gamma: float = math.inf) -> np.ndarray:
+    prof = np.ascontiguousarray(profile, dtype=np.float64)
+    out = np.zeros(num_layers, dtype=np.int32)
+    _check(load().kv_budgets_ripple(num_layers, mean_budget,
+                                    prof.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), beta,
+                                    gamma, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "kv_budgets_ripple")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# convenience: the whole path with torch-allocated outputs
+# ---------------------------------------------------------------------------
+class Buffers:
+    """Device outputs and workspaces of one problem, allocated once and reused."""
+
+    def __init__(self, prob: Problem, budgets_host: np.ndarray):
+        import torch
+        dev = prob.cu_dev.device
+        self.budgets_host = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(-1)
+        self.offsets_host = kv_make_offsets(prob, self.budgets_host)
+        self.total_rows = int(self.offsets_host[-1])
+        self.budgets = torch.from_numpy(self.budgets_host).to(dev)
+        self.offsets = torch.from_numpy(self.offsets_host).to(dev)
+        N, d = prob.total_tokens, prob.head_dim
+        self.scores = torch.empty((prob.num_layers, prob.num_kv_heads, N), dtype=torch.float32,
+                                  device=dev)
+        self.score_ws = torch.zeros(max(kv_score_workspace_size(prob), 256), dtype=torch.uint8,
+                                    device=dev)
+        self.select_ws = torch.zeros(max(kv_select_workspace_size(prob), 256), dtype=torch.uint8,
+                                     device=dev)
+        self.sel = torch.empty(max(self.total_rows, 1), dtype=torch.int32, device=dev)
+        self.k_out = torch.empty((max(self.total_rows, 1), d), dtype=torch.bfloat16, device=dev)
+        self.v_out = torch.empty_like(self.k_out)
+
+
+def evict(prob: Problem, q, k, v, bufs: Buffers, stream=None):
+    """Score, select and compact on `stream`; returns (sel_idx, k_out, v_out, offsets)."""
+    kv_score(prob, q, k, v, bufs.scores, bufs.score_ws, stream)
+    kv_select_topk(prob, bufs.scores, bufs.budgets, bufs.offsets, bufs.sel, bufs.select_ws, stream)
+    kv_compact(prob, k, v, bufs.sel, bufs.offsets, bufs.total_rows, bufs.k_out, bufs.v_out, stream)
+    n = bufs.total_rows
+    return bufs.sel[:n], bufs.k_out[:n], bufs.v_out[:n], bufs.offsets

@@ -1,0 +1,294 @@
+// kv_api.cu -- the extern "C" entry points: argument checks, workspace carve-up,
+// launches, the offsets scan and the per-layer budget policies (host code).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#include "kv_internal.cuh"
+
+using namespace kvevict;
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Validates the problem description and fills the device-side copy.
+kv_status make_problem(const kv_problem *p, DevProblem *P) {
+    if (!p) return KV_ERR_INVALID_ARG;
+    if (p->num_requests < 0 || p->num_layers < 1 || p->num_kv_heads < 1 ||
+        p->num_q_heads < p->num_kv_heads || p->num_q_heads % p->num_kv_heads != 0 ||
+        p->window < 1 || p->num_sinks < 0 || p->reserved != 0)
+        return KV_ERR_INVALID_ARG;
+    if (!(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale)) return KV_ERR_INVALID_ARG;
+    if (p->head_dim != 64 && p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+    const long long G = p->num_q_heads / p->num_kv_heads;
+    if (G * p->window > kMaxRows) return KV_ERR_UNSUPPORTED;
+    P->R = p->num_requests;
+    P->L = p->num_layers;
+    P->H = p->num_kv_heads;
+    P->Hq = p->num_q_heads;
+    P->G = (int)G;
+    P->d = p->head_dim;
+    P->w = p->window;
+    P->sinks = p->num_sinks;
+    P->rows = (int)(G * p->window);
+    P->cu = reinterpret_cast<const long long *>(p->seq_offsets_dev);
+    P->scale_log2 = p->softmax_scale * 1.4426950408889634f;
+    P->units = (long long)P->R * P->L * P->H;
+    P->max_n = 0;
+    P->N_tot = 0;
+    if (P->R > 0) {
+        if (!p->seq_offsets_host || !p->seq_offsets_dev) return KV_ERR_INVALID_ARG;
+        if (p->seq_offsets_host[0] != 0) return KV_ERR_INVALID_ARG;
+        for (int r = 0; r < P->R; ++r) {
+            const long long n = p->seq_offsets_host[r + 1] - p->seq_offsets_host[r];
+            if (n < (long long)p->num_sinks + p->window || n < 1 || n >= (1LL << 31))
+                return KV_ERR_INVALID_ARG;
+            P->max_n = std::max<long long>(P->max_n, n);
+        }
+        P->N_tot = p->seq_offsets_host[P->R];
+    }
+    P->max_splits = (P->max_n + kSplitKeys - 1) / kSplitKeys;
+    return KV_OK;
+}
+
+kv_status map_cuda(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+}  // namespace
+
+namespace kvevict {
+
+ScoreWs score_ws_layout(const DevProblem &P, void *base) {
+    ScoreWs ws{};
+    char *b = static_cast<char *>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = b ? b + off : nullptr;
+        off = round_up(off + bytes, 256);
+        return p;
+    };
+    const size_t U = (size_t)P.units, S = (size_t)P.max_splits, Rr = (size_t)P.rows, D = P.d;
+    ws.status = reinterpret_cast<int *>(take(kHeaderBytes));
+    ws.part_ml = reinterpret_cast<float2 *>(take(U * S * Rr * sizeof(float2)));
+    ws.part_o = reinterpret_cast<float *>(take(U * S * Rr * D * sizeof(float)));
+    ws.stat_ml = reinterpret_cast<float2 *>(take(U * Rr * sizeof(float2)));
+    ws.stat_a2 = reinterpret_cast<float *>(take(U * Rr * sizeof(float)));
+    ws.a_hat = reinterpret_cast<__nv_bfloat16 *>(take(U * Rr * D * sizeof(__nv_bfloat16)));
+    ws.total = off;
+    return ws;
+}
+
+}  // namespace kvevict
+
+extern "C" {
+
+const char *kv_status_string(kv_status s) {
+    switch (s) {
+        case KV_OK: return "KV_OK";
+        case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+        case KV_ERR_BUDGET: return "KV_ERR_BUDGET";
+        case KV_ERR_WORKSPACE: return "KV_ERR_WORKSPACE";
+        case KV_ERR_CUDA: return "KV_ERR_CUDA";
+        case KV_ERR_TIMEOUT: return "KV_ERR_TIMEOUT";
+        case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+    }
+    return "KV_ERR_UNKNOWN";
+}
+
+kv_status kv_score_workspace_size(const kv_problem *p, size_t *bytes) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK) return st;
+    if (!bytes) return KV_ERR_INVALID_ARG;
+    *bytes = score_ws_layout(P, nullptr).total;
+    return KV_OK;
+}
+
+static kv_status check_score_args(const kv_problem *p, DevProblem *P, const void *q,
+                                  const void *k, const void *v, const void *ws, size_t ws_bytes) {
+    kv_status st = make_problem(p, P);
+    if (st != KV_OK) return st;
+    if (P->units == 0) return KV_OK;
+    if (!q || !k || !v || !ws) return KV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+    if (ws_bytes < score_ws_layout(*P, nullptr).total) return KV_ERR_WORKSPACE;
+    return KV_OK;
+}
+
+kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void *k, const void *v,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    DevProblem P;
+    kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
+    if (st != KV_OK || P.units == 0) return st;
+    ScoreWs ws = score_ws_layout(P, workspace);
+    return map_cuda(launch_attention(P, (const __nv_bfloat16 *)q_win, (const __nv_bfloat16 *)k,
+                                     (const __nv_bfloat16 *)v, ws, (cudaStream_t)stream));
+}
+
+kv_status kv_score_rescore(const kv_problem *p, const void *q_win, const void *k, const void *v,
+                           float *scores, void *workspace, size_t workspace_bytes, void *stream) {
+    DevProblem P;
+    kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
+    if (st != KV_OK || P.units == 0) return st;
+    if (!scores || !aligned16(scores)) return KV_ERR_INVALID_ARG;
+    ScoreWs ws = score_ws_layout(P, workspace);
+    return map_cuda(launch_rescore(P, (const __nv_bfloat16 *)q_win, (const __nv_bfloat16 *)k,
+                                   (const __nv_bfloat16 *)v, scores, ws, (cudaStream_t)stream));
+}
+
+kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const void *v,
+                   float *scores, void *workspace, size_t workspace_bytes, void *stream) {
+    DevProblem P;
+    kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
+    if (st != KV_OK || P.units == 0) return st;
+    if (!scores || !aligned16(scores)) return KV_ERR_INVALID_ARG;
+    st = kv_score_attention(p, q_win, k, v, workspace, workspace_bytes, stream);
+    if (st != KV_OK) return st;
+    return kv_score_rescore(p, q_win, k, v, scores, workspace, workspace_bytes, stream);
+}
+
+kv_status kv_make_offsets(const kv_problem *p, const int32_t *budgets_host, int64_t *offsets_host) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK) return st;
+    if (!offsets_host || (P.units > 0 && !budgets_host)) return KV_ERR_INVALID_ARG;
+    offsets_host[0] = 0;
+    for (long long u = 0; u < P.units; ++u) {
+        const int r = (int)(u / ((long long)P.L * P.H));
+        const long long n = p->seq_offsets_host[r + 1] - p->seq_offsets_host[r];
+        const long long b = budgets_host[u];
+        if (b < (long long)P.sinks + P.w || b > n) return KV_ERR_BUDGET;
+        offsets_host[u + 1] = offsets_host[u] + b;
+    }
+    return KV_OK;
+}
+
+kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK) return st;
+    if (!bytes) return KV_ERR_INVALID_ARG;
+    *bytes = kHeaderBytes;
+    return KV_OK;
+}
+
+kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
+                         const int64_t *offsets_dev, int32_t *sel_idx, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK || P.units == 0) return st;
+    if (!scores || !budgets_dev || !offsets_dev || !sel_idx || !workspace) return KV_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(budgets_dev) || !aligned16(offsets_dev) ||
+        !aligned16(sel_idx) || !aligned16(workspace))
+        return KV_ERR_INVALID_ARG;
+    if (workspace_bytes < kHeaderBytes) return KV_ERR_WORKSPACE;
+    return map_cuda(launch_select(P, scores, budgets_dev, offsets_dev, sel_idx,
+                                  static_cast<int *>(workspace), (cudaStream_t)stream));
+}
+
+kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const int32_t *sel_idx,
+                     const int64_t *offsets_dev, int64_t total_rows, void *k_out, void *v_out,
+                     void *stream) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK || P.units == 0) return st;
+    if (total_rows < 0) return KV_ERR_INVALID_ARG;
+    if (total_rows == 0) return KV_OK;
+    if (!k || !v || !sel_idx || !offsets_dev || !k_out || !v_out) return KV_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(sel_idx) || !aligned16(offsets_dev) ||
+        !aligned16(k_out) || !aligned16(v_out))
+        return KV_ERR_INVALID_ARG;
+    return map_cuda(launch_compact(P, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, sel_idx,
+                                   offsets_dev, total_rows, (__nv_bfloat16 *)k_out,
+                                   (__nv_bfloat16 *)v_out, (cudaStream_t)stream));
+}
+
+kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status) {
+    if (!workspace || !device_status) return KV_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (word != 0 && cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return KV_ERR_CUDA;
+    *device_status = word;
+    return KV_OK;
+}
+
+// ----------------------------------------------------------------------------
+// per-layer budgets (host)
+// ----------------------------------------------------------------------------
+static kv_status largest_remainder(int L, int B, const std::vector<double> &mult, int32_t *out) {
+    std::vector<double> x(L), frac(L);
+    long long sum = 0;
+    for (int l = 0; l < L; ++l) {
+        x[l] = (double)B * mult[l];
+        const double f = std::floor(x[l]);
+        frac[l] = x[l] - f;
+        out[l] = (int32_t)f;
+        sum += (long long)f;
+    }
+    const long long deficit = (long long)L * B - sum;
+    if (deficit < 0 || deficit > L) return KV_ERR_INVALID_ARG;
+    std::vector<int> order(L);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        if (frac[a] != frac[b]) return frac[a] > frac[b];
+        return a < b;
+    });
+    for (long long i = 0; i < deficit; ++i) out[order[i]] += 1;
+    return KV_OK;
+}
+
+kv_status kv_budgets_pyramid(int32_t num_layers, int32_t mean_budget, double hi, double lo,
+                             double curve, int32_t *budgets_out) {
+    if (num_layers < 1 || mean_budget < 0 || !budgets_out || !(hi >= lo) || !(lo >= 0.0) ||
+        !(curve > 0.0))
+        return KV_ERR_INVALID_ARG;
+    const int L = num_layers;
+    std::vector<double> m(L, 1.0);
+    if (L > 1) {
+        double sum = 0.0;
+        for (int l = 0; l < L; ++l) {
+            m[l] = lo + (hi - lo) * std::pow(1.0 - (double)l / (double)(L - 1), curve);
+            sum += m[l];
+        }
+        const double mean = sum / L;
+        if (!(mean > 0.0)) return KV_ERR_INVALID_ARG;
+        for (int l = 0; l < L; ++l) m[l] = m[l] / mean;
+    }
+    return largest_remainder(L, mean_budget, m, budgets_out);
+}
+
+kv_status kv_budgets_ripple(int32_t num_layers, int32_t mean_budget, const double *profile,
+                            double beta, double gamma, int32_t *budgets_out) {
+    if (num_layers < 1 || mean_budget < 0 || !profile || !budgets_out || !(beta >= 0.0) ||
+        !(gamma >= 1.0))
+        return KV_ERR_INVALID_ARG;
+    const int L = num_layers;
+    double smin = profile[0], smax = profile[0];
+    for (int l = 0; l < L; ++l) {
+        if (!std::isfinite(profile[l])) return KV_ERR_INVALID_ARG;
+        smin = std::min(smin, profile[l]);
+        smax = std::max(smax, profile[l]);
+    }
+    std::vector<double> m(L);
+    double sum = 0.0;
+    for (int l = 0; l < L; ++l) {
+        const double shat = (smax == smin) ? 0.0 : (profile[l] - smin) / (smax - smin);
+        double t = std::exp(beta * shat);
+        if (std::isfinite(gamma)) t = std::min(std::max(t, 1.0 / gamma), gamma);
+        m[l] = t;
+        sum += t;
+    }
+    const double mean = sum / L;
+    for (int l = 0; l < L; ++l) m[l] = m[l] / mean;
+    return largest_remainder(L, mean_budget, m, budgets_out);
+}
+
+}  // extern "C"

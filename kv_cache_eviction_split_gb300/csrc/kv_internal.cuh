@@ -1,0 +1,82 @@
+// kv_internal.cuh -- shared definitions of the kvevict CUDA library (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/kvevict.h"
+
+namespace kvevict {
+
+// Largest R = G * w the kernels accept.
+constexpr int kMaxRows = 512;
+// Keys per split of the pass-1 attention (each split writes one partial).
+constexpr int kSplitKeys = 16384;
+// Bytes reserved at the start of every workspace for the status word.
+constexpr size_t kHeaderBytes = 256;
+
+// Problem description passed by value to every kernel.
+struct DevProblem {
+    int R, L, H, Hq, G, d, w, sinks;
+    int rows;                 // G * w
+    int max_n;                // longest request
+    int max_splits;           // ceil(max_n / kSplitKeys)
+    long long N_tot;          // packed tokens
+    long long units;          // R * L * H
+    const long long *cu;      // device cu_seqlens [R + 1]
+    float scale_log2;         // softmax_scale * log2(e)
+};
+
+struct UnitInfo {
+    int r, l, h;
+    int n;
+    long long tok0;           // first packed token of the request
+    long long kv_row0;        // first row of this unit in K/V/scores ([L][H][N_tot])
+    long long q_row0;         // first row of this unit's G*w query rows in q_win
+};
+
+__host__ __device__ inline UnitInfo unit_info(const DevProblem &P, long long u, const long long *cu) {
+    UnitInfo U;
+    U.h = (int)(u % P.H);
+    U.l = (int)((u / P.H) % P.L);
+    U.r = (int)(u / ((long long)P.H * P.L));
+    U.tok0 = cu[U.r];
+    U.n = (int)(cu[U.r + 1] - U.tok0);
+    U.kv_row0 = ((long long)U.l * P.H + U.h) * P.N_tot + U.tok0;
+    U.q_row0 = (((long long)U.r * P.L + U.l) * P.Hq + (long long)U.h * P.G) * P.w;
+    return U;
+}
+
+// Score workspace carve-up (all offsets 256-byte aligned).
+struct ScoreWs {
+    int *status;
+    float2 *part_ml;          // [units][max_splits][rows]  (m in log2 units, l)
+    float *part_o;            // [units][max_splits][rows][d]
+    float2 *stat_ml;          // [units][rows]  merged (m, l)
+    float *stat_a2;           // [units][rows]  ||a_hat||^2
+    __nv_bfloat16 *a_hat;     // [units][rows][d]
+    size_t total;
+};
+
+ScoreWs score_ws_layout(const DevProblem &P, void *base);
+
+// Launchers (return cudaGetLastError() of their launches).
+cudaError_t launch_attention(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t s);
+cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                           const __nv_bfloat16 *v, float *scores, const ScoreWs &ws,
+                           cudaStream_t s);
+cudaError_t launch_select(const DevProblem &P, const float *scores, const int32_t *budgets,
+                          const int64_t *offsets, int32_t *sel, int *status, cudaStream_t s);
+cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                           const int32_t *sel, const int64_t *offsets, long long total_rows,
+                           __nv_bfloat16 *kout, __nv_bfloat16 *vout, cudaStream_t s);
+
+__device__ inline void post_status(int *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+}  // namespace kvevict

@@ -135,6 +135,14 @@ def select(S: np.ndarray, w: int, sinks: int, b: int) -> np.ndarray:
 # --------------------------------------------------------------------------
 # per-layer budgets
 # --------------------------------------------------------------------------
+def _plain_sum(xs) -> float:
+    """Left-to-right float sum (Python's ``sum`` compensates rounding since 3.12)."""
+    acc = 0.0
+    for t in xs:
+        acc += t
+    return acc
+
+
 def largest_remainder(L: int, B: int, mult: list) -> list:
     """Integer budgets b_l close to B*m_l with sum exactly L*B.
 
@@ -166,7 +174,7 @@ def pyramid_multipliers(L: int, hi: float = 1.8, lo: float = 0.2, gamma: float =
     if L == 1:
         return [1.0]
     raw = [lo + (hi - lo) * (1.0 - l / (L - 1)) ** gamma for l in range(L)]
-    mean = sum(raw) / L
+    mean = _plain_sum(raw) / L
     return [t / mean for t in raw]
 
 
@@ -189,7 +197,7 @@ def ripple_multipliers(profile, beta: float = 2.0, gamma: float = math.inf) -> l
     wt = [math.exp(beta * t) for t in shat]
     if math.isfinite(gamma):
         wt = [min(max(t, 1.0 / gamma), gamma) for t in wt]
-    mean = sum(wt) / L
+    mean = _plain_sum(wt) / L
     return [t / mean for t in wt]
 
 

@@ -82,28 +82,65 @@ def uniform01(key: int, start: int, count: int) -> np.ndarray:
     return (words(key, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
-def normals_f32(key: int, start: int, count: int, chunk: int = 1 << 22) -> np.ndarray:
-    """Irwin-Hall(12) deviates for elements ``start .. start+count-1``, float32."""
+def _normals_chunk(key: int, start: int, count: int) -> np.ndarray:
+    e = np.arange(start, start + count, dtype=np.uint64)
+    base = e * np.uint64(3) + np.uint64(1)
+    m = np.uint64(0x0000FFFF0000FFFF)
+    acc = np.zeros(count, dtype=np.uint64)   # two 32-bit lanes of partial 16-bit sums
+    for i in range(3):
+        w = mix64((base + np.uint64(i)) * np.uint64(PHI) + np.uint64(key))
+        acc += w & m
+        w >>= np.uint64(16)
+        w &= m
+        acc += w
+    total = (acc & np.uint64(0xFFFFFFFF)) + (acc >> np.uint64(32))
+    return (total.astype(np.int64) - IH12_CENTER).astype(np.float32) * np.float32(1.0 / 65536.0)
+
+
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        import os
+        _POOL = cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+def normals_f32(key: int, start: int, count: int, chunk: int = 1 << 20) -> np.ndarray:
+    """Irwin-Hall(12) deviates for elements ``start .. start+count-1``, float32.
+
+    The sum of the twelve 16-bit fields is formed two fields at a time in the
+    32-bit halves of a uint64 (each half stays below 2**19), then folded.
+    """
     out = np.empty(count, dtype=np.float32)
-    m16 = np.uint64(0xFFFF)
-    for c0 in range(0, count, chunk):
-        c = min(chunk, count - c0)
-        e = np.arange(start + c0, start + c0 + c, dtype=np.uint64)
-        base = e * np.uint64(3) + np.uint64(1)
-        acc = np.zeros(c, dtype=np.int64)
-        for i in range(3):
-            w = mix64((base + np.uint64(i)) * np.uint64(PHI) + np.uint64(key))
-            for sh in (0, 16, 32, 48):
-                acc += ((w >> np.uint64(sh)) & m16).astype(np.int64)
-        out[c0:c0 + c] = (acc - IH12_CENTER).astype(np.float32) * np.float32(1.0 / 65536.0)
+    spans = [(c0, min(chunk, count - c0)) for c0 in range(0, count, chunk)]
+
+    def work(span):
+        c0, c = span
+        out[c0:c0 + c] = _normals_chunk(key, start + c0, c)
+
+    if len(spans) <= 1:
+        for sp in spans:
+            work(sp)
+    else:
+        list(_pool().map(work, spans))
     return out
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bits."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    b = b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))
-    return (b >> np.uint64(16)).astype(np.uint16)
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bits.
+
+    Finite inputs only (the generators never produce inf or NaN), so the
+    uint32 sum below cannot wrap."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (b >> np.uint32(16)) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += b
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

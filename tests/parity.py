@@ -1,0 +1,137 @@
+"""GPU-vs-oracle parity harness used by the ``-m gpu`` tests.
+
+Runs the CUDA path through the C ABI on a device-generated workload and
+compares, unit by unit, against the fp64 oracle run on inputs regenerated on
+the host from the same seed (no oracle input is read back from the GPU):
+
+* scores: |gpu - oracle| <= 1e-3 * oracle elementwise (relative), or
+  <= 1e-30 absolute where the oracle score is below 1e-30;
+* selection: exact equality with the oracle's selection rule applied to the
+  GPU's own scores, and equality with the oracle's selection on oracle scores
+  except for tokens within 1e-3 relative of the oracle's k-th score;
+* compaction: the packed rows equal the input rows at the GPU's indices, bit
+  for bit.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+
+import numpy as np
+
+import oracle
+import synth
+
+SCORE_RTOL = 1e-3
+SCORE_ATOL = 1e-30
+
+
+def product_budgets(kv, wl, profile=None) -> np.ndarray:
+    """int32 [req][L][H] from the library's host budget helpers."""
+    L, H = wl.num_layers, wl.num_kv_heads
+    rows = []
+    for B in wl.mean_budgets():
+        if wl.budget_policy == "uniform":
+            bl = kv.kv_budgets_uniform(L, B)
+        elif wl.budget_policy == "pyramid":
+            bl = kv.kv_budgets_pyramid(L, B, wl.pyramid_max, wl.pyramid_min)
+        else:
+            bl = kv.kv_budgets_ripple(L, B, profile, wl.ripple_beta)
+        rows.append(np.repeat(np.asarray(bl, np.int32)[:, None], H, axis=1))
+    return np.asarray(rows, dtype=np.int32)
+
+
+class GpuRun:
+    """The three C-ABI calls on one workload, results kept on the device."""
+
+    def __init__(self, kv, wl, budgets=None, dw=None):
+        import torch
+        from synth.device import DeviceWorkload
+        self.wl = wl
+        self.dw = dw or DeviceWorkload(wl)
+        self.prob = kv.Problem.for_workload(wl)
+        prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
+        self.profile = prof
+        if budgets is None:
+            budgets = product_budgets(kv, wl, prof)
+        self.budgets = budgets
+        self.bufs = kv.Buffers(self.prob, budgets)
+        kv.evict(self.prob, self.dw.q, self.dw.k, self.dw.v, self.bufs)
+        torch.cuda.synchronize()
+        self.status_score = kv.kv_check_status(self.bufs.score_ws)
+        self.status_select = kv.kv_check_status(self.bufs.select_ws)
+
+    def unit_results(self, r, l, h):
+        wl, b = self.wl, self.bufs
+        cu = self.dw.cu_host
+        u = wl.unit_index(r, l, h)
+        n = int(cu[r + 1] - cu[r])
+        scores = b.scores[l, h, int(cu[r]):int(cu[r + 1])].cpu().numpy()
+        o0, o1 = int(b.offsets_host[u]), int(b.offsets_host[u + 1])
+        sel = b.sel[o0:o1].cpu().numpy()
+        kout = b.k_out[o0:o1].cpu().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+        vout = b.v_out[o0:o1].cpu().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+        return n, scores, sel, kout, vout, int(self.budgets.reshape(-1)[u])
+
+
+def oracle_unit(wl, dw, r, l, h):
+    q, k, v = dw.unit_host(r, l, h)
+    S = oracle.unit_scores(q, k, v, wl.group, wl.window)
+    return q, k, v, S
+
+
+def check_unit(run: GpuRun, r, l, h, oracle_out=None):
+    """Asserts parity of one unit; returns a small dict of error figures."""
+    wl = run.wl
+    n, g_scores, g_sel, kout, vout, b = run.unit_results(r, l, h)
+    q, k, v, S = oracle_out if oracle_out is not None else oracle_unit(wl, run.dw, r, l, h)
+    # scores
+    big = S >= SCORE_ATOL
+    rel = np.abs(g_scores[big].astype(np.float64) - S[big]) / S[big]
+    assert np.all(np.isfinite(g_scores)), "non-finite GPU score"
+    max_rel = float(rel.max()) if rel.size else 0.0
+    assert max_rel <= SCORE_RTOL, "unit (%d,%d,%d): score rel err %.3g" % (r, l, h, max_rel)
+    assert np.all(np.abs(g_scores[~big].astype(np.float64) - S[~big]) <= SCORE_ATOL)
+    # selection: the GPU's rule on its own scores is exact
+    mine = oracle.select(g_scores.astype(np.float64), wl.window, wl.num_sinks, b)
+    np.testing.assert_array_equal(g_sel, mine, err_msg="selection rule on GPU scores")
+    # selection vs oracle scores, within the tie band
+    ref = oracle.select(S, wl.window, wl.num_sinks, b)
+    diff = set(ref.tolist()) ^ set(g_sel.tolist())
+    take = b - wl.num_sinks - wl.window
+    if diff:
+        assert take > 0
+        mid = np.arange(wl.num_sinks, n - wl.window)
+        order = mid[np.lexsort((mid, -S[mid]))]
+        theta = S[order[take - 1]]
+        for j in diff:
+            assert abs(S[j] - theta) <= SCORE_RTOL * theta, \
+                "unit (%d,%d,%d): token %d outside the tie band" % (r, l, h, j)
+    # compaction: bit copy of the GPU's own indices
+    np.testing.assert_array_equal(kout, k[g_sel])
+    np.testing.assert_array_equal(vout, v[g_sel])
+    return {"max_rel": max_rel, "swapped": len(diff) // 2}
+
+
+def check_units(run: GpuRun, units, threads=None):
+    """Oracle for several units in parallel threads (ctypes releases the GIL)."""
+    wl = run.wl
+    threads = threads or min(len(units), os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = {u: ex.submit(oracle_unit, wl, run.dw, *wl.unit_coords(u)) for u in units}
+        out = {}
+        for u in units:
+            out[u] = check_unit(run, *wl.unit_coords(u), oracle_out=futs[u].result())
+    return out
+
+
+def sample_units(wl, count, seed=1234):
+    u = synth.uniform01(synth.stream_key(seed, 99), 0, 4 * count)
+    picks = []
+    for x in u:
+        c = int(x * wl.num_units)
+        if c not in picks:
+            picks.append(c)
+        if len(picks) == count:
+            break
+    return picks

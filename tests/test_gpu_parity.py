@@ -1,0 +1,131 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small workloads are checked on every unit; the full-size configurations on a
+seeded sample of units, in the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cuda_lib, wl, **kw):
+    run = parity.GpuRun(cuda_lib, wl, **kw)
+    assert run.status_score == 0 and run.status_select == 0
+    return run
+
+
+def test_device_generator_matches_host(cuda_lib):
+    import torch
+    from synth.device import DeviceWorkload
+    wl = synth.small_variant(synth.RAGGED_MISTRAL, 0, requests=[3000, 4100])
+    dw = DeviceWorkload(wl)
+    for (r, l, h) in [(0, 0, 0), (1, 1, 1), (1, 0, 1)]:
+        _, k, v = dw.unit_host(r, l, h)
+        c0, c1 = int(dw.cu_host[r]), int(dw.cu_host[r + 1])
+        kd = dw.k[l, h, c0:c1].cpu().view(torch.int16).numpy().view(np.uint16)
+        vd = dw.v[l, h, c0:c1].cpu().view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(kd, k)
+        np.testing.assert_array_equal(vd, v)
+
+
+def test_product_budgets_equal_oracle_budgets(cuda_lib):
+    for wl in synth.CONFIGS:
+        prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
+        np.testing.assert_array_equal(parity.product_budgets(cuda_lib, wl, prof),
+                                      oracle.segment_budgets(wl, prof))
+
+
+@pytest.mark.parametrize("wl", [
+    synth.TINY,
+    synth.small_variant(synth.LLAMA8B_32K, 4999),
+    synth.small_variant(synth.LONG_128K, 3333),
+    synth.small_variant(synth.QWEN7B_128K, 2500, kv_heads=1),
+    synth.small_variant(synth.RAGGED_MISTRAL, 0, requests=[1500, 4097, 2222]),
+], ids=lambda w: w.name)
+def test_small_workloads_all_units(cuda_lib, wl):
+    run = _run(cuda_lib, wl)
+    res = parity.check_units(run, list(range(wl.num_units)))
+    assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
+
+
+def test_head_dim_64_many_splits(cuda_lib):
+    wl = synth.TINY.scaled(name="d64_n40000", lengths=(40000,), num_kv_heads=2, num_q_heads=6,
+                           window=8, budget_tokens=1000)
+    run = _run(cuda_lib, wl)
+    parity.check_units(run, list(range(wl.num_units)))
+
+
+@pytest.mark.parametrize("b_kind", ["minimum", "everything"])
+def test_budget_extremes(cuda_lib, b_kind):
+    wl = synth.small_variant(synth.LLAMA8B_32K, 700, layers=1)
+    n = 700
+    b = wl.num_sinks + wl.window if b_kind == "minimum" else n
+    budgets = np.full((1, wl.num_layers, wl.num_kv_heads), b, dtype=np.int32)
+    run = _run(cuda_lib, wl, budgets=budgets)
+    parity.check_units(run, list(range(wl.num_units)))
+
+
+def test_shortest_request_window_plus_sinks(cuda_lib):
+    """n = sinks + w: no middle candidates; every token kept."""
+    wl = synth.small_variant(synth.RAGGED_MISTRAL, 0, requests=[36, 1200], layers=1)
+    budgets = np.zeros((2, 1, wl.num_kv_heads), dtype=np.int32)
+    budgets[0] = 36
+    budgets[1] = 300
+    wl = wl.scaled(num_heavy=0)
+    run = _run(cuda_lib, wl, budgets=budgets)
+    parity.check_units(run, list(range(wl.num_units)))
+
+
+def test_equal_scores_break_ties_to_lower_index(cuda_lib):
+    """Identical K/V rows give bit-identical GPU scores; the lower index must win."""
+    import torch
+    from synth.device import DeviceWorkload
+    wl = synth.small_variant(synth.LLAMA8B_32K, 900, layers=1, kv_heads=1).scaled(num_heavy=0)
+    dw = DeviceWorkload(wl)
+    dw.k[0, 0, 100:900 - wl.window] = dw.k[0, 0, 100]
+    dw.v[0, 0, 100:900 - wl.window] = dw.v[0, 0, 100]
+    budgets = np.full((1, 1, 1), 200, dtype=np.int32)
+    run = parity.GpuRun(cuda_lib, wl, budgets=budgets, dw=dw)
+    n, scores, sel, _, _, b = run.unit_results(0, 0, 0)
+    mine = oracle.select(scores.astype(np.float64), wl.window, wl.num_sinks, b)
+    np.testing.assert_array_equal(sel, mine)
+    tied = scores[100:n - wl.window]
+    assert np.all(tied == tied[0])
+
+
+def test_bad_device_budget_posts_status(cuda_lib):
+    import torch
+    kv = cuda_lib
+    wl = synth.small_variant(synth.LLAMA8B_32K, 600, layers=1, kv_heads=1)
+    from synth.device import DeviceWorkload
+    dw = DeviceWorkload(wl)
+    prob = kv.Problem.for_workload(wl)
+    good = np.full((1, 1, 1), 100, dtype=np.int32)
+    bufs = kv.Buffers(prob, good)
+    kv.kv_score(prob, dw.q, dw.k, dw.v, bufs.scores, bufs.score_ws)
+    bufs.budgets.fill_(7)   # below sinks + window, and disagrees with offsets
+    kv.kv_select_topk(prob, bufs.scores, bufs.budgets, bufs.offsets, bufs.sel, bufs.select_ws)
+    assert kv.kv_check_status(bufs.select_ws) == kv.KV_ERR_BUDGET
+    assert kv.kv_check_status(bufs.select_ws) == 0   # cleared
+
+
+@pytest.mark.parametrize("wl,count", [(synth.LLAMA8B_32K, 3), (synth.LONG_128K, 2),
+                                      (synth.QWEN7B_128K, 2), (synth.RAGGED_MISTRAL, 3)],
+                         ids=lambda x: getattr(x, "name", str(x)))
+def test_full_size_sampled_units(cuda_lib, wl, count):
+    import torch
+    run = _run(cuda_lib, wl)
+    parity.check_units(run, parity.sample_units(wl, count))
+    # properties that hold on every unit at any size
+    b = run.bufs
+    sel = b.sel[: b.total_rows]
+    seg_len = torch.diff(b.offsets)
+    assert int(seg_len.min()) >= wl.num_sinks + wl.window
+    assert bool(torch.isfinite(b.scores).all()) and float(b.scores.min()) >= 0.0
+    del run
+    torch.cuda.empty_cache()

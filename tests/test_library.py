@@ -1,0 +1,102 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every declared
+symbol, and its host-side logic (argument checks, offsets, budgets) behaves.
+No kernel is launched here."""
+import ctypes
+import math
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+@pytest.fixture(scope="module")
+def kv():
+    import kv_cache_eviction_split_gb300 as kv
+    kv.build()
+    kv.load()
+    return kv
+
+
+def _declared_functions():
+    src = open(__import__("os").path.join(__import__("os").path.dirname(__file__), "..",
+                                          "include", "kvevict.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(kv):
+    declared = _declared_functions()
+    assert len(declared) >= 12
+    lib = kv.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(kv.EXPORTED_SYMBOLS) == declared
+
+
+def _prob(kv, **kw):
+    args = dict(lengths=[1000, 2000], num_layers=2, num_kv_heads=2, num_q_heads=8, head_dim=128,
+                window=32, num_sinks=4, device="cpu")
+    args.update(kw)
+    return kv.Problem(**args)
+
+
+def test_workspace_size_and_shape_checks(kv):
+    assert kv.kv_score_workspace_size(_prob(kv)) > 0
+    assert kv.kv_select_workspace_size(_prob(kv)) >= 4
+    for bad, code in [(dict(head_dim=96), kv.KV_ERR_UNSUPPORTED),
+                      (dict(num_q_heads=7), kv.KV_ERR_INVALID_ARG),
+                      (dict(window=0), kv.KV_ERR_INVALID_ARG),
+                      (dict(lengths=[20, 2000]), kv.KV_ERR_INVALID_ARG),
+                      (dict(num_q_heads=2 * 17, window=32), kv.KV_ERR_UNSUPPORTED)]:
+        with pytest.raises(kv.KvError) as e:
+            kv.kv_score_workspace_size(_prob(kv, **bad))
+        assert e.value.code == code, bad
+
+
+def test_score_argument_checks_before_launch(kv):
+    lib = kv.load()
+    p = _prob(kv)
+    ws = kv.kv_score_workspace_size(p)
+    fake = 1 << 20  # never dereferenced: the checks fail first
+    assert lib.kv_score(p.c, None, fake, fake, fake, fake, ws, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_score(p.c, fake + 4, fake, fake, fake, fake, ws, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_score(p.c, fake, fake, fake, fake, fake, ws - 1, None) == kv.KV_ERR_WORKSPACE
+    assert lib.kv_select_topk(p.c, fake, fake, fake, fake, fake, 3, None) == kv.KV_ERR_WORKSPACE
+    assert lib.kv_compact(p.c, fake, fake, fake, fake, -1, fake, fake, None) == kv.KV_ERR_INVALID_ARG
+    empty = _prob(kv, lengths=[])
+    assert lib.kv_score(empty.c, None, None, None, None, None, 0, None) == kv.KV_OK
+    assert lib.kv_compact(empty.c, None, None, None, None, 0, None, None, None) == kv.KV_OK
+
+
+def test_make_offsets(kv):
+    p = _prob(kv)
+    b = np.array([36, 40, 100, 1000, 36, 2000, 37, 50], np.int32)
+    np.testing.assert_array_equal(kv.kv_make_offsets(p, b), oracle.offsets(b))
+    for bad in (35, 1001):
+        b2 = b.copy()
+        b2[3] = bad
+        with pytest.raises(kv.KvError) as e:
+            kv.kv_make_offsets(p, b2)
+        assert e.value.code == kv.KV_ERR_BUDGET
+
+
+@pytest.mark.parametrize("L,B", [(32, 13107), (28, 6553), (1, 256), (2, 100), (80, 999), (5, 3)])
+def test_budget_helpers_equal_oracle(kv, L, B):
+    prof = synth.ripple_profile(synth.QWEN7B_128K.scaled(num_layers=L))
+    np.testing.assert_array_equal(kv.kv_budgets_pyramid(L, B), oracle.budgets_pyramid(L, B))
+    np.testing.assert_array_equal(kv.kv_budgets_pyramid(L, B, 2.0, 0.25, 0.8),
+                                  oracle.budgets_pyramid(L, B, 2.0, 0.25, 0.8))
+    for beta, gamma in [(2.0, math.inf), (math.log(1.5), math.inf), (3.0, 4.0)]:
+        np.testing.assert_array_equal(kv.kv_budgets_ripple(L, B, prof, beta, gamma),
+                                      oracle.budgets_ripple(L, B, prof, beta, gamma))
+
+
+def test_config_budgets_equal_oracle(kv):
+    from tests import parity
+    for wl in synth.CONFIGS:
+        prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
+        np.testing.assert_array_equal(parity.product_budgets(kv, wl, prof),
+                                      oracle.segment_budgets(wl, prof))
