@@ -37,6 +37,7 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
     P->sinks = p->num_sinks;
     P->rows = (int)(G * p->window);
     P->cu = reinterpret_cast<const long long *>(p->seq_offsets_dev);
+    P->host_cu = reinterpret_cast<const long long *>(p->seq_offsets_host);
     P->scale_log2 = p->softmax_scale * 1.4426950408889634f;
     P->units = (long long)P->R * P->L * P->H;
     P->max_n = 0;
@@ -72,12 +73,20 @@ ScoreWs score_ws_layout(const DevProblem &P, void *base) {
         return p;
     };
     const size_t U = (size_t)P.units, S = (size_t)P.max_splits, Rr = (size_t)P.rows, D = P.d;
+    ws.chunks = (P.rows + 127) / 128;
+    ws.a_rows = ws.chunks * 128;
+    const size_t AR = (size_t)ws.a_rows;
     ws.status = reinterpret_cast<int *>(take(kHeaderBytes));
     ws.part_ml = reinterpret_cast<float2 *>(take(U * S * Rr * sizeof(float2)));
     ws.part_o = reinterpret_cast<float *>(take(U * S * Rr * D * sizeof(float)));
     ws.stat_ml = reinterpret_cast<float2 *>(take(U * Rr * sizeof(float2)));
     ws.stat_a2 = reinterpret_cast<float *>(take(U * Rr * sizeof(float)));
-    ws.a_hat = reinterpret_cast<__nv_bfloat16 *>(take(U * Rr * D * sizeof(__nv_bfloat16)));
+    ws.a_hi = reinterpret_cast<__nv_bfloat16 *>(take(U * AR * D * sizeof(__nv_bfloat16)));
+    ws.a_lo = reinterpret_cast<__nv_bfloat16 *>(take(U * AR * D * sizeof(__nv_bfloat16)));
+    ws.plan = reinterpret_cast<int32_t *>(take((U + 1) * sizeof(int32_t)));
+    const size_t keys = (size_t)P.L * P.H * (size_t)P.N_tot;
+    ws.part_scores = reinterpret_cast<float *>(
+        take(ws.chunks > 1 ? (size_t)ws.chunks * keys * sizeof(float) : 0));
     ws.total = off;
     return ws;
 }

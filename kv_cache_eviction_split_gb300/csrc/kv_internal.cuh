@@ -27,6 +27,7 @@ struct DevProblem {
     long long N_tot;          // packed tokens
     long long units;          // R * L * H
     const long long *cu;      // device cu_seqlens [R + 1]
+    const long long *host_cu; // host copy (host code only; never read on the device)
     float scale_log2;         // softmax_scale * log2(e)
 };
 
@@ -56,8 +57,13 @@ struct ScoreWs {
     float2 *part_ml;          // [units][max_splits][rows]  (m in log2 units, l)
     float *part_o;            // [units][max_splits][rows][d]
     float2 *stat_ml;          // [units][rows]  merged (m, l)
-    float *stat_a2;           // [units][rows]  ||a_hat||^2
-    __nv_bfloat16 *a_hat;     // [units][rows][d]
+    float *stat_a2;           // [units][rows]  ||a_hi + a_lo||^2
+    __nv_bfloat16 *a_hi;      // [units][a_rows][d]  bf16(a)
+    __nv_bfloat16 *a_lo;      // [units][a_rows][d]  bf16(a - a_hi); rows >= rows are zero
+    int32_t *plan;            // [units + 1] pass-2 work plan
+    float *part_scores;       // [chunks][L*H*N_tot] when chunks > 1
+    int a_rows;               // chunks * 128
+    int chunks;               // ceil(rows / 128)
     size_t total;
 };
 

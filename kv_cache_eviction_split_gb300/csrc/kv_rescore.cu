@@ -1,0 +1,541 @@
+// kv_rescore.cu -- pass 2 of the DropKV score on the tcgen05 tensor cores.
+//
+// For every key j of a unit and every window row r that sees it:
+//     s   = q_r . k_j                         (tensor core, fp32 in TMEM)
+//     X   = (a_hi_r + a_lo_r) . v_j           (tensor core, two bf16 MMAs)
+//     e   = 2^(s * scale * log2 e - m_r)      p = e / l_r
+//     x   = ||a_r||^2 - 2 X + ||v_j||^2      = ||a_r - v_j||^2 (the expansion the
+//                                              DropKV scoring-kernel description uses)
+//     S_j += e / (l_r - e) * sqrt(x)         = p/(1-p) * ||a_r - v_j||
+// (DropKV, Key Contributions 1 and Methodology in Plain English).  a = a_hi +
+// a_lo is the pass-1 output split into two bf16 halves, so the expansion keeps
+// ~16 bits of a instead of bf16's 8.
+//
+// Orientation is key-major: one MMA tile is 128 keys (M, TMEM lanes) by the
+// rows of a 128-row chunk of the unit's window rows (N), so each epilogue
+// thread owns one key and sums its score over rows without any cross-thread
+// reduction.  Work items = (unit, 64-key-tile block, row chunk); a persistent
+// grid walks them round-robin, chunk fastest, so the chunks of one key block
+// run on neighbouring SMs at the same time and share K/V through L2.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: the chunk's Q, a_hi, a_lo once per item; K and V
+//               tiles through a 2-stage ring
+//   warp 1      TMEM owner and MMA issuer (one thread): per tile and per half
+//               of the chunk's rows, S = K Q^T, X = V a_hi^T + V a_lo^T
+//   warps 2-9   epilogue: group g (4 warps) handles half g of the rows; group 0
+//               hands its per-key partial sums to group 1 through a smem ring
+// Every wait is bounded: on expiry the kernel posts KV_ERR_TIMEOUT, the other
+// roles drain out, TMEM is freed and the kernel returns.
+#include <algorithm>
+#include <cfloat>
+
+#include <cudaTypedefs.h>
+
+#include "kv_internal.cuh"
+#include "kv_sm100.cuh"
+
+namespace kvevict {
+namespace {
+using namespace sm100;
+
+constexpr int kTileKeys = 128;
+constexpr int kChunkRows = 128;
+constexpr int kTilesPerItem = 64;
+constexpr int kStages = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kBlockBytes = kChunkRows * 128;   // one [128 rows][64 bf16] swizzled box
+
+template <int D>
+struct Layout {
+    static constexpr int kOp = (D / 64) * kBlockBytes;     // one [128][D] bf16 operand
+    static constexpr int kQ = 0;
+    static constexpr int kAhi = kQ + kOp;
+    static constexpr int kAlo = kAhi + kOp;
+    static constexpr int kK = kAlo + kOp;
+    static constexpr int kV = kK + kStages * kOp;
+    static constexpr int kStats = kV + kStages * kOp;      // [2][64] float2 (-m, l)
+    static constexpr int kA2 = kStats + 2 * 64 * 8;        // [2][64] float ||a||^2
+    static constexpr int kRing = kA2 + 2 * 64 * 4;         // [2 slots][128] float
+    static constexpr int kBars = kRing + 2 * 128 * 4;
+    static constexpr int kNumBars = 4 * kStages + 2 + 8;
+    static constexpr int kMisc = kBars + kNumBars * 8;
+    static constexpr int kTotal = kMisc + 16;
+};
+
+struct RescoreArgs {
+    const int32_t *plan;       // [units + 1] prefix of key-tile blocks per unit
+    const float2 *stat_ml;     // [units][rows] (m in log2 units, l)
+    const float *stat_a2;      // [units][rows]
+    float *out;                // scores, or chunk partials [chunks][L*H*N_tot]
+    long long out_stride;      // elements between chunk partials
+    long long total_items;
+    int chunks;
+    int a_rows;                // rows per unit in a_hi / a_lo (chunks * 128)
+    int *status;
+};
+
+struct Item {
+    long long u;
+    int c, t_begin, t_end;
+};
+
+__device__ __forceinline__ Item decode_item(long long item, const RescoreArgs &A, const DevProblem &P) {
+    Item it;
+    it.c = (int)(item % A.chunks);
+    const long long gb = item / A.chunks;
+    long long lo = 0, hi = P.units;            // plan[lo] <= gb < plan[hi]
+    while (hi - lo > 1) {
+        const long long mid = (lo + hi) >> 1;
+        if (A.plan[mid] <= gb) lo = mid; else hi = mid;
+    }
+    it.u = lo;
+    const int n = (int)(P.cu[(int)(lo / ((long long)P.L * P.H)) + 1] -
+                        P.cu[(int)(lo / ((long long)P.L * P.H))]);
+    const int tiles = (n + kTileKeys - 1) / kTileKeys;
+    it.t_begin = (int)(gb - A.plan[lo]) * kTilesPerItem;
+    it.t_end = min(it.t_begin + kTilesPerItem, tiles);
+    return it;
+}
+
+__device__ __forceinline__ int chunk_half_rows(const DevProblem &P, int c) {
+    const int rc = min(kChunkRows, P.rows - c * kChunkRows);
+    return ((rc + 31) / 32) * 16;   // half of the chunk rows rounded up to 32
+}
+
+// ||v||^2 of one row of a swizzled [128][D] bf16 tile.
+template <int D>
+__device__ __forceinline__ float row_sqnorm(const uint8_t *tile, int row) {
+    float acc = 0.f;
+#pragma unroll
+    for (int kb = 0; kb < D / 64; ++kb) {
+        const uint8_t *base = tile + kb * kBlockBytes + row * 128;
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(base + ((c16 ^ (row & 7)) << 4));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(ws[i] << 16);
+                const float hi = __uint_as_float(ws[i] & 0xFFFF0000u);
+                acc = fmaf(lo, lo, acc);
+                acc = fmaf(hi, hi, acc);
+            }
+        }
+    }
+    return acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_ahi,
+                  const __grid_constant__ CUtensorMap tm_alo, const RescoreArgs A) {
+    using Ly = Layout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
+    uint64_t *k_full = bars, *k_empty = bars + kStages;
+    uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
+    uint64_t *qa_full = bars + 4 * kStages, *qa_empty = qa_full + 1;
+    uint64_t *tm_full = qa_empty + 1, *tm_empty = tm_full + 2;
+    uint64_t *part_full = tm_empty + 2, *part_empty = part_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
+        if (*abort_flag) post_status(A.status, KV_ERR_UNSUPPORTED);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1 + kEpiWarps);
+        }
+        mbar_init(qa_full, 1);
+        mbar_init(qa_empty, 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&tm_full[h], 1);
+            mbar_init(&tm_empty[h], 4);
+            mbar_init(&part_full[h], 4);
+            mbar_init(&part_empty[h], 4);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_ahi);
+        prefetch_tensormap(&tm_alo);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool run = *abort_flag == 0;
+
+    if (run && warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            long long tcount = 0, icount = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+                const Item it = decode_item(item, A, P);
+                const UnitInfo U = unit_info(P, it.u, P.cu);
+                ok = mbar_wait(qa_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
+                if (!ok) break;
+                mbar_arrive_expect_tx(qa_full, 3 * Ly::kOp);
+                const int qy = (int)(U.q_row0 + it.c * kChunkRows);
+                const int ay = (int)(it.u * A.a_rows + it.c * kChunkRows);
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb) {
+                    tma_load_2d(smem + Ly::kQ + kb * kBlockBytes, &tm_q, qa_full, kb * 64, qy);
+                    tma_load_2d(smem + Ly::kAhi + kb * kBlockBytes, &tm_ahi, qa_full, kb * 64, ay);
+                    tma_load_2d(smem + Ly::kAlo + kb * kBlockBytes, &tm_alo, qa_full, kb * 64, ay);
+                }
+                for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
+                    const int s = (int)(tcount % kStages);
+                    const uint32_t par = (uint32_t)((tcount / kStages) & 1) ^ 1u;
+                    const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
+                    ok = mbar_wait(&k_empty[s], par, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, &tm_k,
+                                    &k_full[s], kb * 64, ky);
+                    ok = mbar_wait(&v_empty[s], par, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, &tm_v,
+                                    &v_full[s], kb * 64, ky);
+                }
+                ++icount;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
+            // drain: every load this thread issued lands before the CTA exits
+            for (int s = 0; s < kStages; ++s) {
+                const long long uses = tcount / kStages + ((tcount % kStages) > s ? 1 : 0);
+                if (uses > 0) {
+                    const uint32_t par = (uint32_t)((uses - 1) & 1);
+                    mbar_wait(&k_full[s], par, abort_flag, kWaitNs);
+                    mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
+                }
+            }
+        }
+    } else if (run && warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            long long tcount = 0, icount = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+                const Item it = decode_item(item, A, P);
+                const int rch = chunk_half_rows(P, it.c);
+                const uint32_t idesc = idesc_bf16_f32(128, rch);
+                ok = mbar_wait(qa_full, (uint32_t)(icount & 1), abort_flag, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t q_base = smem_u32(smem + Ly::kQ);
+                const uint32_t hi_base = smem_u32(smem + Ly::kAhi);
+                const uint32_t lo_base = smem_u32(smem + Ly::kAlo);
+                for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
+                    const int s = (int)(tcount % kStages);
+                    const uint32_t par = (uint32_t)((tcount / kStages) & 1);
+                    ok = mbar_wait(&k_full[s], par, abort_flag, kWaitNs) &&
+                         mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_base = smem_u32(smem + Ly::kK + s * Ly::kOp);
+                    const uint32_t v_base = smem_u32(smem + Ly::kV + s * Ly::kOp);
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        ok = mbar_wait(&tm_empty[h], (uint32_t)(tcount & 1) ^ 1u, abort_flag,
+                                       kWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t d_s = tmem + h * 128;
+                        const uint32_t d_x = tmem + h * 128 + 64;
+                        const uint32_t boff = h * rch * 128;
+#pragma unroll
+                        for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t ko = kb * kBlockBytes + kk * 32;
+                                mma_ss(d_s, sdesc_k_sw128(k_base + ko),
+                                       sdesc_k_sw128(q_base + ko + boff), idesc, (kb | kk) != 0);
+                            }
+#pragma unroll
+                        for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t ko = kb * kBlockBytes + kk * 32;
+                                mma_ss(d_x, sdesc_k_sw128(v_base + ko),
+                                       sdesc_k_sw128(hi_base + ko + boff), idesc, (kb | kk) != 0);
+                            }
+#pragma unroll
+                        for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t ko = kb * kBlockBytes + kk * 32;
+                                mma_ss(d_x, sdesc_k_sw128(v_base + ko),
+                                       sdesc_k_sw128(lo_base + ko + boff), idesc, 1u);
+                            }
+                        mma_commit(&tm_full[h]);
+                    }
+                    mma_commit(&k_empty[s]);
+                    mma_commit(&v_empty[s]);
+                }
+                mma_commit(qa_empty);
+                ++icount;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
+        }
+    } else if (run) {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;
+        const int g = ew >> 2;                 // half of the chunk rows
+        const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+        const int key_local = quarter * 32 + lane;
+        const int tg = (ew & 3) * 32 + lane;   // thread index within the group
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        float2 *stats = reinterpret_cast<float2 *>(smem + Ly::kStats) + g * 64;
+        float *a2s = reinterpret_cast<float *>(smem + Ly::kA2) + g * 64;
+        float *ring = reinterpret_cast<float *>(smem + Ly::kRing);
+        const float cscale = P.scale_log2;
+        long long tcount = 0;
+        bool ok = true;
+        for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+            const Item it = decode_item(item, A, P);
+            const UnitInfo U = unit_info(P, it.u, P.cu);
+            const int rch = chunk_half_rows(P, it.c);
+            const int row_base = it.c * kChunkRows + g * rch;
+            asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
+            for (int rr = tg; rr < rch; rr += 128) {
+                const int row = row_base + rr;
+                if (row < P.rows) {
+                    const float2 ml = A.stat_ml[it.u * P.rows + row];
+                    stats[rr] = make_float2(-ml.x, ml.y);
+                    a2s[rr] = A.stat_a2[it.u * P.rows + row];
+                } else {
+                    stats[rr] = make_float2(-INFINITY, 1.f);
+                    a2s[rr] = 0.f;
+                }
+            }
+            asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
+            float *out = A.out + (long long)it.c * A.out_stride + U.kv_row0;
+            const int pos0 = U.n - P.w;
+            for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
+                const int s = (int)(tcount % kStages);
+                const uint32_t spar = (uint32_t)((tcount / kStages) & 1);
+                ok = mbar_wait(&tm_full[g], (uint32_t)(tcount & 1), abort_flag, kWaitNs) &&
+                     mbar_wait(&v_full[s], spar, abort_flag, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const float v2 = row_sqnorm<D>(smem + Ly::kV + s * Ly::kOp, key_local);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&v_empty[s]);
+                const int j = t * kTileKeys + key_local;
+                const bool boundary = t * kTileKeys + kTileKeys - 1 > pos0;
+                float acc = 0.f;
+                for (int cc = 0; cc < rch; cc += 16) {
+                    float sv[16], xv[16];
+                    tmem_ld16(tmem + lane_addr + g * 128 + cc, sv);
+                    tmem_ld16(tmem + lane_addr + g * 128 + 64 + cc, xv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 st = stats[cc + i];
+                        const float a2 = a2s[cc + i];
+                        const float e = ex2_approx(fmaf(sv[i], cscale, st.x));
+                        const float den = st.y - e;
+                        const float x = fmaxf(fmaf(xv[i], -2.f, a2 + v2), 0.f);
+                        const float y = fmaxf(den * den * x, FLT_MIN);
+                        float term = e * x * rsqrt_approx(y);
+                        if (boundary) {
+                            const int row = row_base + cc + i;
+                            if (j > pos0 + row % P.w) term = 0.f;
+                        }
+                        acc += term;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tm_empty[g]);
+                const int slot = (int)(tcount & 1);
+                const uint32_t rpar = (uint32_t)((tcount >> 1) & 1);
+                if (g == 0) {
+                    ok = mbar_wait(&part_empty[slot], rpar ^ 1u, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    ring[slot * 128 + key_local] = acc;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&part_full[slot]);
+                } else {
+                    ok = mbar_wait(&part_full[slot], rpar, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    const float tot = acc + ring[slot * 128 + key_local];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&part_empty[slot]);
+                    if (j < U.n) out[j] = tot;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            post_status(A.status, KV_ERR_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// plan[u] = number of 64-tile key blocks of units before u.
+__global__ void __launch_bounds__(1024) plan_kernel(DevProblem P, int32_t *plan) {
+    __shared__ int32_t warp_sums[32];
+    const long long U = P.units;
+    const long long per = (U + blockDim.x - 1) / blockDim.x;
+    const long long u0 = threadIdx.x * per, u1 = min(U, u0 + per);
+    int32_t mine = 0;
+    for (long long u = u0; u < u1; ++u) {
+        const int r = (int)(u / ((long long)P.L * P.H));
+        const int n = (int)(P.cu[r + 1] - P.cu[r]);
+        const int tiles = (n + kTileKeys - 1) / kTileKeys;
+        mine += (tiles + kTilesPerItem - 1) / kTilesPerItem;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = mine;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t t = warp_sums[lane];
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += y;
+        }
+        warp_sums[lane] = t;
+    }
+    __syncthreads();
+    int32_t run = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - mine;
+    for (long long u = u0; u < u1; ++u) {
+        plan[u] = run;
+        const int r = (int)(u / ((long long)P.L * P.H));
+        const int n = (int)(P.cu[r + 1] - P.cu[r]);
+        const int tiles = (n + kTileKeys - 1) / kTileKeys;
+        run += (tiles + kTilesPerItem - 1) / kTilesPerItem;
+    }
+    if (threadIdx.x == blockDim.x - 1) plan[U] = run;
+}
+
+// scores = sum over chunks of the chunk partials, in chunk order.
+__global__ void chunk_sum_kernel(const float *__restrict__ part, long long stride, int chunks,
+                                 float *__restrict__ out) {
+    const long long step = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < stride; i += step) {
+        float acc = part[i];
+        for (int c = 1; c < chunks; ++c) acc += part[c * stride + i];
+        out[i] = acc;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 2-D map over a row-major [rows][D] bf16 tensor; box = 128 rows x 64 columns, 128 B swizzle.
+bool make_map(CUtensorMap *m, const void *base, long long rows, int D) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                      const __nv_bfloat16 *v, float *scores, const ScoreWs &ws, cudaStream_t st) {
+    CUtensorMap mq, mk, mv, mhi, mlo;
+    const long long q_rows = (long long)P.R * P.L * P.Hq * P.w;
+    const long long kv_rows = (long long)P.L * P.H * P.N_tot;
+    const long long a_rows = P.units * ws.a_rows;
+    if (!make_map(&mq, q, q_rows, D) || !make_map(&mk, k, kv_rows, D) ||
+        !make_map(&mv, v, kv_rows, D) || !make_map(&mhi, ws.a_hi, a_rows, D) ||
+        !make_map(&mlo, ws.a_lo, a_rows, D))
+        return cudaErrorInvalidValue;
+    plan_kernel<<<1, 1024, 0, st>>>(P, ws.plan);
+    long long blocks = 0;   // total key blocks, from the host copy of the lengths
+    for (long long u = 0; u < P.units; ++u) {
+        const int r = (int)(u / ((long long)P.L * P.H));
+        const long long n = P.host_cu[r + 1] - P.host_cu[r];
+        blocks += ((n + kTileKeys - 1) / kTileKeys + kTilesPerItem - 1) / kTilesPerItem;
+    }
+    const int chunks = ws.chunks;
+    RescoreArgs A;
+    A.plan = ws.plan;
+    A.stat_ml = ws.stat_ml;
+    A.stat_a2 = ws.stat_a2;
+    A.out = chunks == 1 ? scores : ws.part_scores;
+    A.out_stride = kv_rows;
+    A.total_items = blocks * chunks;
+    A.chunks = chunks;
+    A.a_rows = ws.a_rows;
+    A.status = ws.status;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem = Layout<D>::kTotal;
+    cudaFuncSetAttribute(rescore_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const long long grid = std::min<long long>(sms, A.total_items);
+    if (grid > 0)
+        rescore_tc_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, mhi, mlo, A);
+    if (chunks > 1)
+        chunk_sum_kernel<<<sms * 8, 256, 0, st>>>(ws.part_scores, kv_rows, chunks, scores);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                           const __nv_bfloat16 *v, float *scores, const ScoreWs &ws,
+                           cudaStream_t s) {
+    return P.d == 64 ? rescore_d<64>(P, q, k, v, scores, ws, s)
+                     : rescore_d<128>(P, q, k, v, scores, ws, s);
+}
+
+}  // namespace kvevict

@@ -5,13 +5,8 @@
 // position n - w + t) runs an online softmax over the split's keys and writes
 // a partial (running max m in log2 units, sum l, unnormalised output o).  The
 // merge combines the splits with the log-sum-exp rescale and stores, per row,
-// (m, l), a_hat = bf16(o / l) and ||a_hat||^2.
-//
-// Pass 2 (rescoring): every key j recomputes its logit against every row that
-// sees it, e = 2^(s*log2e - m), the dot a_hat . v_j and ||v_j||^2, and adds
-//     e / (l - e) * sqrt(||a_hat||^2 - 2 a_hat . v_j + ||v_j||^2)
-// = p/(1-p) * ||a - v_j||  (DropKV, Key Contributions 1; the squared-norm
-// expansion is the one the DropKV scoring kernel description uses).
+// (m, l), a = o / l split into a_hi = bf16(a) and a_lo = bf16(a - a_hi), and
+// ||a_hi + a_lo||^2 -- the operands of the rescoring pass (kv_rescore.cu).
 #include <cfloat>
 
 #include "kv_internal.cuh"
@@ -21,8 +16,6 @@ namespace {
 
 constexpr int kP1Threads = 128;   // rows per pass-1 block
 constexpr int kP1Keys = 32;       // keys per pass-1 tile
-constexpr int kP2Keys = 128;      // keys per pass-2 block
-constexpr int kP2Rows = 32;       // rows staged per pass-2 round
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
 
@@ -120,7 +113,15 @@ attn_merge_kernel(DevProblem P, ScoreWs ws) {
     const long long u = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.y * 4 + warp;
-    if (row >= P.rows) return;
+    if (row >= ws.a_rows) return;
+    if (row >= P.rows) {   // padding rows of the last 128-row chunk read as zeros
+        const size_t arow = (size_t)u * ws.a_rows + row;
+        for (int c = lane; c < D; c += 32) {
+            ws.a_hi[arow * D + c] = __float2bfloat16_rn(0.f);
+            ws.a_lo[arow * D + c] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
     const UnitInfo U = unit_info(P, u, P.cu);
     const int nsplit = (U.n + kSplitKeys - 1) / kSplitKeys;
     const size_t base = (size_t)u * P.max_splits * P.rows + row;
@@ -144,12 +145,16 @@ attn_merge_kernel(DevProblem P, ScoreWs ws) {
     const float inv = 1.f / Lsum;
     float a2 = 0.f;
     const size_t srow = (size_t)u * P.rows + row;
+    const size_t arow = (size_t)u * ws.a_rows + row;
 #pragma unroll
     for (int i = 0; i < C; ++i) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(a[i] * inv);
-        ws.a_hat[srow * D + lane + 32 * i] = h;
-        const float hf = __bfloat162float(h);
-        a2 = fmaf(hf, hf, a2);
+        const float av = a[i] * inv;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(av);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(av - __bfloat162float(hi));
+        ws.a_hi[arow * D + lane + 32 * i] = hi;
+        ws.a_lo[arow * D + lane + 32 * i] = lo;
+        const float sum = __bfloat162float(hi) + __bfloat162float(lo);
+        a2 = fmaf(sum, sum, a2);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) a2 += __shfl_xor_sync(0xffffffffu, a2, off);
@@ -157,76 +162,6 @@ attn_merge_kernel(DevProblem P, ScoreWs ws) {
         ws.stat_ml[srow] = make_float2(M, Lsum);
         ws.stat_a2[srow] = a2;
     }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kP2Keys)
-rescore_kernel(DevProblem P, const __nv_bfloat16 *__restrict__ q,
-               const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
-               float *__restrict__ scores, ScoreWs ws) {
-    const long long u = blockIdx.y;
-    const UnitInfo U = unit_info(P, u, P.cu);
-    const int j0 = blockIdx.x * kP2Keys;
-    if (j0 >= U.n) return;
-
-    extern __shared__ float smem[];
-    float *KT = smem;                       // [D][kP2Keys]
-    float *VT = KT + D * kP2Keys;           // [D][kP2Keys]
-    float *Qc = VT + D * kP2Keys;           // [kP2Rows][D]
-    float *Ac = Qc + kP2Rows * D;           // [kP2Rows][D]
-    float *Rm = Ac + kP2Rows * D;           // [kP2Rows] m
-    float *Rl = Rm + kP2Rows;               // [kP2Rows] l
-    float *Ra = Rl + kP2Rows;               // [kP2Rows] ||a_hat||^2
-
-    const int tid = threadIdx.x;
-    const int j = j0 + tid;
-    for (int idx = tid; idx < kP2Keys * D; idx += kP2Keys) {
-        const int jj = idx / D, c = idx % D;
-        const int key = j0 + jj;
-        const bool ok = key < U.n;
-        KT[c * kP2Keys + jj] = ok ? bf(k[(U.kv_row0 + key) * D + c]) : 0.f;
-        VT[c * kP2Keys + jj] = ok ? bf(v[(U.kv_row0 + key) * D + c]) : 0.f;
-    }
-    __syncthreads();
-    float v2 = 0.f;
-    for (int c = 0; c < D; ++c) {
-        const float x = VT[c * kP2Keys + tid];
-        v2 = fmaf(x, x, v2);
-    }
-    float acc = 0.f;
-    const size_t srow0 = (size_t)u * P.rows;
-    for (int r0 = 0; r0 < P.rows; r0 += kP2Rows) {
-        const int nr = min(kP2Rows, P.rows - r0);
-        __syncthreads();
-        for (int idx = tid; idx < nr * D; idx += kP2Keys) {
-            const int rr = idx / D, c = idx % D;
-            Qc[idx] = bf(q[(U.q_row0 + r0 + rr) * D + c]);
-            Ac[idx] = bf(ws.a_hat[(srow0 + r0 + rr) * D + c]);
-        }
-        if (tid < nr) {
-            const float2 ml = ws.stat_ml[srow0 + r0 + tid];
-            Rm[tid] = ml.x;
-            Rl[tid] = ml.y;
-            Ra[tid] = ws.stat_a2[srow0 + r0 + tid];
-        }
-        __syncthreads();
-        if (j >= U.n) continue;
-        for (int rr = 0; rr < nr; ++rr) {
-            const int r = r0 + rr;
-            const int pos = U.n - P.w + (r % P.w);
-            if (j > pos) continue;
-            float s = 0.f, av = 0.f;
-            for (int c = 0; c < D; ++c) {
-                s = fmaf(Qc[rr * D + c], KT[c * kP2Keys + tid], s);
-                av = fmaf(Ac[rr * D + c], VT[c * kP2Keys + tid], av);
-            }
-            const float e = exp2f(s * P.scale_log2 - Rm[rr]);
-            const float x = fmaxf(Ra[rr] - 2.f * av + v2, 0.f);
-            const float den = fmaxf(Rl[rr] - e, FLT_MIN);
-            acc += e * sqrtf(x) / den;
-        }
-    }
-    if (j < U.n) scores[U.kv_row0 + j] = acc;
 }
 
 template <typename K>
@@ -241,18 +176,8 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     set_smem(attn_partial_kernel<D>, smem);
     dim3 g1(P.max_splits, (unsigned)P.units, (P.rows + kP1Threads - 1) / kP1Threads);
     attn_partial_kernel<D><<<g1, kP1Threads, smem, st>>>(P, q, k, v, ws);
-    dim3 g2((unsigned)P.units, (P.rows + 3) / 4);
+    dim3 g2((unsigned)P.units, (ws.a_rows + 3) / 4);
     attn_merge_kernel<D><<<g2, 128, 0, st>>>(P, ws);
-    return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                      const __nv_bfloat16 *v, float *scores, const ScoreWs &ws, cudaStream_t st) {
-    const size_t smem = sizeof(float) * (2 * D * kP2Keys + 2 * kP2Rows * D + 3 * kP2Rows);
-    set_smem(rescore_kernel<D>, smem);
-    dim3 g((P.max_n + kP2Keys - 1) / kP2Keys, (unsigned)P.units);
-    rescore_kernel<D><<<g, kP2Keys, smem, st>>>(P, q, k, v, scores, ws);
     return cudaGetLastError();
 }
 
@@ -261,13 +186,6 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
 cudaError_t launch_attention(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t s) {
     return P.d == 64 ? attention_d<64>(P, q, k, v, ws, s) : attention_d<128>(P, q, k, v, ws, s);
-}
-
-cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                           const __nv_bfloat16 *v, float *scores, const ScoreWs &ws,
-                           cudaStream_t s) {
-    return P.d == 64 ? rescore_d<64>(P, q, k, v, scores, ws, s)
-                     : rescore_d<128>(P, q, k, v, scores, ws, s);
 }
 
 }  // namespace kvevict

@@ -43,8 +43,8 @@ def test_product_budgets_equal_oracle_budgets(cuda_lib):
 @pytest.mark.parametrize("wl", [
     synth.TINY,
     synth.small_variant(synth.LLAMA8B_32K, 4999),
-    synth.small_variant(synth.LONG_128K, 3333),
-    synth.small_variant(synth.QWEN7B_128K, 2500, kv_heads=1),
+    synth.small_variant(synth.LONG_128K, 5003),
+    synth.small_variant(synth.QWEN7B_128K, 10500, kv_heads=1),
     synth.small_variant(synth.RAGGED_MISTRAL, 0, requests=[1500, 4097, 2222]),
 ], ids=lambda w: w.name)
 def test_small_workloads_all_units(cuda_lib, wl):
