@@ -161,6 +161,32 @@ kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const in
  */
 kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status);
 
+/*
+ * kv_score for callers that cannot allocate device memory.  No page these
+ * kernels follow has a counterpart: it is a deployment convenience.
+ *
+ * Same inputs, outputs, layouts and asynchrony as kv_score, but the scratch
+ * lives in one fixed 64 MiB array of device memory that belongs to this
+ * library (held by every GPU that loads it, until the process exits), so the
+ * caller passes no workspace.  It is meant for code that may not call the
+ * CUDA allocator at run time -- a process that reserves all device memory at
+ * start-up, a plugin whose host application owns the allocator, a path that
+ * must avoid cudaMalloc's implicit synchronisation.  It allocates nothing.
+ *
+ *  - Problems whose kv_score workspace (kv_score_workspace_size) exceeds
+ *    64 MiB return KV_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call shares the array and it keeps the last call's contents;
+ *    calls that overlap on the GPU (other streams or host threads on the same
+ *    device) race on it, so order them on one stream.
+ *  - Device-side status (a bounded wait that expired) is written into the
+ *    shared array and not reported; argument and launch errors are returned.
+ */
+kv_status kv_score_noalloc(const kv_problem *p, const void *q_win, const void *k,
+                           const void *v, float *scores, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *kv_status_string(kv_status s);
 

@@ -24,7 +24,7 @@ from . import _build
 
 __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attention",
            "kv_score_rescore", "kv_make_offsets", "kv_select_topk", "kv_compact",
-           "kv_check_status", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
+           "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
            "EXPORTED_SYMBOLS", "evict"]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
@@ -33,7 +33,7 @@ KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_
 EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_score_rescore", "kv_make_offsets", "kv_select_workspace_size",
                     "kv_select_topk", "kv_compact", "kv_check_status", "kv_status_string",
-                    "kv_budgets_pyramid", "kv_budgets_ripple")
+                    "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc")
 
 
 class KvError(RuntimeError):
@@ -84,6 +84,7 @@ def load(path: Optional[str] = None):
         "kv_check_status": [vp, vp, ctypes.POINTER(i32)],
         "kv_budgets_pyramid": [i32, i32, f64, f64, f64, ctypes.POINTER(i32)],
         "kv_budgets_ripple": [i32, i32, ctypes.POINTER(f64), f64, f64, ctypes.POINTER(i32)],
+        "kv_score_noalloc": [P, vp, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -195,6 +196,12 @@ def kv_score_rescore(prob, q, k, v, scores, workspace, stream=None):
     _check(load().kv_score_rescore(prob.c, _ptr(q), _ptr(k), _ptr(v), _ptr(scores),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "kv_score_rescore")
+
+
+def kv_score_noalloc(prob, q, k, v, scores, stream=None):
+    """kv_score with the library's own fixed scratch (no workspace argument)."""
+    _check(load().kv_score_noalloc(prob.c, _ptr(q), _ptr(k), _ptr(v), _ptr(scores),
+                                   _stream(stream)), "kv_score_noalloc")
 
 
 def kv_make_offsets(prob, budgets_host: np.ndarray) -> np.ndarray:
