@@ -1,0 +1,448 @@
+// kv_attention.cu -- pass 1 of the DropKV score on the tcgen05 tensor cores:
+// causal window attention over each unit's keys, split across CTAs (split-K),
+// producing per split the row max m (log2 units), the row sum l of
+// 2^(s*scale*log2 e - m) and the unnormalised output O = sum_j P_j v_j.  The
+// merge in kv_score.cu combines the splits (DropKV, "Methodology in Plain
+// English": the attention output a whose removal shift the score measures).
+//
+// Query-major, one 128-row chunk of the unit's G*w window rows per work item:
+//   S = Q K^T    M = 128 rows, N = 128 keys, K = d     (fp32 in TMEM, 2 buffers)
+//   O += P V     M = 128 rows, N = d, K = 128 keys     (fp32 in TMEM; V is the
+//                MN-major B operand, P is written by the softmax warps to
+//                swizzled shared memory as bf16)
+// The softmax warps own one row each: tile max with the causal mask, a lazy
+// rescale (O and l are rescaled only when the tile max exceeds the running
+// max by more than 2^8, so the running max may trail the true max by at most
+// 8 in log2 units -- every exponent stays <= 2^8), p = 2^(s*c - m), row sums
+// from the unrounded fp32 p.
+//
+// Barrier parities are tracked from use counts; each wait is placed where the
+// barrier cannot have run more than one phase ahead (P V of tile i-2 is known
+// done before P V of tile i-1 is waited for; the item's last P V has its own
+// barrier).
+//
+// Warp roles (192 threads): warp 0 TMA producer (Q chunk per item, K and V
+// tiles through a 2-stage ring); warp 1 TMEM owner and MMA issuer, running
+// S of tile i+1 ahead of P V of tile i; warps 2-5 softmax.  Work items are
+// (unit, 16384-key split, row chunk), chunk fastest, walked round-robin by a
+// persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
+#include <cfloat>
+
+#include "kv_internal.cuh"
+#include "kv_sm100.cuh"
+
+namespace kvevict {
+namespace {
+using namespace sm100;
+
+constexpr int kTileKeys = 128;
+constexpr int kChunkRows = 128;
+constexpr int kStages = 2;
+constexpr int kSoftWarps = 4;
+constexpr int kThreads = (2 + kSoftWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kBlockBytes = 128 * 128;       // [128 rows][64 bf16], 128 B swizzle
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D>
+struct Layout {
+    static constexpr int kOp = (D / 64) * kBlockBytes;   // [128][D] bf16
+    static constexpr int kPbuf = 2 * kBlockBytes;        // [128 rows][128 keys] bf16
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kOp;
+    static constexpr int kV = kK + kStages * kOp;
+    static constexpr int kP = kV + kStages * kOp;
+    static constexpr int kBars = kP + 2 * kPbuf;
+    static constexpr int kNumBars = 4 * kStages + 2 + 8 + 3;
+    static constexpr int kMisc = kBars + kNumBars * 8;
+    static constexpr int kTotal = kMisc + 16;
+};
+
+struct AttnArgs {
+    const int32_t *plan;       // [units + 1] prefix of key splits per unit
+    float2 *part_ml;           // [units][max_splits][rows]
+    float *part_o;             // [units][max_splits][rows][d]
+    long long total_items;
+    int chunks;
+    int *status;
+};
+
+struct Item {
+    long long u;
+    int c, split, t0, t1;
+};
+
+__device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, const DevProblem &P) {
+    Item it;
+    it.c = (int)(item % A.chunks);
+    const long long gs = item / A.chunks;
+    long long lo = 0, hi = P.units;
+    while (hi - lo > 1) {
+        const long long mid = (lo + hi) >> 1;
+        if (A.plan[mid] <= gs) lo = mid; else hi = mid;
+    }
+    it.u = lo;
+    const int r = (int)(lo / ((long long)P.L * P.H));
+    const int n = (int)(P.cu[r + 1] - P.cu[r]);
+    it.split = (int)(gs - A.plan[lo]);
+    const int k0 = it.split * kSplitKeys;
+    const int k1 = min(n, k0 + kSplitKeys);
+    it.t0 = k0 / kTileKeys;
+    it.t1 = (k1 + kTileKeys - 1) / kTileKeys;
+    return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const AttnArgs A) {
+    using Ly = Layout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
+    uint64_t *k_full = bars, *k_empty = bars + kStages;
+    uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
+    uint64_t *q_full = bars + 4 * kStages, *q_empty = q_full + 1;
+    uint64_t *s_full = q_empty + 1, *s_empty = s_full + 2;
+    uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
+    uint64_t *o_full = p_empty + 2, *o_empty = o_full + 1, *o_final = o_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
+        if (*abort_flag) post_status(A.status, KV_ERR_UNSUPPORTED);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_empty[b], kSoftWarps);
+            mbar_init(&p_full[b], kSoftWarps);
+            mbar_init(&p_empty[b], 1);
+        }
+        mbar_init(o_full, 1);
+        mbar_init(o_empty, kSoftWarps);
+        mbar_init(o_final, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool run = *abort_flag == 0;
+
+    if (run && warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            long long tcount = 0, icount = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+                const Item it = decode_item(item, A, P);
+                const UnitInfo U = unit_info(P, it.u, P.cu);
+                ok = mbar_wait(q_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
+                if (!ok) break;
+                mbar_arrive_expect_tx(q_full, Ly::kOp);
+                const int qy = (int)(U.q_row0 + it.c * kChunkRows);
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb)
+                    tma_load_2d(smem + Ly::kQ + kb * kBlockBytes, &tm_q, q_full, kb * 64, qy);
+                for (int t = it.t0; ok && t < it.t1; ++t, ++tcount) {
+                    const int s = (int)(tcount % kStages);
+                    const uint32_t par = (uint32_t)((tcount / kStages) & 1) ^ 1u;
+                    const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
+                    ok = mbar_wait(&k_empty[s], par, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, &tm_k,
+                                    &k_full[s], kb * 64, ky);
+                    ok = mbar_wait(&v_empty[s], par, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, &tm_v,
+                                    &v_full[s], kb * 64, ky);
+                }
+                ++icount;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
+            for (int s = 0; s < kStages; ++s) {
+                const long long uses = tcount / kStages + ((tcount % kStages) > s ? 1 : 0);
+                if (uses > 0) {
+                    const uint32_t par = (uint32_t)((uses - 1) & 1);
+                    mbar_wait(&k_full[s], par, abort_flag, kWaitNs);
+                    mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
+                }
+            }
+        }
+    } else if (run && warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(128, kTileKeys);
+            const uint32_t idesc_pv = idesc_bf16_f32_bmn(128, D);
+            const uint32_t q_base = smem_u32(smem + Ly::kQ);
+            long long tcount = 0, icount = 0;
+            bool ok = true;
+            // O += P V for global tile tc (the item's first tile overwrites O)
+            auto pv = [&](long long tc, bool first) {
+                const int pb = (int)(tc & 1);
+                const int s = (int)(tc % kStages);
+                if (first)
+                    ok = ok && mbar_wait(o_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
+                ok = ok && mbar_wait(&p_full[pb], (uint32_t)((tc >> 1) & 1), abort_flag, kWaitNs);
+                ok = ok && mbar_wait(&v_full[s], (uint32_t)((tc / kStages) & 1), abort_flag,
+                                     kWaitNs);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t p_base = smem_u32(smem + Ly::kP + pb * Ly::kPbuf);
+                const uint32_t v_base = smem_u32(smem + Ly::kV + s * Ly::kOp);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + kOCol, sdesc_k_sw128(p_base + kb * kBlockBytes + kk * 32),
+                               sdesc_mn_sw128(v_base + (kb * 64 + kk * 16) * 128, kBlockBytes),
+                               idesc_pv, (first && kb == 0 && kk == 0) ? 0u : 1u);
+                mma_commit(&p_empty[pb]);
+                mma_commit(&v_empty[s]);
+                mma_commit(o_full);
+            };
+            for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+                const Item it = decode_item(item, A, P);
+                const int ntiles = it.t1 - it.t0;
+                ok = mbar_wait(q_full, (uint32_t)(icount & 1), abort_flag, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const long long tc = tcount + i;
+                    const int sb = (int)(tc & 1);
+                    const int s = (int)(tc % kStages);
+                    ok = mbar_wait(&s_empty[sb], (uint32_t)((tc >> 1) & 1) ^ 1u, abort_flag,
+                                   kWaitNs) &&
+                         mbar_wait(&k_full[s], (uint32_t)((tc / kStages) & 1), abort_flag, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_base = smem_u32(smem + Ly::kK + s * Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t ko = kb * kBlockBytes + kk * 32;
+                            mma_ss(tmem + sb * kTileKeys, sdesc_k_sw128(q_base + ko),
+                                   sdesc_k_sw128(k_base + ko), idesc_s, (kb | kk) != 0);
+                        }
+                    mma_commit(&s_full[sb]);
+                    mma_commit(&k_empty[s]);
+                    if (i > 0) pv(tc - 1, i == 1);
+                }
+                if (ok && ntiles > 0) pv(tcount + ntiles - 1, ntiles == 1);
+                mma_commit(o_final);
+                mma_commit(q_empty);
+                tcount += ntiles;
+                ++icount;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
+        }
+    } else if (run) {
+        // ------------------------------------------------------------ softmax
+        const int quarter = warp & 3;
+        const int rr = quarter * 32 + lane;               // row of the chunk = TMEM lane
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const float cs = P.scale_log2;
+        long long tcount = 0, icount = 0;
+        bool ok = true;
+        for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+            const Item it = decode_item(item, A, P);
+            const UnitInfo U = unit_info(P, it.u, P.cu);
+            const int ntiles = it.t1 - it.t0;
+            const int row = it.c * kChunkRows + rr;
+            const bool row_valid = row < P.rows;
+            const int pos = U.n - P.w + (row % P.w);
+            const int pos_min = U.n - P.w;
+            float m_used = -INFINITY, l = 0.f;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const long long tc = tcount + i;
+                const int sb = (int)(tc & 1);
+                const int kt = (it.t0 + i) * kTileKeys;
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)((tc >> 1) & 1),
+                                                       abort_flag, kWaitNs));
+                if (!ok) break;
+                tc_fence_after();
+                float sv[kTileKeys];
+#pragma unroll
+                for (int c = 0; c < kTileKeys / 16; ++c) {
+                    float tmp[16];
+                    tmem_ld16(tmem + lane_addr + sb * kTileKeys + c * 16, tmp);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sv[c * 16 + j] = tmp[j];
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                // causal mask (only the tiles that reach into the window need it)
+                const bool boundary = kt + kTileKeys - 1 > pos_min;
+                const int lim = row_valid ? (boundary ? pos - kt : kTileKeys - 1) : -1;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kTileKeys; ++j)
+                    if (j <= lim) mx = fmaxf(mx, sv[j]);
+                const float m_tile = mx * cs;
+                const bool need = m_tile > m_used + kRescaleLog2;
+                const float factor = need ? ex2_approx(m_used - m_tile) : 1.f;
+                // P buffer pb is free once P V of tile tc-2 is done; waiting here first
+                // also guarantees o_full below cannot alias an older completion
+                const int pb = (int)(tc & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(&p_empty[pb], (uint32_t)((tc >> 1) & 1) ^ 1u,
+                                                       abort_flag, kWaitNs));
+                if (!ok) break;
+                if (__any_sync(0xffffffffu, need && i > 0)) {
+                    // O holds P V of earlier tiles: rescale it once P V of tile tc-1 is done
+                    ok = __all_sync(0xffffffffu, mbar_wait(o_full, (uint32_t)((tc - 1) & 1),
+                                                           abort_flag, kWaitNs));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 16; ++c) {
+                        float o[16];
+                        tmem_ld16(tmem + lane_addr + kOCol + c * 16, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) o[j] *= factor;
+                        tmem_st16(tmem + lane_addr + kOCol + c * 16, o);
+                    }
+                    tmem_st_wait();
+                }
+                if (need) {
+                    l *= factor;
+                    m_used = m_tile;
+                }
+                uint8_t *prow = smem + Ly::kP + pb * Ly::kPbuf + rr * 128;
+                float lsum = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < kTileKeys / 8; ++ch) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int j0 = ch * 8 + 2 * h;
+                        const float p0 = (j0 <= lim) ? ex2_approx(fmaf(sv[j0], cs, -m_used)) : 0.f;
+                        const float p1 =
+                            (j0 + 1 <= lim) ? ex2_approx(fmaf(sv[j0 + 1], cs, -m_used)) : 0.f;
+                        lsum += p0 + p1;
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                        w4[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    const int blk = ch >> 3, c16 = ch & 7;
+                    *reinterpret_cast<uint4 *>(prow + blk * kBlockBytes + ((c16 ^ (rr & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                l += lsum;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[pb]);
+            }
+            if (!ok) break;
+            // item end: read O once the last P V is done, write this split's partial
+            const size_t prow_idx = (((size_t)it.u * P.max_splits + it.split) * P.rows) + row;
+            if (ntiles > 0) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(o_final, (uint32_t)(icount & 1), abort_flag, kWaitNs));
+                if (!ok) break;
+                tc_fence_after();
+                float *po = A.part_o + prow_idx * D;
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    float o[16];
+                    tmem_ld16(tmem + lane_addr + kOCol + c * 16, o);
+                    tmem_ld_wait();
+                    if (row_valid) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(po + c * 16 + j) =
+                                make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty);
+            }
+            if (row_valid) A.part_ml[prow_idx] = make_float2(m_used, l);
+            tcount += ntiles;
+            ++icount;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            post_status(A.status, KV_ERR_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                        const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    const long long q_rows = (long long)P.R * P.L * P.Hq * P.w;
+    const long long kv_rows = (long long)P.L * P.H * P.N_tot;
+    if (!make_tile_map(&mq, q, q_rows, D) || !make_tile_map(&mk, k, kv_rows, D) ||
+        !make_tile_map(&mv, v, kv_rows, D))
+        return cudaErrorInvalidValue;
+    launch_plan(P, kSplitKeys, ws.plan, st);
+    AttnArgs A;
+    A.plan = ws.plan;
+    A.part_ml = ws.part_ml;
+    A.part_o = ws.part_o;
+    A.chunks = ws.chunks;
+    A.total_items = total_blocks(P, kSplitKeys) * ws.chunks;
+    A.status = ws.status;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem = Layout<D>::kTotal;
+    cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const long long grid = std::min<long long>(sms, A.total_items);
+    if (grid > 0) attn_tc_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_partials(const DevProblem &P, const __nv_bfloat16 *q,
+                                      const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                      const ScoreWs &ws, cudaStream_t s) {
+    return P.d == 64 ? attention_d<64>(P, q, k, v, ws, s) : attention_d<128>(P, q, k, v, ws, s);
+}
+
+}  // namespace kvevict

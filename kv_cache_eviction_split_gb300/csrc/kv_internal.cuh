@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -69,7 +70,18 @@ struct ScoreWs {
 
 ScoreWs score_ws_layout(const DevProblem &P, void *base);
 
+// plan[u] = sum over units u' < u of ceil(n_u' / keys_per_block); plan[units] = total.
+void launch_plan(const DevProblem &P, int keys_per_block, int32_t *plan, cudaStream_t s);
+// 2-D TMA map over a row-major [rows][D] bf16 tensor: box 128 rows x 64 columns,
+// 128-byte swizzle, out-of-range rows read as zero.  False if encoding fails.
+bool make_tile_map(CUtensorMap *m, const void *base, long long rows, int D);
+// Total blocks of ceil(n_u / keys_per_block) over all units (host, from host_cu).
+long long total_blocks(const DevProblem &P, int keys_per_block);
+
 // Launchers (return cudaGetLastError() of their launches).
+cudaError_t launch_attention_partials(const DevProblem &P, const __nv_bfloat16 *q,
+                                      const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                      const ScoreWs &ws, cudaStream_t s);
 cudaError_t launch_attention(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t s);
 cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,

@@ -30,8 +30,6 @@
 #include <algorithm>
 #include <cfloat>
 
-#include <cudaTypedefs.h>
-
 #include "kv_internal.cuh"
 #include "kv_sm100.cuh"
 
@@ -345,8 +343,9 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
                 const int s = (int)(tcount % kStages);
                 const uint32_t spar = (uint32_t)((tcount / kStages) & 1);
-                ok = mbar_wait(&tm_full[g], (uint32_t)(tcount & 1), abort_flag, kWaitNs) &&
-                     mbar_wait(&v_full[s], spar, abort_flag, kWaitNs);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&tm_full[g], (uint32_t)(tcount & 1), abort_flag, kWaitNs) &&
+                                    mbar_wait(&v_full[s], spar, abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
                 const float v2 = row_sqnorm<D>(smem + Ly::kV + s * Ly::kOp, key_local);
@@ -382,13 +381,15 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const int slot = (int)(tcount & 1);
                 const uint32_t rpar = (uint32_t)((tcount >> 1) & 1);
                 if (g == 0) {
-                    ok = mbar_wait(&part_empty[slot], rpar ^ 1u, abort_flag, kWaitNs);
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&part_empty[slot], rpar ^ 1u, abort_flag, kWaitNs));
                     if (!ok) break;
                     ring[slot * 128 + key_local] = acc;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&part_full[slot]);
                 } else {
-                    ok = mbar_wait(&part_full[slot], rpar, abort_flag, kWaitNs);
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&part_full[slot], rpar, abort_flag, kWaitNs));
                     if (!ok) break;
                     const float tot = acc + ring[slot * 128 + key_local];
                     __syncwarp();
@@ -409,47 +410,6 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// plan[u] = number of 64-tile key blocks of units before u.
-__global__ void __launch_bounds__(1024) plan_kernel(DevProblem P, int32_t *plan) {
-    __shared__ int32_t warp_sums[32];
-    const long long U = P.units;
-    const long long per = (U + blockDim.x - 1) / blockDim.x;
-    const long long u0 = threadIdx.x * per, u1 = min(U, u0 + per);
-    int32_t mine = 0;
-    for (long long u = u0; u < u1; ++u) {
-        const int r = (int)(u / ((long long)P.L * P.H));
-        const int n = (int)(P.cu[r + 1] - P.cu[r]);
-        const int tiles = (n + kTileKeys - 1) / kTileKeys;
-        mine += (tiles + kTilesPerItem - 1) / kTilesPerItem;
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int32_t incl = mine;
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int32_t t = warp_sums[lane];
-        for (int off = 1; off < 32; off <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, t, off);
-            if (lane >= off) t += y;
-        }
-        warp_sums[lane] = t;
-    }
-    __syncthreads();
-    int32_t run = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - mine;
-    for (long long u = u0; u < u1; ++u) {
-        plan[u] = run;
-        const int r = (int)(u / ((long long)P.L * P.H));
-        const int n = (int)(P.cu[r + 1] - P.cu[r]);
-        const int tiles = (n + kTileKeys - 1) / kTileKeys;
-        run += (tiles + kTilesPerItem - 1) / kTilesPerItem;
-    }
-    if (threadIdx.x == blockDim.x - 1) plan[U] = run;
-}
-
 // scores = sum over chunks of the chunk partials, in chunk order.
 __global__ void chunk_sum_kernel(const float *__restrict__ part, long long stride, int chunks,
                                  float *__restrict__ out) {
@@ -461,32 +421,6 @@ __global__ void chunk_sum_kernel(const float *__restrict__ part, long long strid
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-// 2-D map over a row-major [rows][D] bf16 tensor; box = 128 rows x 64 columns, 128 B swizzle.
-bool make_map(CUtensorMap *m, const void *base, long long rows, int D) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                       const __nv_bfloat16 *v, float *scores, const ScoreWs &ws, cudaStream_t st) {
@@ -494,17 +428,12 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
     const long long q_rows = (long long)P.R * P.L * P.Hq * P.w;
     const long long kv_rows = (long long)P.L * P.H * P.N_tot;
     const long long a_rows = P.units * ws.a_rows;
-    if (!make_map(&mq, q, q_rows, D) || !make_map(&mk, k, kv_rows, D) ||
-        !make_map(&mv, v, kv_rows, D) || !make_map(&mhi, ws.a_hi, a_rows, D) ||
-        !make_map(&mlo, ws.a_lo, a_rows, D))
+    if (!make_tile_map(&mq, q, q_rows, D) || !make_tile_map(&mk, k, kv_rows, D) ||
+        !make_tile_map(&mv, v, kv_rows, D) || !make_tile_map(&mhi, ws.a_hi, a_rows, D) ||
+        !make_tile_map(&mlo, ws.a_lo, a_rows, D))
         return cudaErrorInvalidValue;
-    plan_kernel<<<1, 1024, 0, st>>>(P, ws.plan);
-    long long blocks = 0;   // total key blocks, from the host copy of the lengths
-    for (long long u = 0; u < P.units; ++u) {
-        const int r = (int)(u / ((long long)P.L * P.H));
-        const long long n = P.host_cu[r + 1] - P.host_cu[r];
-        blocks += ((n + kTileKeys - 1) / kTileKeys + kTilesPerItem - 1) / kTilesPerItem;
-    }
+    launch_plan(P, kTileKeys * kTilesPerItem, ws.plan, st);
+    const long long blocks = total_blocks(P, kTileKeys * kTilesPerItem);
     const int chunks = ws.chunks;
     RescoreArgs A;
     A.plan = ws.plan;

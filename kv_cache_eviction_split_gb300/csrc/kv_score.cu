@@ -1,8 +1,8 @@
-// kv_score.cu -- the two streaming passes of the DropKV removal score.
+// kv_score.cu -- the split-K merge between the two streaming passes of the
+// DropKV removal score.
 //
-// Pass 1 (window attention, split-K): for every unit and every split of its
-// keys, each window row (query head g of the GQA group, window slot t, causal
-// position n - w + t) runs an online softmax over the split's keys and writes
+// Pass 1 (kv_attention.cu) leaves, for every unit, split of its keys and window
+// row (query head g of the GQA group, window slot t, causal position n - w + t),
 // a partial (running max m in log2 units, sum l, unnormalised output o).  The
 // merge combines the splits with the log-sum-exp rescale and stores, per row,
 // (m, l), a = o / l split into a_hi = bf16(a) and a_lo = bf16(a - a_hi), and
@@ -13,99 +13,6 @@
 
 namespace kvevict {
 namespace {
-
-constexpr int kP1Threads = 128;   // rows per pass-1 block
-constexpr int kP1Keys = 32;       // keys per pass-1 tile
-
-__device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
-
-template <int D>
-__global__ void __launch_bounds__(kP1Threads)
-attn_partial_kernel(DevProblem P, const __nv_bfloat16 *__restrict__ q,
-                    const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
-                    ScoreWs ws) {
-    const int split = blockIdx.x;
-    const long long u = blockIdx.y;
-    const int chunk = blockIdx.z;
-    const UnitInfo U = unit_info(P, u, P.cu);
-    const int nsplit = (U.n + kSplitKeys - 1) / kSplitKeys;
-    if (split >= nsplit) return;
-    const int k_begin = split * kSplitKeys;
-    const int k_end = min(U.n, k_begin + kSplitKeys);
-
-    extern __shared__ float smem[];
-    float *qT = smem;                     // [D][kP1Threads]
-    float *Ks = qT + D * kP1Threads;      // [kP1Keys][D]
-    float *Vs = Ks + kP1Keys * D;         // [kP1Keys][D]
-
-    const int tid = threadIdx.x;
-    const int row = chunk * kP1Threads + tid;
-    const bool active = row < P.rows;
-    const int pos = U.n - P.w + (row % P.w);
-
-    for (int idx = tid; idx < kP1Threads * D; idx += kP1Threads) {
-        const int rr = idx / D, c = idx % D;
-        const int grow = chunk * kP1Threads + rr;
-        qT[c * kP1Threads + rr] = grow < P.rows ? bf(q[(U.q_row0 + grow) * D + c]) : 0.f;
-    }
-
-    float o[D];
-#pragma unroll
-    for (int c = 0; c < D; ++c) o[c] = 0.f;
-    float m = -INFINITY, l = 0.f;
-
-    for (int t0 = k_begin; t0 < k_end; t0 += kP1Keys) {
-        __syncthreads();
-        for (int idx = tid; idx < kP1Keys * D; idx += kP1Threads) {
-            const int jj = idx / D, c = idx % D;
-            const int key = t0 + jj;
-            const bool ok = key < k_end;
-            Ks[idx] = ok ? bf(k[(U.kv_row0 + key) * D + c]) : 0.f;
-            Vs[idx] = ok ? bf(v[(U.kv_row0 + key) * D + c]) : 0.f;
-        }
-        __syncthreads();
-        if (!active || t0 > pos) continue;
-
-        float s[kP1Keys];
-#pragma unroll
-        for (int j = 0; j < kP1Keys; ++j) s[j] = 0.f;
-        for (int c = 0; c < D; ++c) {
-            const float qc = qT[c * kP1Threads + tid];
-#pragma unroll
-            for (int j = 0; j < kP1Keys; ++j) s[j] = fmaf(qc, Ks[j * D + c], s[j]);
-        }
-        float mt = m;
-#pragma unroll
-        for (int j = 0; j < kP1Keys; ++j) {
-            const int key = t0 + j;
-            s[j] = (key < k_end && key <= pos) ? s[j] * P.scale_log2 : -INFINITY;
-            mt = fmaxf(mt, s[j]);
-        }
-        const float corr = exp2f(m - mt);
-        l *= corr;
-#pragma unroll
-        for (int c = 0; c < D; ++c) o[c] *= corr;
-#pragma unroll
-        for (int j = 0; j < kP1Keys; ++j) {
-            s[j] = exp2f(s[j] - mt);
-            l += s[j];
-        }
-#pragma unroll
-        for (int c = 0; c < D; ++c) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < kP1Keys; ++j) acc = fmaf(s[j], Vs[j * D + c], acc);
-            o[c] += acc;
-        }
-        m = mt;
-    }
-    if (!active) return;
-    const size_t prow = ((size_t)u * P.max_splits + split) * P.rows + row;
-    ws.part_ml[prow] = make_float2(m, l);
-    float *po = ws.part_o + prow * D;
-#pragma unroll
-    for (int c = 0; c < D; ++c) po[c] = o[c];
-}
 
 template <int D>
 __global__ void __launch_bounds__(128)
@@ -164,20 +71,10 @@ attn_merge_kernel(DevProblem P, ScoreWs ws) {
     }
 }
 
-template <typename K>
-void set_smem(K kernel, size_t bytes) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 template <int D>
-cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                        const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t st) {
-    const size_t smem = sizeof(float) * (D * kP1Threads + 2 * kP1Keys * D);
-    set_smem(attn_partial_kernel<D>, smem);
-    dim3 g1(P.max_splits, (unsigned)P.units, (P.rows + kP1Threads - 1) / kP1Threads);
-    attn_partial_kernel<D><<<g1, kP1Threads, smem, st>>>(P, q, k, v, ws);
-    dim3 g2((unsigned)P.units, (ws.a_rows + 3) / 4);
-    attn_merge_kernel<D><<<g2, 128, 0, st>>>(P, ws);
+cudaError_t merge_d(const DevProblem &P, const ScoreWs &ws, cudaStream_t st) {
+    dim3 g((unsigned)P.units, (ws.a_rows + 3) / 4);
+    attn_merge_kernel<D><<<g, 128, 0, st>>>(P, ws);
     return cudaGetLastError();
 }
 
@@ -185,7 +82,9 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
 
 cudaError_t launch_attention(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t s) {
-    return P.d == 64 ? attention_d<64>(P, q, k, v, ws, s) : attention_d<128>(P, q, k, v, ws, s);
+    cudaError_t e = launch_attention_partials(P, q, k, v, ws, s);
+    if (e != cudaSuccess) return e;
+    return P.d == 64 ? merge_d<64>(P, ws, s) : merge_d<128>(P, ws, s);
 }
 
 }  // namespace kvevict

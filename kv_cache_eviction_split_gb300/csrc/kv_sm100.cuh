@@ -146,6 +146,27 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "r"(taddr));
 }
 
+// Stores 16 consecutive 32-bit columns for the warp's 32 lanes (inverse of tmem_ld16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (the tensor core reading them as an MMA operand).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -165,6 +186,22 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t addr) {
     return d;
 }
 
+// Shared-memory matrix descriptor, MN-major operand in the 128-byte swizzle
+// layout: 64 elements (128 B) contiguous along M/N per row, rows along K 128 B
+// apart in 8-row atoms of 1024 B (stride byte offset), and successive 64-wide
+// M/N blocks `mn_block_bytes` apart (leading byte offset).  This is how a
+// [K rows][N] tile loaded by TMA (128 B inner box, 128 B swizzle) looks when
+// N is the contiguous dimension, e.g. V[keys][d] as the B operand of P V.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t addr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an
 // fp32 accumulator, for an M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
@@ -173,6 +210,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | (1u << 10)                                 // B: bf16
            | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
+}
+
+// Same with the B operand MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+    return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
