@@ -44,7 +44,8 @@ ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (0: enough for about 2 s of timed work, at least 20)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -236,11 +237,13 @@ def run_reference(args, wl, budgets):
 # Kernels of one step and how many launches each makes (the timed region
 # launches only these).  The score passes run on the CUDA cores in fp32.
 STAGES = ["attention", "rescore", "select", "compact"]
-LAUNCHES_PER_STEP = {"attention": 2, "rescore": 1, "select": 1, "compact": 1}
-STAGE_KERNELS = {"attention": "attn_partial_kernel+attn_merge_kernel",
-                 "rescore": "rescore_kernel", "select": "select_kernel",
-                 "compact": "compact_kernel"}
-SCORE_ENGINE = "alu"
+# attention: plan_kernel, attn_tc_kernel, attn_merge_kernel; rescore: plan_kernel,
+# rescore_tc_kernel and, when the window rows span more than one 128-row chunk,
+# chunk_sum_kernel.
+LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "select": 1, "compact": 1}
+STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
+                 "select": "select_kernel", "compact": "compact_kernel"}
+SCORE_ENGINE = "tensor"
 # DRAM bytes per launch from an ncu capture of the current kernels (None: not taken)
 TRAFFIC = {}
 
@@ -353,9 +356,13 @@ def main(argv=None):
 
     sampler = ClockSampler(gpu_uuid(torch, dev))
     sampler.start()
+    t_w0 = time.perf_counter()
     for _ in range(max(args.warmup, 0)):
         step()
     barrier()
+    if args.steps <= 0:
+        per = (time.perf_counter() - t_w0) / max(args.warmup, 1)
+        args.steps = int(min(2000, max(20, math.ceil(2.0 / max(per, 1e-4)))))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -406,7 +413,8 @@ def main(argv=None):
                     "peak_source": peak_src},
             "stages_ms": stage_ms,
             "roofline": roof,
-            "gpu_launches": args.steps * sum(LAUNCHES_PER_STEP.values()),
+            "gpu_launches": args.steps * (sum(LAUNCHES_PER_STEP.values())
+                                          + (1 if wl.rows > 128 else 0)),
             "clocks": clocks}
 
     if not args.no_e2e:

@@ -8,18 +8,22 @@
 // Query-major, one 128-row chunk of the unit's G*w window rows per work item:
 //   S = Q K^T    M = 128 rows, N = 128 keys, K = d     (fp32 in TMEM, 2 buffers)
 //   O += P V     M = 128 rows, N = d, K = 128 keys     (fp32 in TMEM; V is the
-//                MN-major B operand, P is written by the softmax warps to
-//                swizzled shared memory as bf16)
+//                MN-major B operand; the softmax warps write P to swizzled
+//                shared memory as two bf16 halves P_hi = bf16(p) and
+//                P_lo = bf16(p - P_hi), and O accumulates P_hi V + P_lo V)
+// A single bf16 P leaves a with ~2^-9 relative error, which the rescoring
+// expansion amplifies where a is close to a value row (short requests,
+// concentrated attention); the split keeps ~16 bits of p.
 // The softmax warps own one row each: tile max with the causal mask, a lazy
 // rescale (O and l are rescaled only when the tile max exceeds the running
 // max by more than 2^8, so the running max may trail the true max by at most
 // 8 in log2 units -- every exponent stays <= 2^8), p = 2^(s*c - m), row sums
 // from the unrounded fp32 p.
 //
-// Barrier parities are tracked from use counts; each wait is placed where the
-// barrier cannot have run more than one phase ahead (P V of tile i-2 is known
-// done before P V of tile i-1 is waited for; the item's last P V has its own
-// barrier).
+// Barrier parities are tracked from use counts; no barrier can run more than
+// one phase ahead of its waiter.  The P buffer is single: the softmax warps
+// write P of tile i only after P V of tile i-1 is done, which is also the
+// moment O may be rescaled.
 //
 // Warp roles (192 threads): warp 0 TMA producer (Q chunk per item, K and V
 // tiles through a 2-stage ring); warp 1 TMEM owner and MMA issuer, running
@@ -49,13 +53,13 @@ constexpr float kRescaleLog2 = 8.f;
 template <int D>
 struct Layout {
     static constexpr int kOp = (D / 64) * kBlockBytes;   // [128][D] bf16
-    static constexpr int kPbuf = 2 * kBlockBytes;        // [128 rows][128 keys] bf16
+    static constexpr int kPbuf = 2 * kBlockBytes;        // [128 rows][128 keys] bf16 (hi, then lo)
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kOp;
     static constexpr int kV = kK + kStages * kOp;
     static constexpr int kP = kV + kStages * kOp;
     static constexpr int kBars = kP + 2 * kPbuf;
-    static constexpr int kNumBars = 4 * kStages + 2 + 8 + 3;
+    static constexpr int kNumBars = 4 * kStages + 2 + 4 + 2 + 2;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -108,8 +112,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
     uint64_t *q_full = bars + 4 * kStages, *q_empty = q_full + 1;
     uint64_t *s_full = q_empty + 1, *s_empty = s_full + 2;
-    uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
-    uint64_t *o_full = p_empty + 2, *o_empty = o_full + 1, *o_final = o_empty + 1;
+    uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1;
+    uint64_t *o_empty = p_empty + 1, *o_final = o_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
@@ -127,10 +131,9 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&s_empty[b], kSoftWarps);
-            mbar_init(&p_full[b], kSoftWarps);
-            mbar_init(&p_empty[b], 1);
         }
-        mbar_init(o_full, 1);
+        mbar_init(p_full, kSoftWarps);
+        mbar_init(p_empty, 1);
         mbar_init(o_empty, kSoftWarps);
         mbar_init(o_final, 1);
         fence_barrier_init();
@@ -207,29 +210,31 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             const uint32_t q_base = smem_u32(smem + Ly::kQ);
             long long tcount = 0, icount = 0;
             bool ok = true;
-            // O += P V for global tile tc (the item's first tile overwrites O)
+            // O += P_hi V + P_lo V for global tile tc (the item's first tile overwrites O)
             auto pv = [&](long long tc, bool first) {
-                const int pb = (int)(tc & 1);
                 const int s = (int)(tc % kStages);
                 if (first)
                     ok = ok && mbar_wait(o_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
-                ok = ok && mbar_wait(&p_full[pb], (uint32_t)((tc >> 1) & 1), abort_flag, kWaitNs);
+                ok = ok && mbar_wait(p_full, (uint32_t)(tc & 1), abort_flag, kWaitNs);
                 ok = ok && mbar_wait(&v_full[s], (uint32_t)((tc / kStages) & 1), abort_flag,
                                      kWaitNs);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t p_base = smem_u32(smem + Ly::kP + pb * Ly::kPbuf);
                 const uint32_t v_base = smem_u32(smem + Ly::kV + s * Ly::kOp);
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t p_base = smem_u32(smem + Ly::kP + part * Ly::kPbuf);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + kOCol, sdesc_k_sw128(p_base + kb * kBlockBytes + kk * 32),
-                               sdesc_mn_sw128(v_base + (kb * 64 + kk * 16) * 128, kBlockBytes),
-                               idesc_pv, (first && kb == 0 && kk == 0) ? 0u : 1u);
-                mma_commit(&p_empty[pb]);
+                    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + kOCol,
+                                   sdesc_k_sw128(p_base + kb * kBlockBytes + kk * 32),
+                                   sdesc_mn_sw128(v_base + (kb * 64 + kk * 16) * 128, kBlockBytes),
+                                   idesc_pv, (first && part == 0 && kb == 0 && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(p_empty);
                 mma_commit(&v_empty[s]);
-                mma_commit(o_full);
             };
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
@@ -317,18 +322,11 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const float m_tile = mx * cs;
                 const bool need = m_tile > m_used + kRescaleLog2;
                 const float factor = need ? ex2_approx(m_used - m_tile) : 1.f;
-                // P buffer pb is free once P V of tile tc-2 is done; waiting here first
-                // also guarantees o_full below cannot alias an older completion
-                const int pb = (int)(tc & 1);
-                ok = __all_sync(0xffffffffu, mbar_wait(&p_empty[pb], (uint32_t)((tc >> 1) & 1) ^ 1u,
+                // the P buffer is free once P V of tile tc-1 is done; O is then stable
+                ok = __all_sync(0xffffffffu, mbar_wait(p_empty, (uint32_t)(tc & 1) ^ 1u,
                                                        abort_flag, kWaitNs));
                 if (!ok) break;
                 if (__any_sync(0xffffffffu, need && i > 0)) {
-                    // O holds P V of earlier tiles: rescale it once P V of tile tc-1 is done
-                    ok = __all_sync(0xffffffffu, mbar_wait(o_full, (uint32_t)((tc - 1) & 1),
-                                                           abort_flag, kWaitNs));
-                    if (!ok) break;
-                    tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c) {
                         float o[16];
@@ -344,11 +342,11 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     l *= factor;
                     m_used = m_tile;
                 }
-                uint8_t *prow = smem + Ly::kP + pb * Ly::kPbuf + rr * 128;
+                uint8_t *prow = smem + Ly::kP + rr * 128;
                 float lsum = 0.f;
 #pragma unroll
                 for (int ch = 0; ch < kTileKeys / 8; ++ch) {
-                    uint32_t w4[4];
+                    uint32_t whi[4], wlo[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const int j0 = ch * 8 + 2 * h;
@@ -356,18 +354,22 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         const float p1 =
                             (j0 + 1 <= lim) ? ex2_approx(fmaf(sv[j0 + 1], cs, -m_used)) : 0.f;
                         lsum += p0 + p1;
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                        w4[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p0, p1);
+                        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(
+                            p0 - __low2float(hi2), p1 - __high2float(hi2));
+                        whi[h] = *reinterpret_cast<const uint32_t *>(&hi2);
+                        wlo[h] = *reinterpret_cast<const uint32_t *>(&lo2);
                     }
-                    const int blk = ch >> 3, c16 = ch & 7;
-                    *reinterpret_cast<uint4 *>(prow + blk * kBlockBytes + ((c16 ^ (rr & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    const int off = (ch >> 3) * kBlockBytes + (((ch & 7) ^ (rr & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+                    *reinterpret_cast<uint4 *>(prow + Ly::kPbuf + off) =
+                        make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
                 }
                 l += lsum;
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[pb]);
+                if (lane == 0) mbar_arrive(p_full);
             }
             if (!ok) break;
             // item end: read O once the last P V is done, write this split's partial
