@@ -403,7 +403,15 @@ RAGGED_MISTRAL = Workload("ragged8_mistral7b_32L_8kv_32q_d128_n16k-128k", num_la
                           ragged_range=(16384, 131072, 8), budget_ratio=0.30)
 
 CONFIGS = [TINY, LLAMA8B_32K, LONG_128K, QWEN7B_128K, RAGGED_MISTRAL]
-BY_NAME = {c.name: c for c in CONFIGS}
+# Reduced copies for kernel profiles: the same per-unit shapes, few units
+# (K+V still larger than L2, a few GB on the device at most).
+PROFILE_CASES = [
+    LONG_128K.scaled(name="long_2L_2kv_8q_d128_n131072_pyramid10", num_layers=2,
+                     num_kv_heads=2, num_q_heads=8),
+    QWEN7B_128K.scaled(name="qwen7b_2L_2kv_14q_d128_n131072_ripple5", num_layers=2,
+                       num_kv_heads=2, num_q_heads=14),
+]
+BY_NAME = {c.name: c for c in CONFIGS + PROFILE_CASES}
 
 
 def small_variant(wl: Workload, n: int, layers: int = 2, kv_heads: int = 2,
