@@ -98,6 +98,51 @@ __device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, c
     return it;
 }
 
+// Running maxima (4 independent chains) of 16 logits; keys past `lim` excluded.
+__device__ __forceinline__ void tile_max16(const float (&v)[16], int j0, int lim, bool masked,
+                                           float (&mx)[4]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float x = (masked && j0 + j > lim) ? -INFINITY : v[j];
+        mx[j & 3] = fmaxf(mx[j & 3], x);
+    }
+}
+
+// p = 2^(s c - m) for 16 keys (two 8-key groups of the P tile): adds p to the
+// row sum and stores bf16(p) to the P_hi tile and bf16(p - P_hi) to the P_lo
+// tile (kPbuf bytes later), in the 128-byte swizzled K-major layout.
+template <int kPbuf>
+__device__ __forceinline__ void soft16(const float (&v)[16], int j0, int lim, bool masked,
+                                       float cs, float negm, float2 &lsum, uint8_t *prow, int rr) {
+    const float2 cs2 = make_float2(cs, cs);
+    const float2 nm2 = make_float2(negm, negm);
+    const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+    for (int g8 = 0; g8 < 2; ++g8) {
+        uint32_t whi[4], wlo[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int j = g8 * 8 + 2 * h;
+            const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), cs2, nm2);
+            float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            if (masked) {
+                if (j0 + j > lim) p.x = 0.f;
+                if (j0 + j + 1 > lim) p.y = 0.f;
+            }
+            lsum = __fadd2_rn(lsum, p);
+            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p.x, p.y);
+            const float2 lo = __ffma2_rn(__bfloat1622float2(hi2), neg1, p);
+            const __nv_bfloat162 lo2 = __floats2bfloat162_rn(lo.x, lo.y);
+            whi[h] = *reinterpret_cast<const uint32_t *>(&hi2);
+            wlo[h] = *reinterpret_cast<const uint32_t *>(&lo2);
+        }
+        const int ch = (j0 >> 3) + g8;    // 8-key chunk of the 128-key row
+        const int off = (ch >> 3) * kBlockBytes + (((ch & 7) ^ (rr & 7)) << 4);
+        *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+        *reinterpret_cast<uint4 *>(prow + kPbuf + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
@@ -300,25 +345,28 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                                        abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
-                float sv[kTileKeys];
-#pragma unroll
-                for (int c = 0; c < kTileKeys / 16; ++c) {
-                    float tmp[16];
-                    tmem_ld16(tmem + lane_addr + sb * kTileKeys + c * 16, tmp);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) sv[c * 16 + j] = tmp[j];
-                }
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                const uint32_t s_col = tmem + lane_addr + sb * kTileKeys;
                 // causal mask (only the tiles that reach into the window need it)
                 const bool boundary = kt + kTileKeys - 1 > pos_min;
                 const int lim = row_valid ? (boundary ? pos - kt : kTileKeys - 1) : -1;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < kTileKeys; ++j)
-                    if (j <= lim) mx = fmaxf(mx, sv[j]);
+                const bool masked = lim < kTileKeys - 1;
+                // pass A: row max of the tile
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                {
+                    float bA[16], bB[16];
+                    tmem_ld16(s_col, bA);
+                    for (int c = 0; c < kTileKeys / 16; c += 2) {
+                        tmem_ld_wait();
+                        reg_fence(bA);
+                        tmem_ld16(s_col + (c + 1) * 16, bB);
+                        tile_max16(bA, c * 16, lim, masked, mx4);
+                        tmem_ld_wait();
+                        reg_fence(bB);
+                        if (c + 2 < kTileKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
+                        tile_max16(bB, (c + 1) * 16, lim, masked, mx4);
+                    }
+                }
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
                 const float m_tile = mx * cs;
                 const bool need = m_tile > m_used + kRescaleLog2;
                 const float factor = need ? ex2_approx(m_used - m_tile) : 1.f;
@@ -342,30 +390,28 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     l *= factor;
                     m_used = m_tile;
                 }
+                // pass B: p = 2^(s c - m), row sum, P_hi / P_lo to shared memory
                 uint8_t *prow = smem + Ly::kP + rr * 128;
-                float lsum = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < kTileKeys / 8; ++ch) {
-                    uint32_t whi[4], wlo[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int j0 = ch * 8 + 2 * h;
-                        const float p0 = (j0 <= lim) ? ex2_approx(fmaf(sv[j0], cs, -m_used)) : 0.f;
-                        const float p1 =
-                            (j0 + 1 <= lim) ? ex2_approx(fmaf(sv[j0 + 1], cs, -m_used)) : 0.f;
-                        lsum += p0 + p1;
-                        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p0, p1);
-                        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(
-                            p0 - __low2float(hi2), p1 - __high2float(hi2));
-                        whi[h] = *reinterpret_cast<const uint32_t *>(&hi2);
-                        wlo[h] = *reinterpret_cast<const uint32_t *>(&lo2);
+                float2 lsum = make_float2(0.f, 0.f);
+                const float negm = m_used == -INFINITY ? 0.f : -m_used;
+                {
+                    float bA[16], bB[16];
+                    tmem_ld16(s_col, bA);
+                    for (int c = 0; c < kTileKeys / 16; c += 2) {
+                        tmem_ld_wait();
+                        reg_fence(bA);
+                        tmem_ld16(s_col + (c + 1) * 16, bB);
+                        soft16<Ly::kPbuf>(bA, c * 16, lim, masked, cs, negm, lsum, prow, rr);
+                        tmem_ld_wait();
+                        reg_fence(bB);
+                        if (c + 2 < kTileKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
+                        soft16<Ly::kPbuf>(bB, (c + 1) * 16, lim, masked, cs, negm, lsum, prow, rr);
                     }
-                    const int off = (ch >> 3) * kBlockBytes + (((ch & 7) ^ (rr & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-                    *reinterpret_cast<uint4 *>(prow + Ly::kPbuf + off) =
-                        make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
                 }
-                l += lsum;
+                l += lsum.x + lsum.y;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();

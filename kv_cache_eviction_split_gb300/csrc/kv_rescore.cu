@@ -55,9 +55,10 @@ struct Layout {
     static constexpr int kAlo = kAhi + kOp;
     static constexpr int kK = kAlo + kOp;
     static constexpr int kV = kK + kStages * kOp;
-    static constexpr int kStats = kV + kStages * kOp;      // [2][64] float2 (-m, l)
-    static constexpr int kA2 = kStats + 2 * 64 * 8;        // [2][64] float ||a||^2
-    static constexpr int kRing = kA2 + 2 * 64 * 4;         // [2 slots][128] float
+    static constexpr int kStats = kV + kStages * kOp;      // [2][32] float4 (-m0,-m1,l0,l1)
+    static constexpr int kA2 = kStats + 2 * 32 * 16;       // [2][32] float2 ||a||^2 pairs
+    static constexpr int kRmod = kA2 + 2 * 32 * 8;         // [2][64] uint16 row % w
+    static constexpr int kRing = kRmod + 2 * 64 * 2;       // [2 slots][128] float
     static constexpr int kBars = kRing + 2 * 128 * 4;
     static constexpr int kNumBars = 4 * kStages + 2 + 8;
     static constexpr int kMisc = kBars + kNumBars * 8;
@@ -125,6 +126,39 @@ __device__ __forceinline__ float row_sqnorm(const uint8_t *tile, int row) {
         }
     }
     return acc;
+}
+
+// Adds the terms of 16 rows (columns of one TMEM load) for this thread's key:
+// e/(l - e) * sqrt(x) with e = 2^(s c - m), x = max(||a||^2 - 2X + ||v||^2, 0),
+// written as e * x * rsqrt((l - e)^2 x + tiny) so one MUFU op gives sqrt(x)/(l-e)
+// and x = 0 gives 0.  Two rows at a time in packed f32x2 arithmetic.
+__device__ __forceinline__ void rescore16(const float (&sv)[16], const float (&xv)[16],
+                                          const float4 *st, const float2 *a2p,
+                                          const uint16_t *rmod, bool boundary, int jrel,
+                                          float cscale, float2 v2v2, float2 &acc) {
+    const float2 cs2 = make_float2(cscale, cscale);
+    const float2 neg1 = make_float2(-1.f, -1.f);
+    const float2 neg2 = make_float2(-2.f, -2.f);
+    const float2 tiny = make_float2(1e-30f, 1e-30f);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const float4 s4 = st[p];
+        const float2 t = __ffma2_rn(make_float2(sv[2 * p], sv[2 * p + 1]), cs2,
+                                    make_float2(s4.x, s4.y));
+        const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        const float2 den = __ffma2_rn(e, neg1, make_float2(s4.z, s4.w));
+        const float2 av = __fadd2_rn(a2p[p], v2v2);
+        float2 x = __ffma2_rn(make_float2(xv[2 * p], xv[2 * p + 1]), neg2, av);
+        x.x = fmaxf(x.x, 0.f);
+        x.y = fmaxf(x.y, 0.f);
+        const float2 y = __ffma2_rn(__fmul2_rn(den, den), x, tiny);
+        float2 ex = __fmul2_rn(e, x);
+        if (boundary) {
+            if (jrel > (int)rmod[2 * p]) ex.x = 0.f;
+            if (jrel > (int)rmod[2 * p + 1]) ex.y = 0.f;
+        }
+        acc = __ffma2_rn(ex, make_float2(rsqrt_approx(y.x), rsqrt_approx(y.y)), acc);
+    }
 }
 
 template <int D>
@@ -314,8 +348,9 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         const int key_local = quarter * 32 + lane;
         const int tg = (ew & 3) * 32 + lane;   // thread index within the group
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        float2 *stats = reinterpret_cast<float2 *>(smem + Ly::kStats) + g * 64;
-        float *a2s = reinterpret_cast<float *>(smem + Ly::kA2) + g * 64;
+        float4 *stats = reinterpret_cast<float4 *>(smem + Ly::kStats) + g * 32;
+        float2 *a2s = reinterpret_cast<float2 *>(smem + Ly::kA2) + g * 32;
+        uint16_t *rmod = reinterpret_cast<uint16_t *>(smem + Ly::kRmod) + g * 64;
         float *ring = reinterpret_cast<float *>(smem + Ly::kRing);
         const float cscale = P.scale_log2;
         long long tcount = 0;
@@ -326,16 +361,26 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             const int rch = chunk_half_rows(P, it.c);
             const int row_base = it.c * kChunkRows + g * rch;
             asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
-            for (int rr = tg; rr < rch; rr += 128) {
-                const int row = row_base + rr;
-                if (row < P.rows) {
-                    const float2 ml = A.stat_ml[it.u * P.rows + row];
-                    stats[rr] = make_float2(-ml.x, ml.y);
-                    a2s[rr] = A.stat_a2[it.u * P.rows + row];
-                } else {
-                    stats[rr] = make_float2(-INFINITY, 1.f);
-                    a2s[rr] = 0.f;
+            for (int pp = tg; pp < rch / 2; pp += 128) {
+                float nm[2], ll[2], aa[2];
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int row = row_base + 2 * pp + k2;
+                    if (row < P.rows) {
+                        const float2 ml = A.stat_ml[it.u * P.rows + row];
+                        nm[k2] = -ml.x;
+                        ll[k2] = ml.y;
+                        aa[k2] = A.stat_a2[it.u * P.rows + row];
+                        rmod[2 * pp + k2] = (uint16_t)(row % P.w);
+                    } else {   // padding row: e = 0, so its term is 0
+                        nm[k2] = -INFINITY;
+                        ll[k2] = 1.f;
+                        aa[k2] = 0.f;
+                        rmod[2 * pp + k2] = 0;
+                    }
                 }
+                stats[pp] = make_float4(nm[0], nm[1], ll[0], ll[1]);
+                a2s[pp] = make_float2(aa[0], aa[1]);
             }
             asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
             float *out = A.out + (long long)it.c * A.out_stride + U.kv_row0;
@@ -353,28 +398,39 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 if (lane == 0) mbar_arrive(&v_empty[s]);
                 const int j = t * kTileKeys + key_local;
                 const bool boundary = t * kTileKeys + kTileKeys - 1 > pos0;
-                float acc = 0.f;
-                for (int cc = 0; cc < rch; cc += 16) {
-                    float sv[16], xv[16];
-                    tmem_ld16(tmem + lane_addr + g * 128 + cc, sv);
-                    tmem_ld16(tmem + lane_addr + g * 128 + 64 + cc, xv);
+                // rows with j > pos0 + (row % w) do not see key j (only near the window)
+                const int jrel = j - pos0;
+                float2 acc = make_float2(0.f, 0.f);
+                const float2 v2v2 = make_float2(v2, v2);
+                const uint32_t s_col = tmem + lane_addr + g * 128;
+                const uint32_t x_col = s_col + 64;
+                float sA[16], xA[16], sB[16], xB[16];
+                tmem_ld16(s_col, sA);
+                tmem_ld16(x_col, xA);
+                for (int cc = 0; cc < rch; cc += 32) {
                     tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 st = stats[cc + i];
-                        const float a2 = a2s[cc + i];
-                        const float e = ex2_approx(fmaf(sv[i], cscale, st.x));
-                        const float den = st.y - e;
-                        const float x = fmaxf(fmaf(xv[i], -2.f, a2 + v2), 0.f);
-                        const float y = fmaxf(den * den * x, FLT_MIN);
-                        float term = e * x * rsqrt_approx(y);
-                        if (boundary) {
-                            const int row = row_base + cc + i;
-                            if (j > pos0 + row % P.w) term = 0.f;
+                    reg_fence(sA);
+                    reg_fence(xA);
+                    const bool second = cc + 16 < rch;
+                    if (second) {
+                        tmem_ld16(s_col + cc + 16, sB);
+                        tmem_ld16(x_col + cc + 16, xB);
+                    }
+                    rescore16(sA, xA, stats + cc / 2, a2s + cc / 2, rmod + cc, boundary, jrel,
+                              cscale, v2v2, acc);
+                    if (second) {
+                        tmem_ld_wait();
+                        reg_fence(sB);
+                        reg_fence(xB);
+                        if (cc + 32 < rch) {
+                            tmem_ld16(s_col + cc + 32, sA);
+                            tmem_ld16(x_col + cc + 32, xA);
                         }
-                        acc += term;
+                        rescore16(sB, xB, stats + cc / 2 + 8, a2s + cc / 2 + 8, rmod + cc + 16,
+                                  boundary, jrel, cscale, v2v2, acc);
                     }
                 }
+                const float acc_sum = acc.x + acc.y;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tm_empty[g]);
@@ -384,14 +440,14 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     ok = __all_sync(0xffffffffu,
                                     mbar_wait(&part_empty[slot], rpar ^ 1u, abort_flag, kWaitNs));
                     if (!ok) break;
-                    ring[slot * 128 + key_local] = acc;
+                    ring[slot * 128 + key_local] = acc_sum;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&part_full[slot]);
                 } else {
                     ok = __all_sync(0xffffffffu,
                                     mbar_wait(&part_full[slot], rpar, abort_flag, kWaitNs));
                     if (!ok) break;
-                    const float tot = acc + ring[slot * 128 + key_local];
+                    const float tot = acc_sum + ring[slot * 128 + key_local];
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&part_empty[slot]);
                     if (j < U.n) out[j] = tot;

@@ -171,6 +171,14 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// After tmem_ld_wait: makes later uses of registers filled by an earlier
+// tcgen05.ld depend on the wait, so the compiler cannot hoist them above it.
+template <int N>
+__device__ __forceinline__ void reg_fence(float (&v)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
+
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // layout that TMA writes for a box whose inner extent is 128 bytes: rows of
 // 128 B, 8-row atoms of 1024 B (stride between atoms = 1024 B), 16-byte
