@@ -25,9 +25,9 @@
 // write P of tile i only after P V of tile i-1 is done, which is also the
 // moment O may be rescaled.
 //
-// Warp roles (192 threads): warp 0 TMA producer (Q chunk per item, K and V
+// Warp roles (320 threads): warp 0 TMA producer (Q chunk per item, K and V
 // tiles through a 2-stage ring); warp 1 TMEM owner and MMA issuer, running
-// S of tile i+1 ahead of P V of tile i; warps 2-5 softmax.  Work items are
+// S of tile i+1 ahead of P V of tile i; warps 2-9 softmax, two per row.  Work items are
 // (unit, 16384-key split, row chunk), chunk fastest, walked round-robin by a
 // persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
 #include <cfloat>
@@ -42,7 +42,7 @@ using namespace sm100;
 constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
 constexpr int kStages = 2;
-constexpr int kSoftWarps = 4;
+constexpr int kSoftWarps = 8;    // two per row quarter, each on half of a tile's keys
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
@@ -58,8 +58,10 @@ struct Layout {
     static constexpr int kK = kQ + kOp;
     static constexpr int kV = kK + kStages * kOp;
     static constexpr int kP = kV + kStages * kOp;
-    static constexpr int kBars = kP + 2 * kPbuf;
-    static constexpr int kNumBars = 4 * kStages + 2 + 4 + 2 + 2;
+    static constexpr int kXmax = kP + 2 * kPbuf;          // [2 slots][2 halves][128] float
+    static constexpr int kXl = kXmax + 2 * 2 * 128 * 4;    // [128] float
+    static constexpr int kBars = kXl + 128 * 4;
+    static constexpr int kNumBars = 4 * kStages + 2 + 4 + 2 + 2 + 8 + 4;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -159,6 +161,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *s_full = q_empty + 1, *s_empty = s_full + 2;
     uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1;
     uint64_t *o_empty = p_empty + 1, *o_final = o_empty + 1;
+    uint64_t *xm_bar = o_final + 1;          // [2 slots][4 row quarters], pair max exchange
+    uint64_t *xl_bar = xm_bar + 8;           // [4 row quarters], pair row-sum exchange
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
@@ -181,6 +185,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         mbar_init(p_empty, 1);
         mbar_init(o_empty, kSoftWarps);
         mbar_init(o_final, 1);
+        for (int b = 0; b < 8; ++b) mbar_init(&xm_bar[b], 2);
+        for (int b = 0; b < 4; ++b) mbar_init(&xl_bar[b], 2);
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -265,19 +271,21 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                      kWaitNs);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t v_base = smem_u32(smem + Ly::kV + s * Ly::kOp);
+                const uint64_t vb = sdesc_mn_sw128(smem_u32(smem + Ly::kV + s * Ly::kOp), kBlockBytes);
+                const uint64_t pa0 = sdesc_k_sw128(smem_u32(smem + Ly::kP));
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t p_base = smem_u32(smem + Ly::kP + part * Ly::kPbuf);
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + kOCol,
-                                   sdesc_k_sw128(p_base + kb * kBlockBytes + kk * 32),
-                                   sdesc_mn_sw128(v_base + (kb * 64 + kk * 16) * 128, kBlockBytes),
-                                   idesc_pv, (first && part == 0 && kb == 0 && kk == 0) ? 0u : 1u);
-                }
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_add(pa0, part * Ly::kPbuf + kb * kBlockBytes + kk * 32);
+                            const uint64_t b = sdesc_add(vb, (kb * 64 + kk * 16) * 128);
+                            if (part == 0 && kb == 0 && kk == 0 && first)
+                                mma_ss_c<false>(tmem + kOCol, a, b, idesc_pv);
+                            else
+                                mma_ss_c<true>(tmem + kOCol, a, b, idesc_pv);
+                        }
                 mma_commit(p_empty);
                 mma_commit(&v_empty[s]);
             };
@@ -296,14 +304,17 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                          mbar_wait(&k_full[s], (uint32_t)((tc / kStages) & 1), abort_flag, kWaitNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t k_base = smem_u32(smem + Ly::kK + s * Ly::kOp);
+                    const uint64_t kb0 = sdesc_k_sw128(smem_u32(smem + Ly::kK + s * Ly::kOp));
+                    const uint64_t qa0 = sdesc_k_sw128(q_base);
+                    const uint32_t d_s = tmem + sb * kTileKeys;
+                    mma_ss_c<false>(d_s, qa0, kb0, idesc_s);
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t ko = kb * kBlockBytes + kk * 32;
-                            mma_ss(tmem + sb * kTileKeys, sdesc_k_sw128(q_base + ko),
-                                   sdesc_k_sw128(k_base + ko), idesc_s, (kb | kk) != 0);
+                            if (kb | kk)
+                                mma_ss_c<true>(d_s, sdesc_add(qa0, ko), sdesc_add(kb0, ko), idesc_s);
                         }
                     mma_commit(&s_full[sb]);
                     mma_commit(&k_empty[s]);
@@ -322,10 +333,19 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         }
     } else if (run) {
         // ------------------------------------------------------------ softmax
+        // Warps w and w+4 own the same 32 rows (TMEM lane quarter w % 4); warp
+        // half 0 takes keys 0-63 of every tile, half 1 keys 64-127, and O columns
+        // split the same way.  They agree on the row max through shared memory.
+        const int ew = warp - 2;
+        const int half = ew >> 2;
         const int quarter = warp & 3;
         const int rr = quarter * 32 + lane;               // row of the chunk = TMEM lane
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        float *xmax = reinterpret_cast<float *>(smem + Ly::kXmax);
+        float *xl = reinterpret_cast<float *>(smem + Ly::kXl);
         const float cs = P.scale_log2;
+        constexpr int kHalfKeys = kTileKeys / 2;
+        constexpr int kHalfD = D / 2;
         long long tcount = 0, icount = 0;
         bool ok = true;
         for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
@@ -345,28 +365,39 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                                        abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t s_col = tmem + lane_addr + sb * kTileKeys;
+                const int j0 = half * kHalfKeys;
+                const uint32_t s_col = tmem + lane_addr + sb * kTileKeys + j0;
                 // causal mask (only the tiles that reach into the window need it)
                 const bool boundary = kt + kTileKeys - 1 > pos_min;
                 const int lim = row_valid ? (boundary ? pos - kt : kTileKeys - 1) : -1;
                 const bool masked = lim < kTileKeys - 1;
-                // pass A: row max of the tile
+                // pass A: row max over this warp's 64 keys, then over the pair
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 {
                     float bA[16], bB[16];
                     tmem_ld16(s_col, bA);
-                    for (int c = 0; c < kTileKeys / 16; c += 2) {
+#pragma unroll
+                    for (int c = 0; c < kHalfKeys / 16; c += 2) {
                         tmem_ld_wait();
                         reg_fence(bA);
                         tmem_ld16(s_col + (c + 1) * 16, bB);
-                        tile_max16(bA, c * 16, lim, masked, mx4);
+                        tile_max16(bA, j0 + c * 16, lim, masked, mx4);
                         tmem_ld_wait();
                         reg_fence(bB);
-                        if (c + 2 < kTileKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
-                        tile_max16(bB, (c + 1) * 16, lim, masked, mx4);
+                        if (c + 2 < kHalfKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
+                        tile_max16(bB, j0 + (c + 1) * 16, lim, masked, mx4);
                     }
                 }
-                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                float *slot = xmax + (int)(tc & 1) * 256;
+                slot[half * 128 + rr] = mh;
+                __syncwarp();
+                uint64_t *xb = &xm_bar[(int)(tc & 1) * 4 + quarter];
+                if (lane == 0) mbar_arrive(xb);
+                ok = __all_sync(0xffffffffu, mbar_wait(xb, (uint32_t)((tc >> 1) & 1), abort_flag,
+                                                       kWaitNs));
+                if (!ok) break;
+                const float mx = fmaxf(mh, slot[(half ^ 1) * 128 + rr]);
                 const float m_tile = mx * cs;
                 const bool need = m_tile > m_used + kRescaleLog2;
                 const float factor = need ? ex2_approx(m_used - m_tile) : 1.f;
@@ -376,13 +407,15 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 if (!ok) break;
                 if (__any_sync(0xffffffffu, need && i > 0)) {
 #pragma unroll
-                    for (int c = 0; c < D / 16; ++c) {
+                    for (int c = 0; c < kHalfD / 16; ++c) {
                         float o[16];
-                        tmem_ld16(tmem + lane_addr + kOCol + c * 16, o);
+                        const uint32_t oc = tmem + lane_addr + kOCol + half * kHalfD + c * 16;
+                        tmem_ld16(oc, o);
                         tmem_ld_wait();
+                        reg_fence(o);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) o[j] *= factor;
-                        tmem_st16(tmem + lane_addr + kOCol + c * 16, o);
+                        tmem_st16(oc, o);
                     }
                     tmem_st_wait();
                 }
@@ -397,15 +430,17 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 {
                     float bA[16], bB[16];
                     tmem_ld16(s_col, bA);
-                    for (int c = 0; c < kTileKeys / 16; c += 2) {
+#pragma unroll
+                    for (int c = 0; c < kHalfKeys / 16; c += 2) {
                         tmem_ld_wait();
                         reg_fence(bA);
                         tmem_ld16(s_col + (c + 1) * 16, bB);
-                        soft16<Ly::kPbuf>(bA, c * 16, lim, masked, cs, negm, lsum, prow, rr);
+                        soft16<Ly::kPbuf>(bA, j0 + c * 16, lim, masked, cs, negm, lsum, prow, rr);
                         tmem_ld_wait();
                         reg_fence(bB);
-                        if (c + 2 < kTileKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
-                        soft16<Ly::kPbuf>(bB, (c + 1) * 16, lim, masked, cs, negm, lsum, prow, rr);
+                        if (c + 2 < kHalfKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
+                        soft16<Ly::kPbuf>(bB, j0 + (c + 1) * 16, lim, masked, cs, negm, lsum, prow,
+                                          rr);
                     }
                 }
                 l += lsum.x + lsum.y;
@@ -425,12 +460,13 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                 mbar_wait(o_final, (uint32_t)(icount & 1), abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
-                float *po = A.part_o + prow_idx * D;
+                float *po = A.part_o + prow_idx * D + half * kHalfD;
 #pragma unroll
-                for (int c = 0; c < D / 16; ++c) {
+                for (int c = 0; c < kHalfD / 16; ++c) {
                     float o[16];
-                    tmem_ld16(tmem + lane_addr + kOCol + c * 16, o);
+                    tmem_ld16(tmem + lane_addr + kOCol + half * kHalfD + c * 16, o);
                     tmem_ld_wait();
+                    reg_fence(o);
                     if (row_valid) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
@@ -442,7 +478,14 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(o_empty);
             }
-            if (row_valid) A.part_ml[prow_idx] = make_float2(m_used, l);
+            // the row sum is split between the pair: half 1 hands its part to half 0
+            if (half == 1) xl[rr] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xl_bar[quarter]);
+            ok = __all_sync(0xffffffffu, mbar_wait(&xl_bar[quarter], (uint32_t)(icount & 1),
+                                                   abort_flag, kWaitNs));
+            if (!ok) break;
+            if (half == 0 && row_valid) A.part_ml[prow_idx] = make_float2(m_used, l + xl[rr]);
             tcount += ntiles;
             ++icount;
         }

@@ -21,8 +21,10 @@
 // Warp roles (320 threads):
 //   warp 0      TMA producer: the chunk's Q, a_hi, a_lo once per item; K and V
 //               tiles through a 2-stage ring
-//   warp 1      TMEM owner and MMA issuer (one thread): per tile and per half
-//               of the chunk's rows, S = K Q^T, X = V a_hi^T + V a_lo^T
+//   warp 1      TMEM owner and MMA issuer (one thread): per tile S = K Q^T and
+//               X = V a_hi^T + V a_lo^T over all rows of the chunk, into one of
+//               two TMEM buffers, so tile i+1 computes while tile i is scored
+//               and a K/V stage frees as soon as its MMAs complete
 //   warps 2-9   epilogue: group g (4 warps) handles half g of the rows; group 0
 //               hands its per-key partial sums to group 1 through a smem ring
 // Every wait is bounded: on expiry the kernel posts KV_ERR_TIMEOUT, the other
@@ -43,7 +45,7 @@ constexpr int kTilesPerItem = 64;
 constexpr int kStages = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kBlockBytes = kChunkRows * 128;   // one [128 rows][64 bf16] swizzled box
 
@@ -194,7 +196,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         mbar_init(qa_empty, 1);
         for (int h = 0; h < 2; ++h) {
             mbar_init(&tm_full[h], 1);
-            mbar_init(&tm_empty[h], 4);
+            mbar_init(&tm_empty[h], kEpiWarps);
             mbar_init(&part_full[h], 4);
             mbar_init(&part_empty[h], 4);
         }
@@ -279,57 +281,56 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
                 const int rch = chunk_half_rows(P, it.c);
-                const uint32_t idesc = idesc_bf16_f32(128, rch);
+                const uint32_t idesc = idesc_bf16_f32(128, 2 * rch);
                 ok = mbar_wait(qa_full, (uint32_t)(icount & 1), abort_flag, kWaitNs);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t q_base = smem_u32(smem + Ly::kQ);
-                const uint32_t hi_base = smem_u32(smem + Ly::kAhi);
-                const uint32_t lo_base = smem_u32(smem + Ly::kAlo);
+                const uint64_t qb = sdesc_k_sw128(smem_u32(smem + Ly::kQ));
+                const uint64_t hb = sdesc_k_sw128(smem_u32(smem + Ly::kAhi));
+                const uint64_t lb = sdesc_k_sw128(smem_u32(smem + Ly::kAlo));
                 for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
                     const int s = (int)(tcount % kStages);
                     const uint32_t par = (uint32_t)((tcount / kStages) & 1);
-                    ok = mbar_wait(&k_full[s], par, abort_flag, kWaitNs) &&
-                         mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
+                    const int b = (int)(tcount & 1);          // TMEM buffer of this tile
+                    ok = mbar_wait(&tm_empty[b], (uint32_t)((tcount >> 1) & 1) ^ 1u, abort_flag,
+                                   kWaitNs) &&
+                         mbar_wait(&k_full[s], par, abort_flag, kWaitNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t k_base = smem_u32(smem + Ly::kK + s * Ly::kOp);
-                    const uint32_t v_base = smem_u32(smem + Ly::kV + s * Ly::kOp);
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        ok = mbar_wait(&tm_empty[h], (uint32_t)(tcount & 1) ^ 1u, abort_flag,
-                                       kWaitNs);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t d_s = tmem + h * 128;
-                        const uint32_t d_x = tmem + h * 128 + 64;
-                        const uint32_t boff = h * rch * 128;
+                    const uint32_t d_s = tmem + b * 256;
+                    const uint32_t d_x = d_s + 128;
+                    const uint64_t ka = sdesc_k_sw128(smem_u32(smem + Ly::kK + s * Ly::kOp));
+                    const uint64_t va = sdesc_k_sw128(smem_u32(smem + Ly::kV + s * Ly::kOp));
+                    mma_ss_c<false>(d_s, ka, qb, idesc);
 #pragma unroll
-                        for (int kb = 0; kb < D / 64; ++kb)
+                    for (int kb = 0; kb < D / 64; ++kb)
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint32_t ko = kb * kBlockBytes + kk * 32;
-                                mma_ss(d_s, sdesc_k_sw128(k_base + ko),
-                                       sdesc_k_sw128(q_base + ko + boff), idesc, (kb | kk) != 0);
-                            }
-#pragma unroll
-                        for (int kb = 0; kb < D / 64; ++kb)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint32_t ko = kb * kBlockBytes + kk * 32;
-                                mma_ss(d_x, sdesc_k_sw128(v_base + ko),
-                                       sdesc_k_sw128(hi_base + ko + boff), idesc, (kb | kk) != 0);
-                            }
-#pragma unroll
-                        for (int kb = 0; kb < D / 64; ++kb)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint32_t ko = kb * kBlockBytes + kk * 32;
-                                mma_ss(d_x, sdesc_k_sw128(v_base + ko),
-                                       sdesc_k_sw128(lo_base + ko + boff), idesc, 1u);
-                            }
-                        mma_commit(&tm_full[h]);
-                    }
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t ko = kb * kBlockBytes + kk * 32;
+                            if (kb | kk)
+                                mma_ss_c<true>(d_s, sdesc_add(ka, ko), sdesc_add(qb, ko), idesc);
+                        }
                     mma_commit(&k_empty[s]);
+                    ok = mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_ss_c<false>(d_x, va, hb, idesc);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t ko = kb * kBlockBytes + kk * 32;
+                            if (kb | kk)
+                                mma_ss_c<true>(d_x, sdesc_add(va, ko), sdesc_add(hb, ko), idesc);
+                        }
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t ko = kb * kBlockBytes + kk * 32;
+                            mma_ss_c<true>(d_x, sdesc_add(va, ko), sdesc_add(lb, ko), idesc);
+                        }
+                    mma_commit(&tm_full[b]);
                     mma_commit(&v_empty[s]);
                 }
                 mma_commit(qa_empty);
@@ -388,8 +389,10 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
                 const int s = (int)(tcount % kStages);
                 const uint32_t spar = (uint32_t)((tcount / kStages) & 1);
+                const int b = (int)(tcount & 1);              // TMEM buffer of this tile
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&tm_full[g], (uint32_t)(tcount & 1), abort_flag, kWaitNs) &&
+                                mbar_wait(&tm_full[b], (uint32_t)((tcount >> 1) & 1), abort_flag,
+                                          kWaitNs) &&
                                     mbar_wait(&v_full[s], spar, abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
@@ -402,8 +405,8 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const int jrel = j - pos0;
                 float2 acc = make_float2(0.f, 0.f);
                 const float2 v2v2 = make_float2(v2, v2);
-                const uint32_t s_col = tmem + lane_addr + g * 128;
-                const uint32_t x_col = s_col + 64;
+                const uint32_t s_col = tmem + lane_addr + b * 256 + g * rch;
+                const uint32_t x_col = s_col + 128;
                 float sA[16], xA[16], sB[16], xB[16];
                 tmem_ld16(s_col, sA);
                 tmem_ld16(x_col, xA);
@@ -433,7 +436,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const float acc_sum = acc.x + acc.y;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tm_empty[g]);
+                if (lane == 0) mbar_arrive(&tm_empty[b]);
                 const int slot = (int)(tcount & 1);
                 const uint32_t rpar = (uint32_t)((tcount >> 1) & 1);
                 if (g == 0) {
