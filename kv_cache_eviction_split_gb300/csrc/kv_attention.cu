@@ -6,28 +6,32 @@
 // English": the attention output a whose removal shift the score measures).
 //
 // Query-major, one 128-row chunk of the unit's G*w window rows per work item:
-//   S = Q K^T    M = 128 rows, N = 128 keys, K = d     (fp32 in TMEM, 2 buffers)
-//   O += P V     M = 128 rows, N = d, K = 128 keys     (fp32 in TMEM; V is the
-//                MN-major B operand; the softmax warps write P to swizzled
-//                shared memory as two bf16 halves P_hi = bf16(p) and
-//                P_lo = bf16(p - P_hi), and O accumulates P_hi V + P_lo V)
-// A single bf16 P leaves a with ~2^-9 relative error, which the rescoring
-// expansion amplifies where a is close to a value row (short requests,
-// concentrated attention); the split keeps ~16 bits of p.
-// The softmax warps own one row each: tile max with the causal mask, a lazy
-// rescale (O and l are rescaled only when the tile max exceeds the running
-// max by more than 2^8, so the running max may trail the true max by at most
-// 8 in log2 units -- every exponent stays <= 2^8), p = 2^(s*c - m), row sums
-// from the unrounded fp32 p.
+//   S = Q K^T    M = 128 rows, N = 128 keys, K = d   (fp32 in TMEM, 3 buffers)
+//   O += P V     M = 128 rows, N = d, K = 128 keys   (fp32 in TMEM; P is the
+//                A operand read from TMEM, V the MN-major B operand in smem)
+// The softmax warps turn S into P = 2^(s c - m) and store it, as two bf16
+// halves P_hi = bf16(p) and P_lo = bf16(p - P_hi), back into the TMEM columns
+// of the same S buffer (each 16-key chunk's 16 columns hold its 8 P_hi then 8
+// P_lo columns); O accumulates P_hi V + P_lo V.  (A single bf16 P
+// leaves a with ~2^-9 relative error, which the rescoring expansion amplifies
+// where a is close to a value row; the split keeps ~16 bits of p.)  Because P
+// lives in the S buffer, P is triple-buffered with S: S of tile i+1 and the
+// softmax of tile i+1 overlap P V of tile i.
+//
+// Softmax details: tile max with the causal mask; a lazy rescale (O and l are
+// rescaled only when the tile max exceeds the running max by more than 2^8,
+// so every exponent stays <= 2^8); row sums from the unrounded fp32 p.  Warps
+// w and w+4 share the 32 rows of TMEM lane quarter w % 4, each taking 64 of a
+// tile's 128 keys and half of O's columns; they agree on the row max through
+// shared memory.
 //
 // Barrier parities are tracked from use counts; no barrier can run more than
-// one phase ahead of its waiter.  The P buffer is single: the softmax warps
-// write P of tile i only after P V of tile i-1 is done, which is also the
-// moment O may be rescaled.
+// one phase ahead of its waiter (the S/P buffer of tile i is only refilled
+// after P V of tile i-3 completes).
 //
 // Warp roles (320 threads): warp 0 TMA producer (Q chunk per item, K and V
-// tiles through a 2-stage ring); warp 1 TMEM owner and MMA issuer, running
-// S of tile i+1 ahead of P V of tile i; warps 2-9 softmax, two per row.  Work items are
+// tiles through a 3-stage ring); warp 1 TMEM owner and MMA issuer, running
+// S of tile i+1 ahead of P V of tile i; warps 2-9 softmax.  Work items are
 // (unit, 16384-key split, row chunk), chunk fastest, walked round-robin by a
 // persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
 #include <cfloat>
@@ -41,11 +45,12 @@ using namespace sm100;
 
 constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
-constexpr int kStages = 2;
-constexpr int kSoftWarps = 8;    // two per row quarter, each on half of a tile's keys
+constexpr int kStages = 3;
+constexpr int kSoftWarps = 8;
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;
+constexpr int kSBufs = 3;                    // S/P buffers in TMEM
+constexpr uint32_t kOCol = kSBufs * 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kBlockBytes = 128 * 128;       // [128 rows][64 bf16], 128 B swizzle
 constexpr float kRescaleLog2 = 8.f;
@@ -53,15 +58,13 @@ constexpr float kRescaleLog2 = 8.f;
 template <int D>
 struct Layout {
     static constexpr int kOp = (D / 64) * kBlockBytes;   // [128][D] bf16
-    static constexpr int kPbuf = 2 * kBlockBytes;        // [128 rows][128 keys] bf16 (hi, then lo)
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kOp;
     static constexpr int kV = kK + kStages * kOp;
-    static constexpr int kP = kV + kStages * kOp;
-    static constexpr int kXmax = kP + 2 * kPbuf;          // [2 slots][2 halves][128] float
+    static constexpr int kXmax = kV + kStages * kOp;      // [2 slots][2 halves][128] float
     static constexpr int kXl = kXmax + 2 * 2 * 128 * 4;    // [128] float
     static constexpr int kBars = kXl + 128 * 4;
-    static constexpr int kNumBars = 4 * kStages + 2 + 4 + 2 + 2 + 8 + 4;
+    static constexpr int kNumBars = 4 * kStages + 2 + 3 * kSBufs + 2 + 8 + 4;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -100,49 +103,34 @@ __device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, c
     return it;
 }
 
-// Running maxima (4 independent chains) of 16 logits; keys past `lim` excluded.
-__device__ __forceinline__ void tile_max16(const float (&v)[16], int j0, int lim, bool masked,
-                                           float (&mx)[4]) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const float x = (masked && j0 + j > lim) ? -INFINITY : v[j];
-        mx[j & 3] = fmaxf(mx[j & 3], x);
-    }
-}
-
-// p = 2^(s c - m) for 16 keys (two 8-key groups of the P tile): adds p to the
-// row sum and stores bf16(p) to the P_hi tile and bf16(p - P_hi) to the P_lo
-// tile (kPbuf bytes later), in the 128-byte swizzled K-major layout.
-template <int kPbuf>
-__device__ __forceinline__ void soft16(const float (&v)[16], int j0, int lim, bool masked,
-                                       float cs, float negm, float2 &lsum, uint8_t *prow, int rr) {
+// p = 2^(s c - m) for 16 keys held in registers; adds p to the row sum and
+// stores bf16(p) at TMEM column hi_col and bf16(p - bf16(p)) at lo_col (8
+// columns each, two keys per column, the lower key in the low half).
+__device__ __forceinline__ void soft16_tmem(const float *v, int j0, int lim, bool masked, float cs,
+                                            float negm, float2 &lsum, uint32_t hi_col,
+                                            uint32_t lo_col) {
     const float2 cs2 = make_float2(cs, cs);
     const float2 nm2 = make_float2(negm, negm);
     const float2 neg1 = make_float2(-1.f, -1.f);
+    uint32_t whi[8], wlo[8];
 #pragma unroll
-    for (int g8 = 0; g8 < 2; ++g8) {
-        uint32_t whi[4], wlo[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int j = g8 * 8 + 2 * h;
-            const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), cs2, nm2);
-            float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            if (masked) {
-                if (j0 + j > lim) p.x = 0.f;
-                if (j0 + j + 1 > lim) p.y = 0.f;
-            }
-            lsum = __fadd2_rn(lsum, p);
-            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p.x, p.y);
-            const float2 lo = __ffma2_rn(__bfloat1622float2(hi2), neg1, p);
-            const __nv_bfloat162 lo2 = __floats2bfloat162_rn(lo.x, lo.y);
-            whi[h] = *reinterpret_cast<const uint32_t *>(&hi2);
-            wlo[h] = *reinterpret_cast<const uint32_t *>(&lo2);
+    for (int h = 0; h < 8; ++h) {
+        const int j = 2 * h;
+        const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), cs2, nm2);
+        float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        if (masked) {
+            if (j0 + j > lim) p.x = 0.f;
+            if (j0 + j + 1 > lim) p.y = 0.f;
         }
-        const int ch = (j0 >> 3) + g8;    // 8-key chunk of the 128-key row
-        const int off = (ch >> 3) * kBlockBytes + (((ch & 7) ^ (rr & 7)) << 4);
-        *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-        *reinterpret_cast<uint4 *>(prow + kPbuf + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+        lsum = __fadd2_rn(lsum, p);
+        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(p.x, p.y);
+        const float2 lo = __ffma2_rn(__bfloat1622float2(hi2), neg1, p);
+        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(lo.x, lo.y);
+        whi[h] = *reinterpret_cast<const uint32_t *>(&hi2);
+        wlo[h] = *reinterpret_cast<const uint32_t *>(&lo2);
     }
+    tmem_st8u(hi_col, whi);
+    tmem_st8u(lo_col, wlo);
 }
 
 template <int D>
@@ -158,9 +146,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *k_full = bars, *k_empty = bars + kStages;
     uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
     uint64_t *q_full = bars + 4 * kStages, *q_empty = q_full + 1;
-    uint64_t *s_full = q_empty + 1, *s_empty = s_full + 2;
-    uint64_t *p_full = s_empty + 2, *p_empty = p_full + 1;
-    uint64_t *o_empty = p_empty + 1, *o_final = o_empty + 1;
+    uint64_t *s_full = q_empty + 1, *s_empty = s_full + kSBufs, *p_full = s_empty + kSBufs;
+    uint64_t *o_empty = p_full + kSBufs, *o_final = o_empty + 1;
     uint64_t *xm_bar = o_final + 1;          // [2 slots][4 row quarters], pair max exchange
     uint64_t *xl_bar = xm_bar + 8;           // [4 row quarters], pair row-sum exchange
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
@@ -177,12 +164,11 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kSBufs; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], kSoftWarps);
+            mbar_init(&s_empty[b], 1);
+            mbar_init(&p_full[b], kSoftWarps);
         }
-        mbar_init(p_full, kSoftWarps);
-        mbar_init(p_empty, 1);
         mbar_init(o_empty, kSoftWarps);
         mbar_init(o_final, 1);
         for (int b = 0; b < 8; ++b) mbar_init(&xm_bar[b], 2);
@@ -244,6 +230,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 *abort_flag = 1;
                 post_status(A.status, KV_ERR_TIMEOUT);
             }
+            // drain: every load this thread issued lands before the CTA exits
             for (int s = 0; s < kStages; ++s) {
                 const long long uses = tcount / kStages + ((tcount % kStages) > s ? 1 : 0);
                 if (uses > 0) {
@@ -258,35 +245,36 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(128, kTileKeys);
             const uint32_t idesc_pv = idesc_bf16_f32_bmn(128, D);
-            const uint32_t q_base = smem_u32(smem + Ly::kQ);
+            const uint64_t qa0 = sdesc_k_sw128(smem_u32(smem + Ly::kQ));
             long long tcount = 0, icount = 0;
             bool ok = true;
             // O += P_hi V + P_lo V for global tile tc (the item's first tile overwrites O)
             auto pv = [&](long long tc, bool first) {
                 const int s = (int)(tc % kStages);
+                const int b = (int)(tc % kSBufs);
                 if (first)
                     ok = ok && mbar_wait(o_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
-                ok = ok && mbar_wait(p_full, (uint32_t)(tc & 1), abort_flag, kWaitNs);
+                ok = ok && mbar_wait(&p_full[b], (uint32_t)((tc / kSBufs) & 1), abort_flag, kWaitNs);
                 ok = ok && mbar_wait(&v_full[s], (uint32_t)((tc / kStages) & 1), abort_flag,
                                      kWaitNs);
                 if (!ok) return;
                 tc_fence_after();
-                const uint64_t vb = sdesc_mn_sw128(smem_u32(smem + Ly::kV + s * Ly::kOp), kBlockBytes);
-                const uint64_t pa0 = sdesc_k_sw128(smem_u32(smem + Ly::kP));
+                const uint64_t vb =
+                    sdesc_mn_sw128(smem_u32(smem + Ly::kV + s * Ly::kOp), kBlockBytes);
+                const uint32_t pcol = tmem + b * kTileKeys;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = sdesc_add(pa0, part * Ly::kPbuf + kb * kBlockBytes + kk * 32);
-                            const uint64_t b = sdesc_add(vb, (kb * 64 + kk * 16) * 128);
-                            if (part == 0 && kb == 0 && kk == 0 && first)
-                                mma_ss_c<false>(tmem + kOCol, a, b, idesc_pv);
-                            else
-                                mma_ss_c<true>(tmem + kOCol, a, b, idesc_pv);
-                        }
-                mma_commit(p_empty);
+                    for (int q = 0; q < kTileKeys / 16; ++q) {
+                        // keys 16q..16q+15: P_hi in columns 16q..16q+7, P_lo in 16q+8..16q+15
+                        const uint32_t a = pcol + q * 16 + part * 8;
+                        const uint64_t bd = sdesc_add(vb, q * 16 * 128);
+                        if (part == 0 && q == 0 && first)
+                            mma_ts_c<false>(tmem + kOCol, a, bd, idesc_pv);
+                        else
+                            mma_ts_c<true>(tmem + kOCol, a, bd, idesc_pv);
+                    }
+                mma_commit(&s_empty[b]);
                 mma_commit(&v_empty[s]);
             };
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
@@ -297,16 +285,15 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_after();
                 for (int i = 0; ok && i < ntiles; ++i) {
                     const long long tc = tcount + i;
-                    const int sb = (int)(tc & 1);
+                    const int b = (int)(tc % kSBufs);
                     const int s = (int)(tc % kStages);
-                    ok = mbar_wait(&s_empty[sb], (uint32_t)((tc >> 1) & 1) ^ 1u, abort_flag,
+                    ok = mbar_wait(&s_empty[b], (uint32_t)((tc / kSBufs) & 1) ^ 1u, abort_flag,
                                    kWaitNs) &&
                          mbar_wait(&k_full[s], (uint32_t)((tc / kStages) & 1), abort_flag, kWaitNs);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t kb0 = sdesc_k_sw128(smem_u32(smem + Ly::kK + s * Ly::kOp));
-                    const uint64_t qa0 = sdesc_k_sw128(q_base);
-                    const uint32_t d_s = tmem + sb * kTileKeys;
+                    const uint32_t d_s = tmem + b * kTileKeys;
                     mma_ss_c<false>(d_s, qa0, kb0, idesc_s);
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
@@ -316,7 +303,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                             if (kb | kk)
                                 mma_ss_c<true>(d_s, sdesc_add(qa0, ko), sdesc_add(kb0, ko), idesc_s);
                         }
-                    mma_commit(&s_full[sb]);
+                    mma_commit(&s_full[b]);
                     mma_commit(&k_empty[s]);
                     if (i > 0) pv(tc - 1, i == 1);
                 }
@@ -333,9 +320,6 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         }
     } else if (run) {
         // ------------------------------------------------------------ softmax
-        // Warps w and w+4 own the same 32 rows (TMEM lane quarter w % 4); warp
-        // half 0 takes keys 0-63 of every tile, half 1 keys 64-127, and O columns
-        // split the same way.  They agree on the row max through shared memory.
         const int ew = warp - 2;
         const int half = ew >> 2;
         const int quarter = warp & 3;
@@ -359,33 +343,30 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             float m_used = -INFINITY, l = 0.f;
             for (int i = 0; ok && i < ntiles; ++i) {
                 const long long tc = tcount + i;
-                const int sb = (int)(tc & 1);
+                const int b = (int)(tc % kSBufs);
                 const int kt = (it.t0 + i) * kTileKeys;
-                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)((tc >> 1) & 1),
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t)((tc / kSBufs) & 1),
                                                        abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
                 const int j0 = half * kHalfKeys;
-                const uint32_t s_col = tmem + lane_addr + sb * kTileKeys + j0;
+                const uint32_t s_col = tmem + lane_addr + b * kTileKeys + j0;
                 // causal mask (only the tiles that reach into the window need it)
                 const bool boundary = kt + kTileKeys - 1 > pos_min;
                 const int lim = row_valid ? (boundary ? pos - kt : kTileKeys - 1) : -1;
                 const bool masked = lim < kTileKeys - 1;
-                // pass A: row max over this warp's 64 keys, then over the pair
+                // row max over this warp's 64 keys, 16 columns at a time
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                {
-                    float bA[16], bB[16];
-                    tmem_ld16(s_col, bA);
+#pragma unroll 1
+                for (int c = 0; c < kHalfKeys / 16; ++c) {
+                    float sv[16];
+                    tmem_ld16(s_col + c * 16, sv);
+                    tmem_ld_wait();
+                    reg_fence(sv);
 #pragma unroll
-                    for (int c = 0; c < kHalfKeys / 16; c += 2) {
-                        tmem_ld_wait();
-                        reg_fence(bA);
-                        tmem_ld16(s_col + (c + 1) * 16, bB);
-                        tile_max16(bA, j0 + c * 16, lim, masked, mx4);
-                        tmem_ld_wait();
-                        reg_fence(bB);
-                        if (c + 2 < kHalfKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
-                        tile_max16(bB, j0 + (c + 1) * 16, lim, masked, mx4);
+                    for (int j = 0; j < 16; ++j) {
+                        const float x = (masked && j0 + c * 16 + j > lim) ? -INFINITY : sv[j];
+                        mx4[j & 3] = fmaxf(mx4[j & 3], x);
                     }
                 }
                 const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
@@ -401,11 +382,16 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const float m_tile = mx * cs;
                 const bool need = m_tile > m_used + kRescaleLog2;
                 const float factor = need ? ex2_approx(m_used - m_tile) : 1.f;
-                // the P buffer is free once P V of tile tc-1 is done; O is then stable
-                ok = __all_sync(0xffffffffu, mbar_wait(p_empty, (uint32_t)(tc & 1) ^ 1u,
-                                                       abort_flag, kWaitNs));
-                if (!ok) break;
                 if (__any_sync(0xffffffffu, need && i > 0)) {
+                    // O holds P V of earlier tiles: rescale it once P V of tile tc-1 is done.
+                    // That P V frees tile tc-1's S/P buffer; the previous phase of that
+                    // barrier (P V of tc-1-kSBufs) is known done, so this cannot alias.
+                    const long long tp = tc - 1;
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&s_empty[(int)(tp % kSBufs)],
+                                              (uint32_t)((tp / kSBufs) & 1), abort_flag, kWaitNs));
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < kHalfD / 16; ++c) {
                         float o[16];
@@ -417,40 +403,29 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         for (int j = 0; j < 16; ++j) o[j] *= factor;
                         tmem_st16(oc, o);
                     }
-                    tmem_st_wait();
                 }
                 if (need) {
                     l *= factor;
                     m_used = m_tile;
                 }
-                // pass B: p = 2^(s c - m), row sum, P_hi / P_lo to shared memory
-                uint8_t *prow = smem + Ly::kP + rr * 128;
+                // P over the S columns just read: each 16-key chunk's own 16 columns
+                // take its P_hi (first 8) and P_lo (last 8)
                 float2 lsum = make_float2(0.f, 0.f);
                 const float negm = m_used == -INFINITY ? 0.f : -m_used;
-                {
-                    float bA[16], bB[16];
-                    tmem_ld16(s_col, bA);
-#pragma unroll
-                    for (int c = 0; c < kHalfKeys / 16; c += 2) {
-                        tmem_ld_wait();
-                        reg_fence(bA);
-                        tmem_ld16(s_col + (c + 1) * 16, bB);
-                        soft16<Ly::kPbuf>(bA, j0 + c * 16, lim, masked, cs, negm, lsum, prow, rr);
-                        tmem_ld_wait();
-                        reg_fence(bB);
-                        if (c + 2 < kHalfKeys / 16) tmem_ld16(s_col + (c + 2) * 16, bA);
-                        soft16<Ly::kPbuf>(bB, j0 + (c + 1) * 16, lim, masked, cs, negm, lsum, prow,
-                                          rr);
-                    }
+#pragma unroll 1
+                for (int c = 0; c < kHalfKeys / 16; ++c) {
+                    float sv[16];
+                    const uint32_t col = s_col + c * 16;
+                    tmem_ld16(col, sv);
+                    tmem_ld_wait();
+                    reg_fence(sv);
+                    soft16_tmem(sv, j0 + c * 16, lim, masked, cs, negm, lsum, col, col + 8);
                 }
                 l += lsum.x + lsum.y;
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
+                if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
             // item end: read O once the last P V is done, write this split's partial

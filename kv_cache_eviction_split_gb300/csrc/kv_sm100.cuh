@@ -144,6 +144,34 @@ __device__ __forceinline__ void mma_ss_c(uint32_t d_tmem, uint64_t a_desc, uint6
             : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A is read from TMEM (lane = row
+// of A, 32-bit column c = elements 2c and 2c+1 of the K dimension as bf16x2).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc) {
+    if (kAccumulate)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(b_desc), "r"(idesc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(b_desc), "r"(idesc)
+            : "memory");
+}
+
+// Stores 8 consecutive 32-bit columns (raw bits) for the warp's 32 lanes.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+
 // Descriptor of the same operand `bytes` further on (the start-address field
 // holds address / 16 in bits 0-13 and cannot carry within shared memory).
 __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
