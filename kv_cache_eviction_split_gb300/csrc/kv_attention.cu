@@ -106,7 +106,8 @@ __device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, c
 // p = 2^(s c - m) for 16 keys held in registers; adds p to the row sum and
 // stores bf16(p) at TMEM column hi_col and bf16(p - bf16(p)) at lo_col (8
 // columns each, two keys per column, the lower key in the low half).
-__device__ __forceinline__ void soft16_tmem(const float *v, int j0, int lim, bool masked, float cs,
+template <bool kMasked>
+__device__ __forceinline__ void soft16_tmem(const float *v, int j0, int lim, float cs,
                                             float negm, float2 &lsum, uint32_t hi_col,
                                             uint32_t lo_col) {
     const float2 cs2 = make_float2(cs, cs);
@@ -118,7 +119,7 @@ __device__ __forceinline__ void soft16_tmem(const float *v, int j0, int lim, boo
         const int j = 2 * h;
         const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), cs2, nm2);
         float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-        if (masked) {
+        if (kMasked) {
             if (j0 + j > lim) p.x = 0.f;
             if (j0 + j + 1 > lim) p.y = 0.f;
         }
@@ -354,7 +355,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 // causal mask (only the tiles that reach into the window need it)
                 const bool boundary = kt + kTileKeys - 1 > pos_min;
                 const int lim = row_valid ? (boundary ? pos - kt : kTileKeys - 1) : -1;
-                const bool masked = lim < kTileKeys - 1;
+                // warp-uniform: the mask code only runs on tiles that need it
+                const bool masked = __any_sync(0xffffffffu, lim < kTileKeys - 1);
                 // row max over this warp's 64 keys, 16 columns at a time
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
@@ -363,10 +365,15 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     tmem_ld16(s_col + c * 16, sv);
                     tmem_ld_wait();
                     reg_fence(sv);
+                    if (masked) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float x = (masked && j0 + c * 16 + j > lim) ? -INFINITY : sv[j];
-                        mx4[j & 3] = fmaxf(mx4[j & 3], x);
+                        for (int j = 0; j < 16; ++j) {
+                            const float x = (j0 + c * 16 + j > lim) ? -INFINITY : sv[j];
+                            mx4[j & 3] = fmaxf(mx4[j & 3], x);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
                     }
                 }
                 const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
@@ -419,7 +426,10 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     tmem_ld16(col, sv);
                     tmem_ld_wait();
                     reg_fence(sv);
-                    soft16_tmem(sv, j0 + c * 16, lim, masked, cs, negm, lsum, col, col + 8);
+                    if (masked)
+                        soft16_tmem<true>(sv, j0 + c * 16, lim, cs, negm, lsum, col, col + 8);
+                    else
+                        soft16_tmem<false>(sv, j0 + c * 16, lim, cs, negm, lsum, col, col + 8);
                 }
                 l += lsum.x + lsum.y;
                 tmem_st_wait();
