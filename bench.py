@@ -37,8 +37,6 @@ METRIC = "KV tokens scored+selected+compacted/s at n=128K; achieved HBM GB/s vs 
 UNIT = "unit-tokens/s"
 DEFAULT_WORKLOAD = "long_32L_8kv_32q_d128_n131072_pyramid10"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# fp32 FMA ceiling of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
-ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def parse_args(argv=None):
@@ -243,9 +241,14 @@ STAGES = ["attention", "rescore", "select", "compact"]
 LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "select": 1, "compact": 1}
 STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
                  "select": "select_kernel", "compact": "compact_kernel"}
-SCORE_ENGINE = "tensor"
-# DRAM bytes per launch from an ncu capture of the current kernels (None: not taken)
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch from the single-pass ncu capture of the
+# current kernels on the default workload (profiles/dram_traffic_long_32L_8kv_n131072.md).
+# Only valid for that workload and these kernel versions; None elsewhere.
+TRAFFIC_WORKLOAD = DEFAULT_WORKLOAD
+TRAFFIC = {"attn_tc_kernel": 17199287296 + 266214400,
+           "rescore_tc_kernel": 17266129408 + 267070208,
+           "select_kernel": 668149504 + 8272640,
+           "compact_kernel": 1731538176 + 1657757952}
 
 
 def product_budgets(kv, wl):
@@ -265,28 +268,34 @@ def product_budgets(kv, wl):
 
 
 def stage_roofline(stage, ms, wl, budgets, peaks):
+    """Roofline of one stage's kernel from its algorithmic bytes (and, for the two
+    scoring passes, their algorithmic tensor flops: two d-long dot products per
+    (window row, visible key) pair each)."""
     d = wl.head_dim
     units = wl.num_units
     n_tot = sum(wl.seq_lengths())
+    L, H = wl.num_layers, wl.num_kv_heads
     rows = int(np.asarray(budgets).sum())
-    if stage in ("attention", "rescore"):
-        flops = pass_pairs(wl) * 4 * d       # two d-long dot products per (row, key)
-        achieved = flops / (ms * 1e-3) / 1e12
-        if SCORE_ENGINE == "tensor":
-            peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
-            bound = "tensor"
-        else:
-            peak = ALU_FP32_TFLOPS
-            bound = "alu"
-        return {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "algorithmic": flops}
-    if stage == "select":
-        nbytes = n_tot * wl.num_layers * wl.num_kv_heads * 4 + rows * 4 + 8 * (units + 1) * 2
+    kv = kv_cache_bytes(L, H, d, n_tot)
+    q = wl.num_requests * L * wl.num_q_heads * wl.window * d * 2
+    keys = n_tot * L * H
+    if stage == "attention":
+        nbytes = kv + q                        # K, V and the window queries, once
+    elif stage == "rescore":
+        nbytes = kv + q + keys * 4             # ... plus one fp32 score per key
+    elif stage == "select":
+        nbytes = keys * 4 + rows * 4 + 8 * (units + 1) * 2
     else:
         nbytes = rows * (2 * d * 2) * 2 + rows * 4 + 8 * (units + 1)
     achieved = nbytes / (ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "algorithmic": nbytes}
+    out = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": achieved / peaks["hbm_gbs"], "algorithmic_bytes": nbytes}
+    if stage in ("attention", "rescore"):
+        flops = pass_pairs(wl) * 4 * d
+        tpeak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        out["tensor"] = {"algorithmic_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
+                         "peak_tflops": tpeak, "frac": flops / (ms * 1e-3) / 1e12 / tpeak}
+    return out
 
 
 def gpu_uuid(torch, dev):
@@ -391,13 +400,16 @@ def main(argv=None):
 
     dominant = max(("attention", "rescore", "select", "compact"), key=lambda s: stage_ms[s])
     roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks)
+    traffic = TRAFFIC.get(STAGE_KERNELS[dominant]) if wl.name == TRAFFIC_WORKLOAD else None
     roof.update({"kernel": STAGE_KERNELS[dominant], "peak_source": peak_src,
-                 "traffic": TRAFFIC.get(STAGE_KERNELS[dominant])})
+                 "traffic": traffic, "stage_ms": stage_ms[dominant],
+                 "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks)["frac"]
+                                for s in STAGES}})
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if SCORE_ENGINE == "alu" else "bf16", "data": "synthetic",
+            "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "layers": wl.num_layers,
                        "kv_heads": wl.num_kv_heads, "q_heads": wl.num_q_heads,
                        "head_dim": wl.head_dim, "n": wl.seq_lengths(), "window": wl.window,
