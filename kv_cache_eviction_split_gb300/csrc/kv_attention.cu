@@ -46,6 +46,7 @@ using namespace sm100;
 constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
 constexpr int kStages = 3;
+constexpr int kPrefetchTiles = 4;   // K/V tiles requested into L2 ahead of the smem loads
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -196,6 +197,33 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) {
             long long tcount = 0, icount = 0;
             bool ok = true;
+            // L2 prefetch cursor: walks the same (item, tile) sequence as the loads,
+            // kPrefetchTiles tiles ahead of them, so the smem ring's loads hit L2.
+            long long pf_item = blockIdx.x, pf_row0 = 0;
+            int pf_t = 0, pf_end = 0;
+            auto pf_open = [&]() {
+                if (pf_item < A.total_items) {
+                    const Item pi = decode_item(pf_item, A, P);
+                    pf_row0 = unit_info(P, pi.u, P.cu).kv_row0;
+                    pf_t = pi.t0;
+                    pf_end = pi.t1;
+                }
+            };
+            auto pf_step = [&]() {
+                if (pf_item >= A.total_items) return;
+                const int ky = (int)(pf_row0 + (long long)pf_t * kTileKeys);
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb) {
+                    tma_prefetch_2d(&tm_k, kb * 64, ky);
+                    tma_prefetch_2d(&tm_v, kb * 64, ky);
+                }
+                if (++pf_t >= pf_end) {
+                    pf_item += gridDim.x;
+                    pf_open();
+                }
+            };
+            pf_open();
+            for (int i = 0; i < kPrefetchTiles; ++i) pf_step();
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
@@ -210,6 +238,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const int s = (int)(tcount % kStages);
                     const uint32_t par = (uint32_t)((tcount / kStages) & 1) ^ 1u;
                     const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
+                    pf_step();
                     ok = mbar_wait(&k_empty[s], par, abort_flag, kWaitNs);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&k_full[s], Ly::kOp);

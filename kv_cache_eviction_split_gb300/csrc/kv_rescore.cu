@@ -3,20 +3,23 @@
 // For every key j of a unit and every window row r that sees it:
 //     s   = q_r . k_j                         (tensor core, fp32 in TMEM)
 //     X   = (a_hi_r + a_lo_r) . v_j           (tensor core, two bf16 MMAs)
-//     e   = 2^(s * scale * log2 e - m_r)      p = e / l_r
+//     p   = 2^(s * scale * log2 e - m_r - log2 l_r)     (= e / l_r)
 //     x   = ||a_r||^2 - 2 X + ||v_j||^2      = ||a_r - v_j||^2 (the expansion the
 //                                              DropKV scoring-kernel description uses)
-//     S_j += e / (l_r - e) * sqrt(x)         = p/(1-p) * ||a_r - v_j||
+//     S_j += p / (1 - p) * sqrt(x)           = p/(1-p) * ||a_r - v_j||
 // (DropKV, Key Contributions 1 and Methodology in Plain English).  a = a_hi +
 // a_lo is the pass-1 output split into two bf16 halves, so the expansion keeps
 // ~16 bits of a instead of bf16's 8.
 //
 // Orientation is key-major: one MMA tile is 128 keys (M, TMEM lanes) by the
-// rows of a 128-row chunk of the unit's window rows (N), so each epilogue
-// thread owns one key and sums its score over rows without any cross-thread
-// reduction.  Work items = (unit, 64-key-tile block, row chunk); a persistent
-// grid walks them round-robin, chunk fastest, so the chunks of one key block
-// run on neighbouring SMs at the same time and share K/V through L2.
+// rows of a 128-row chunk of the unit's window rows (N).  The epilogue reads
+// TMEM in the 16x256b shape, so each thread holds two keys and a fixed set of
+// 32 rows: the per-row statistics stay in registers for the whole work item
+// and the inner loop touches no shared memory (the SS MMAs keep the shared
+// memory data path busy, and loads issued behind them wait long).  Work items
+// = (unit, 64-key-tile block, row chunk); a persistent grid walks them
+// round-robin, chunk fastest, so the chunks of one key block run on
+// neighbouring SMs at the same time and share K/V through L2.
 //
 // Warp roles (320 threads):
 //   warp 0      TMA producer: the chunk's Q, a_hi, a_lo once per item; K and V
@@ -25,8 +28,9 @@
 //               X = V a_hi^T + V a_lo^T over all rows of the chunk, into one of
 //               two TMEM buffers, so tile i+1 computes while tile i is scored
 //               and a K/V stage frees as soon as its MMAs complete
-//   warps 2-9   epilogue: group g (4 warps) handles half g of the rows; group 0
-//               hands its per-key partial sums to group 1 through a smem ring
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) + 16 h .. +15
+//               (h = 0 for warps 2-5, 1 for 6-9) over all rows of the chunk;
+//               the four threads that share a key add their sums by shuffles
 // Every wait is bounded: on expiry the kernel posts KV_ERR_TIMEOUT, the other
 // roles drain out, TMEM is freed and the kernel returns.
 #include <algorithm>
@@ -43,6 +47,7 @@ constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
 constexpr int kTilesPerItem = 64;
 constexpr int kStages = 2;
+constexpr int kPrefetchTiles = 4;   // K/V tiles requested into L2 ahead of the smem loads
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -57,12 +62,8 @@ struct Layout {
     static constexpr int kAlo = kAhi + kOp;
     static constexpr int kK = kAlo + kOp;
     static constexpr int kV = kK + kStages * kOp;
-    static constexpr int kStats = kV + kStages * kOp;      // [2][32] float4 (-m0,-m1,l0,l1)
-    static constexpr int kA2 = kStats + 2 * 32 * 16;       // [2][32] float2 ||a||^2 pairs
-    static constexpr int kRmod = kA2 + 2 * 32 * 8;         // [2][64] uint16 row % w
-    static constexpr int kRing = kRmod + 2 * 64 * 2;       // [2 slots][128] float
-    static constexpr int kBars = kRing + 2 * 128 * 4;
-    static constexpr int kNumBars = 4 * kStages + 2 + 8;
+    static constexpr int kBars = kV + kStages * kOp;
+    static constexpr int kNumBars = 4 * kStages + 2 + 4;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -102,64 +103,117 @@ __device__ __forceinline__ Item decode_item(long long item, const RescoreArgs &A
     return it;
 }
 
-__device__ __forceinline__ int chunk_half_rows(const DevProblem &P, int c) {
+// Rows of chunk c rounded up to a multiple of 32 (the MMA N and the TMEM columns used).
+__device__ __forceinline__ int chunk_rows_n(const DevProblem &P, int c) {
     const int rc = min(kChunkRows, P.rows - c * kChunkRows);
-    return ((rc + 31) / 32) * 16;   // half of the chunk rows rounded up to 32
+    return ((rc + 31) / 32) * 32;
 }
 
-// ||v||^2 of one row of a swizzled [128][D] bf16 tile.
+// Adds the squares of the two bf16 halves of `w` to `acc` (fp32 products of bf16
+// are exact; one rounding per addition).
+__device__ __forceinline__ void sq_acc_bf16x2(float &acc, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, lo, lo, %0;\n\tfma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+}
+
+// Part of ||v||^2 of one row of a swizzled [128][D] bf16 tile: the 16-byte
+// chunks {part, part + 4} of each 64-column block.  The four threads that share
+// a row take part = 0..3; which of the two chunks comes first alternates with
+// the row's parity, so the 8 threads of a quarter-warp (two rows) read 8
+// different bank groups.
 template <int D>
-__device__ __forceinline__ float row_sqnorm(const uint8_t *tile, int row) {
-    float acc = 0.f;
+__device__ __forceinline__ float row_sqnorm_part(const uint8_t *tile, int row, int part) {
+    float acc[2] = {0.f, 0.f};
 #pragma unroll
     for (int kb = 0; kb < D / 64; ++kb) {
         const uint8_t *base = tile + kb * kBlockBytes + row * 128;
 #pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
+        for (int h = 0; h < 2; ++h) {
+            const int c16 = part + 4 * (h ^ (row & 1));
             const uint4 w = *reinterpret_cast<const uint4 *>(base + ((c16 ^ (row & 7)) << 4));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = __uint_as_float(ws[i] << 16);
-                const float hi = __uint_as_float(ws[i] & 0xFFFF0000u);
-                acc = fmaf(lo, lo, acc);
-                acc = fmaf(hi, hi, acc);
-            }
+            sq_acc_bf16x2(acc[h], w.x);
+            sq_acc_bf16x2(acc[h], w.y);
+            sq_acc_bf16x2(acc[h], w.z);
+            sq_acc_bf16x2(acc[h], w.w);
         }
     }
-    return acc;
+    return acc[0] + acc[1];
 }
 
-// Adds the terms of 16 rows (columns of one TMEM load) for this thread's key:
-// e/(l - e) * sqrt(x) with e = 2^(s c - m), x = max(||a||^2 - 2X + ||v||^2, 0),
-// written as e * x * rsqrt((l - e)^2 x + tiny) so one MUFU op gives sqrt(x)/(l-e)
-// and x = 0 gives 0.  Two rows at a time in packed f32x2 arithmetic.
-__device__ __forceinline__ void rescore16(const float (&sv)[16], const float (&xv)[16],
-                                          const float4 *st, const float2 *a2p,
-                                          const uint16_t *rmod, bool boundary, int jrel,
-                                          float cscale, float2 v2v2, float2 &acc) {
-    const float2 cs2 = make_float2(cscale, cscale);
-    const float2 neg1 = make_float2(-1.f, -1.f);
-    const float2 neg2 = make_float2(-2.f, -2.f);
-    const float2 tiny = make_float2(1e-30f, 1e-30f);
+// One (row pair, key) term pair: p/(1 - p) * sqrt(x) with p = 2^(s c - m'),
+// x = max(||a||^2 - 2X + ||v||^2, 0), written as p * x * rsqrt((1 - p)^2 x + tiny)
+// so one MUFU op gives sqrt(x)/(1-p) and x = 0 gives 0.  `vis` = 0 drops a row
+// that does not see the key.
+__device__ __forceinline__ void term_pair(float2 sp, float2 xp, float2 nm, float2 a2, float2 v2,
+                                          float cscale, float2 &acc, bool vis0 = true,
+                                          bool vis1 = true) {
+    const float2 t = __ffma2_rn(sp, make_float2(cscale, cscale), nm);
+    float2 pr = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (!vis0) pr.x = 0.f;
+    if (!vis1) pr.y = 0.f;
+    const float2 den = __ffma2_rn(pr, make_float2(-1.f, -1.f), make_float2(1.f, 1.f));
+    const float2 av = __fadd2_rn(a2, v2);
+    float2 x = __ffma2_rn(xp, make_float2(-2.f, -2.f), av);
+    x.x = fmaxf(x.x, 0.f);
+    x.y = fmaxf(x.y, 0.f);
+    const float2 y = __ffma2_rn(__fmul2_rn(den, den), x, make_float2(1e-30f, 1e-30f));
+    const float2 px = __fmul2_rn(pr, x);
+    acc = __ffma2_rn(px, make_float2(rsqrt_approx(y.x), rsqrt_approx(y.y)), acc);
+}
+
+// Adds the terms of one 32-column group for the thread's two keys: sv / xv are
+// 16x256b.x4 loads of S and X (v[4r], v[4r+1]: key 0, rows 2 part + 8r + {0,1};
+// v[4r+2], v[4r+3]: key 1, the same rows).  Every row sees both keys.
+__device__ __forceinline__ void rescore_x4(const float (&sv)[16], const float (&xv)[16],
+                                           const float2 *nm, const float2 *a2, float cscale,
+                                           const float2 (&v2)[2], float2 (&acc)[2]) {
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const float4 s4 = st[p];
-        const float2 t = __ffma2_rn(make_float2(sv[2 * p], sv[2 * p + 1]), cs2,
-                                    make_float2(s4.x, s4.y));
-        const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-        const float2 den = __ffma2_rn(e, neg1, make_float2(s4.z, s4.w));
-        const float2 av = __fadd2_rn(a2p[p], v2v2);
-        float2 x = __ffma2_rn(make_float2(xv[2 * p], xv[2 * p + 1]), neg2, av);
-        x.x = fmaxf(x.x, 0.f);
-        x.y = fmaxf(x.y, 0.f);
-        const float2 y = __ffma2_rn(__fmul2_rn(den, den), x, tiny);
-        float2 ex = __fmul2_rn(e, x);
-        if (boundary) {
-            if (jrel > (int)rmod[2 * p]) ex.x = 0.f;
-            if (jrel > (int)rmod[2 * p + 1]) ex.y = 0.f;
-        }
-        acc = __ffma2_rn(ex, make_float2(rsqrt_approx(y.x), rsqrt_approx(y.y)), acc);
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            term_pair(make_float2(sv[4 * r + 2 * k], sv[4 * r + 2 * k + 1]),
+                      make_float2(xv[4 * r + 2 * k], xv[4 * r + 2 * k + 1]), nm[r], a2[r], v2[k],
+                      cscale, acc[k]);
+}
+
+// -m' = -(m + log2 l) and ||a||^2 of one unit-local row; padding rows (>= rows)
+// get p = 0.
+__device__ __forceinline__ void row_stats(const float2 *ml, const float *a2, int row, int rows,
+                                          float &nm, float &aa) {
+    if (row < rows) {
+        const float2 v = ml[row];
+        nm = -(v.x + log2f(v.y));
+        aa = a2[row];
+    } else {
+        nm = -INFINITY;
+        aa = 0.f;
+    }
+}
+
+// As rescore_x4 for a tile that reaches the observation window, where a row at
+// window slot t sees key j only when j - (n - w) <= t (jrel[k] = j_k - (n - w)).
+// Recomputes the row statistics from the unit's arrays (row0 = unit-local row of
+// pair 0): this path runs for one or two tiles per unit, in a loop of its own so
+// the masks stay out of the unrolled code of the other tiles.
+__device__ __forceinline__ void rescore_x4_window(const float (&sv)[16], const float (&xv)[16],
+                                               const float2 *ml, const float *a2g, int rows,
+                                               int row0, int w, const int (&jrel)[2],
+                                               float cscale, const float2 (&v2)[2],
+                                               float2 (&acc)[2]) {
+    for (int r = 0; r < 4; ++r) {
+        const int row = row0 + 8 * r;
+        float n0, n1, q0, q1;
+        row_stats(ml, a2g, row, rows, n0, q0);
+        row_stats(ml, a2g, row + 1, rows, n1, q1);
+        const int rm0 = row % w;
+        const int rm1 = rm0 + 1 == w ? 0 : rm0 + 1;
+        for (int k = 0; k < 2; ++k)
+            term_pair(make_float2(sv[4 * r + 2 * k], sv[4 * r + 2 * k + 1]),
+                      make_float2(xv[4 * r + 2 * k], xv[4 * r + 2 * k + 1]),
+                      make_float2(n0, n1), make_float2(q0, q1), v2[k], cscale, acc[k],
+                      jrel[k] <= rm0, jrel[k] <= rm1);
     }
 }
 
@@ -179,7 +233,6 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
     uint64_t *qa_full = bars + 4 * kStages, *qa_empty = qa_full + 1;
     uint64_t *tm_full = qa_empty + 1, *tm_empty = tm_full + 2;
-    uint64_t *part_full = tm_empty + 2, *part_empty = part_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
@@ -197,8 +250,6 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         for (int h = 0; h < 2; ++h) {
             mbar_init(&tm_full[h], 1);
             mbar_init(&tm_empty[h], kEpiWarps);
-            mbar_init(&part_full[h], 4);
-            mbar_init(&part_empty[h], 4);
         }
         fence_barrier_init();
     }
@@ -224,6 +275,33 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) {
             long long tcount = 0, icount = 0;
             bool ok = true;
+            // L2 prefetch cursor: walks the same (item, tile) sequence as the loads,
+            // kPrefetchTiles tiles ahead of them, so the smem ring's loads hit L2.
+            long long pf_item = blockIdx.x, pf_row0 = 0;
+            int pf_t = 0, pf_end = 0;
+            auto pf_open = [&]() {
+                if (pf_item < A.total_items) {
+                    const Item pi = decode_item(pf_item, A, P);
+                    pf_row0 = unit_info(P, pi.u, P.cu).kv_row0;
+                    pf_t = pi.t_begin;
+                    pf_end = pi.t_end;
+                }
+            };
+            auto pf_step = [&]() {
+                if (pf_item >= A.total_items) return;
+                const int ky = (int)(pf_row0 + (long long)pf_t * kTileKeys);
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb) {
+                    tma_prefetch_2d(&tm_k, kb * 64, ky);
+                    tma_prefetch_2d(&tm_v, kb * 64, ky);
+                }
+                if (++pf_t >= pf_end) {
+                    pf_item += gridDim.x;
+                    pf_open();
+                }
+            };
+            pf_open();
+            for (int i = 0; i < kPrefetchTiles; ++i) pf_step();
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
@@ -242,6 +320,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const int s = (int)(tcount % kStages);
                     const uint32_t par = (uint32_t)((tcount / kStages) & 1) ^ 1u;
                     const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
+                    pf_step();
                     ok = mbar_wait(&k_empty[s], par, abort_flag, kWaitNs);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
@@ -280,8 +359,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             bool ok = true;
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
-                const int rch = chunk_half_rows(P, it.c);
-                const uint32_t idesc = idesc_bf16_f32(128, 2 * rch);
+                const uint32_t idesc = idesc_bf16_f32(128, chunk_rows_n(P, it.c));
                 ok = mbar_wait(qa_full, (uint32_t)(icount & 1), abort_flag, kWaitNs);
                 if (!ok) break;
                 tc_fence_after();
@@ -343,47 +421,28 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         }
     } else if (run) {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2;
-        const int g = ew >> 2;                 // half of the chunk rows
-        const int quarter = warp & 3;          // TMEM lane quarter this warp may access
-        const int key_local = quarter * 32 + lane;
-        const int tg = (ew & 3) * 32 + lane;   // thread index within the group
-        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        float4 *stats = reinterpret_cast<float4 *>(smem + Ly::kStats) + g * 32;
-        float2 *a2s = reinterpret_cast<float2 *>(smem + Ly::kA2) + g * 32;
-        uint16_t *rmod = reinterpret_cast<uint16_t *>(smem + Ly::kRmod) + g * 64;
-        float *ring = reinterpret_cast<float *>(smem + Ly::kRing);
+        const int quarter = warp & 3;                  // TMEM lane quarter of this warp
+        const int lane_base = quarter * 32 + ((warp - 2) >> 2) * 16;
+        const int part = lane & 3;
+        const int key0 = lane_base + (lane >> 2);      // tile-local keys: key0, key0 + 8
+        const uint32_t lane_addr = (uint32_t)lane_base << 16;
         const float cscale = P.scale_log2;
         long long tcount = 0;
         bool ok = true;
         for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
             const Item it = decode_item(item, A, P);
             const UnitInfo U = unit_info(P, it.u, P.cu);
-            const int rch = chunk_half_rows(P, it.c);
-            const int row_base = it.c * kChunkRows + g * rch;
-            asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
-            for (int pp = tg; pp < rch / 2; pp += 128) {
-                float nm[2], ll[2], aa[2];
+            const int groups = chunk_rows_n(P, it.c) / 32;
+            const int row_first = it.c * kChunkRows + 2 * part;   // unit-local row of pair 0
+            // statistics of the thread's rows (pair rp: rows row_first + 8 rp + {0, 1})
+            const float2 *u_ml = A.stat_ml + it.u * P.rows;
+            const float *u_a2 = A.stat_a2 + it.u * P.rows;
+            float2 nm[16], a2[16];
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int row = row_base + 2 * pp + k2;
-                    if (row < P.rows) {
-                        const float2 ml = A.stat_ml[it.u * P.rows + row];
-                        nm[k2] = -ml.x;
-                        ll[k2] = ml.y;
-                        aa[k2] = A.stat_a2[it.u * P.rows + row];
-                        rmod[2 * pp + k2] = (uint16_t)(row % P.w);
-                    } else {   // padding row: e = 0, so its term is 0
-                        nm[k2] = -INFINITY;
-                        ll[k2] = 1.f;
-                        aa[k2] = 0.f;
-                        rmod[2 * pp + k2] = 0;
-                    }
-                }
-                stats[pp] = make_float4(nm[0], nm[1], ll[0], ll[1]);
-                a2s[pp] = make_float2(aa[0], aa[1]);
+            for (int rp = 0; rp < 16; ++rp) {
+                row_stats(u_ml, u_a2, row_first + 8 * rp, P.rows, nm[rp].x, a2[rp].x);
+                row_stats(u_ml, u_a2, row_first + 8 * rp + 1, P.rows, nm[rp].y, a2[rp].y);
             }
-            asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
             float *out = A.out + (long long)it.c * A.out_stride + U.kv_row0;
             const int pos0 = U.n - P.w;
             for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
@@ -396,65 +455,58 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                     mbar_wait(&v_full[s], spar, abort_flag, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
-                const float v2 = row_sqnorm<D>(smem + Ly::kV + s * Ly::kOp, key_local);
+                const uint32_t s_col = tmem + lane_addr + b * 256;
+                const uint32_t x_col = s_col + 128;
+                float sA[16], xA[16];
+                // ||v||^2 of the two keys, each from four threads' parts
+                const uint8_t *vt = smem + Ly::kV + s * Ly::kOp;
+                float q0 = row_sqnorm_part<D>(vt, key0, part);
+                float q1 = row_sqnorm_part<D>(vt, key0 + 8, part);
+                q0 += __shfl_xor_sync(0xffffffffu, q0, 1);
+                q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+                q0 += __shfl_xor_sync(0xffffffffu, q0, 2);
+                q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&v_empty[s]);
-                const int j = t * kTileKeys + key_local;
+                const float2 v2[2] = {make_float2(q0, q0), make_float2(q1, q1)};
+                const int j0 = t * kTileKeys + key0;
                 const bool boundary = t * kTileKeys + kTileKeys - 1 > pos0;
-                // rows with j > pos0 + (row % w) do not see key j (only near the window)
-                const int jrel = j - pos0;
-                float2 acc = make_float2(0.f, 0.f);
-                const float2 v2v2 = make_float2(v2, v2);
-                const uint32_t s_col = tmem + lane_addr + b * 256 + g * rch;
-                const uint32_t x_col = s_col + 128;
-                float sA[16], xA[16], sB[16], xB[16];
-                tmem_ld16(s_col, sA);
-                tmem_ld16(x_col, xA);
-                for (int cc = 0; cc < rch; cc += 32) {
-                    tmem_ld_wait();
-                    reg_fence(sA);
-                    reg_fence(xA);
-                    const bool second = cc + 16 < rch;
-                    if (second) {
-                        tmem_ld16(s_col + cc + 16, sB);
-                        tmem_ld16(x_col + cc + 16, xB);
-                    }
-                    rescore16(sA, xA, stats + cc / 2, a2s + cc / 2, rmod + cc, boundary, jrel,
-                              cscale, v2v2, acc);
-                    if (second) {
-                        tmem_ld_wait();
-                        reg_fence(sB);
-                        reg_fence(xB);
-                        if (cc + 32 < rch) {
-                            tmem_ld16(s_col + cc + 32, sA);
-                            tmem_ld16(x_col + cc + 32, xA);
+                const int jrel[2] = {j0 - pos0, j0 + 8 - pos0};
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                if (!boundary) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (g < groups) {
+                            tmem_ld16x256_x4(s_col + g * 32, sA);
+                            tmem_ld16x256_x4(x_col + g * 32, xA);
+                            tmem_ld_wait();
+                            reg_fence(sA);
+                            reg_fence(xA);
+                            rescore_x4(sA, xA, nm + 4 * g, a2 + 4 * g, cscale, v2, acc);
                         }
-                        rescore16(sB, xB, stats + cc / 2 + 8, a2s + cc / 2 + 8, rmod + cc + 16,
-                                  boundary, jrel, cscale, v2v2, acc);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int g = 0; g < groups; ++g) {
+                        tmem_ld16x256_x4(s_col + g * 32, sA);
+                        tmem_ld16x256_x4(x_col + g * 32, xA);
+                        tmem_ld_wait();
+                        reg_fence(sA);
+                        reg_fence(xA);
+                        rescore_x4_window(sA, xA, u_ml, u_a2, P.rows, row_first + 32 * g, P.w,
+                                          jrel, cscale, v2, acc);
                     }
                 }
-                const float acc_sum = acc.x + acc.y;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tm_empty[b]);
-                const int slot = (int)(tcount & 1);
-                const uint32_t rpar = (uint32_t)((tcount >> 1) & 1);
-                if (g == 0) {
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&part_empty[slot], rpar ^ 1u, abort_flag, kWaitNs));
-                    if (!ok) break;
-                    ring[slot * 128 + key_local] = acc_sum;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&part_full[slot]);
-                } else {
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&part_full[slot], rpar, abort_flag, kWaitNs));
-                    if (!ok) break;
-                    const float tot = acc_sum + ring[slot * 128 + key_local];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&part_empty[slot]);
-                    if (j < U.n) out[j] = tot;
-                }
+                float s0 = acc[0].x + acc[0].y, s1 = acc[1].x + acc[1].y;
+                s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+                s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+                if (part == 0 && j0 < U.n) out[j0] = s0;
+                if (part == 1 && j0 + 8 < U.n) out[j0 + 8] = s1;
             }
         }
         if (!ok) {
