@@ -74,11 +74,12 @@ ScoreWs score_ws_layout(const DevProblem &P, void *base) {
     };
     const size_t U = (size_t)P.units, S = (size_t)P.max_splits, Rr = (size_t)P.rows, D = P.d;
     ws.chunks = (P.rows + 127) / 128;
+    ws.parts = ws.chunks == 1 ? 2 : 1;
     ws.a_rows = ws.chunks * 128;
-    const size_t AR = (size_t)ws.a_rows;
+    const size_t AR = (size_t)ws.a_rows, SP = S * (size_t)ws.parts;
     ws.status = reinterpret_cast<int *>(take(kHeaderBytes));
-    ws.part_ml = reinterpret_cast<float2 *>(take(U * S * Rr * sizeof(float2)));
-    ws.part_o = reinterpret_cast<float *>(take(U * S * Rr * D * sizeof(float)));
+    ws.part_ml = reinterpret_cast<float2 *>(take(U * SP * Rr * sizeof(float2)));
+    ws.part_o = reinterpret_cast<float *>(take(U * SP * Rr * D * sizeof(float)));
     ws.stat_ml = reinterpret_cast<float2 *>(take(U * Rr * sizeof(float2)));
     ws.stat_a2 = reinterpret_cast<float *>(take(U * Rr * sizeof(float)));
     ws.a_hi = reinterpret_cast<__nv_bfloat16 *>(take(U * AR * D * sizeof(__nv_bfloat16)));

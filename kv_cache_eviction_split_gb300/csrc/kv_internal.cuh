@@ -55,8 +55,8 @@ __host__ __device__ inline UnitInfo unit_info(const DevProblem &P, long long u, 
 // Score workspace carve-up (all offsets 256-byte aligned).
 struct ScoreWs {
     int *status;
-    float2 *part_ml;          // [units][max_splits][rows]  (m in log2 units, l)
-    float *part_o;            // [units][max_splits][rows][d]
+    float2 *part_ml;          // [units][max_splits * parts][rows]  (m in log2 units, l)
+    float *part_o;            // [units][max_splits * parts][rows][d]
     float2 *stat_ml;          // [units][rows]  merged (m, l)
     float *stat_a2;           // [units][rows]  ||a_hi + a_lo||^2
     __nv_bfloat16 *a_hi;      // [units][a_rows][d]  bf16(a)
@@ -65,6 +65,7 @@ struct ScoreWs {
     float *part_scores;       // [chunks][L*H*N_tot] when chunks > 1
     int a_rows;               // chunks * 128
     int chunks;               // ceil(rows / 128)
+    int parts;                // pass-1 partials per split: 2 with one chunk, else 1
     size_t total;
 };
 

@@ -1,10 +1,11 @@
 // kv_score.cu -- the split-K merge between the two streaming passes of the
 // DropKV removal score.
 //
-// Pass 1 (kv_attention.cu) leaves, for every unit, split of its keys and window
-// row (query head g of the GQA group, window slot t, causal position n - w + t),
-// a partial (running max m in log2 units, sum l, unnormalised output o).  The
-// merge combines the splits with the log-sum-exp rescale and stores, per row,
+// Pass 1 (kv_attention.cu) leaves, for every unit, split of its keys (one or two
+// partials per split) and window row (query head g of the GQA group, window slot
+// t, causal position n - w + t), a partial (running max m in log2 units, sum l,
+// unnormalised output o).  The merge combines them with the log-sum-exp rescale
+// and stores, per row,
 // (m, l), a = o / l split into a_hi = bf16(a) and a_lo = bf16(a - a_hi), and
 // ||a_hi + a_lo||^2 -- the operands of the rescoring pass (kv_rescore.cu).
 #include <cfloat>
@@ -30,19 +31,24 @@ attn_merge_kernel(DevProblem P, ScoreWs ws) {
         return;
     }
     const UnitInfo U = unit_info(P, u, P.cu);
-    const int nsplit = (U.n + kSplitKeys - 1) / kSplitKeys;
-    const size_t base = (size_t)u * P.max_splits * P.rows + row;
+    const int nslots = (U.n + kSplitKeys - 1) / kSplitKeys * ws.parts;
+    const size_t base = (size_t)u * P.max_splits * ws.parts * P.rows + row;
 
+    // partials with l = 0 saw no key of this row (or no tile at all): skipped
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ws.part_ml[base + (size_t)s * P.rows].x);
+    for (int s = 0; s < nslots; ++s) {
+        const float2 ml = ws.part_ml[base + (size_t)s * P.rows];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
     constexpr int C = D / 32;
     float a[C];
 #pragma unroll
     for (int i = 0; i < C; ++i) a[i] = 0.f;
     float Lsum = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
+    for (int s = 0; s < nslots; ++s) {
         const size_t pr = base + (size_t)s * P.rows;
         const float2 ml = ws.part_ml[pr];
+        if (!(ml.y > 0.f)) continue;
         const float f = exp2f(ml.x - M);
         Lsum += ml.y * f;
         const float *po = ws.part_o + pr * D;
