@@ -187,6 +187,20 @@ kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status)
 kv_status kv_score_noalloc(const kv_problem *p, const void *q_win, const void *k,
                            const void *v, float *scores, void *stream);
 
+/*
+ * Watchdog of the device waits.  Every wait inside the tensor-core kernels (a
+ * pipeline stage, a tensor-core result) gives up after `ns` nanoseconds,
+ * posts KV_ERR_TIMEOUT to the workspace status word (read it with
+ * kv_check_status) and lets the kernel return with the context usable; the
+ * kernel's waits for its own copies and MMAs still in flight always allow
+ * 2 s.  Process-wide; applies to launches made after the call.  The default
+ * is 2e9 (2 s); 0 makes every wait that is not already satisfied give up at
+ * once, which exercises the failure path.  No page has a counterpart: this
+ * is the library's own failure detection.
+ */
+void kv_set_wait_limit_ns(uint64_t ns);
+uint64_t kv_get_wait_limit_ns(void);
+
 /* Static, human-readable name of a status code. */
 const char *kv_status_string(kv_status s);
 

@@ -25,7 +25,7 @@ from . import _build
 __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attention",
            "kv_score_rescore", "kv_make_offsets", "kv_select_topk", "kv_compact",
            "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
-           "EXPORTED_SYMBOLS", "evict"]
+           "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "EXPORTED_SYMBOLS", "evict"]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
     KV_ERR_UNSUPPORTED = range(7)
@@ -33,7 +33,8 @@ KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_
 EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_score_rescore", "kv_make_offsets", "kv_select_workspace_size",
                     "kv_select_topk", "kv_compact", "kv_check_status", "kv_status_string",
-                    "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc")
+                    "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc",
+                    "kv_set_wait_limit_ns", "kv_get_wait_limit_ns")
 
 
 class KvError(RuntimeError):
@@ -92,6 +93,10 @@ def load(path: Optional[str] = None):
         fn.restype = ctypes.c_int
     lib.kv_status_string.argtypes = [ctypes.c_int]
     lib.kv_status_string.restype = ctypes.c_char_p
+    lib.kv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.kv_set_wait_limit_ns.restype = None
+    lib.kv_get_wait_limit_ns.argtypes = []
+    lib.kv_get_wait_limit_ns.restype = ctypes.c_uint64
     _lib = lib
     return lib
 
@@ -231,6 +236,15 @@ def kv_check_status(workspace, stream=None) -> int:
     _check(load().kv_check_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
            "kv_check_status")
     return st.value
+
+
+def kv_set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' device waits for launches after this call (default 2 s)."""
+    load().kv_set_wait_limit_ns(int(ns))
+
+
+def kv_get_wait_limit_ns() -> int:
+    return int(load().kv_get_wait_limit_ns())
 
 
 def kv_budgets_uniform(num_layers: int, mean_budget: int) -> np.ndarray:

@@ -1,6 +1,7 @@
 // kv_api.cu -- the extern "C" entry points: argument checks, workspace carve-up,
 // launches, the offsets scan and the per-layer budget policies (host code).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <numeric>
@@ -11,6 +12,9 @@
 using namespace kvevict;
 
 namespace {
+
+// Pipeline wait limit of the kernels (kv_set_wait_limit_ns).
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -39,6 +43,7 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
     P->cu = reinterpret_cast<const long long *>(p->seq_offsets_dev);
     P->host_cu = reinterpret_cast<const long long *>(p->seq_offsets_host);
     P->scale_log2 = p->softmax_scale * 1.4426950408889634f;
+    P->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     P->units = (long long)P->R * P->L * P->H;
     P->max_n = 0;
     P->N_tot = 0;
@@ -217,6 +222,10 @@ kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const in
                                    offsets_dev, total_rows, (__nv_bfloat16 *)k_out,
                                    (__nv_bfloat16 *)v_out, (cudaStream_t)stream));
 }
+
+void kv_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
+
+uint64_t kv_get_wait_limit_ns(void) { return g_wait_ns.load(std::memory_order_relaxed); }
 
 kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status) {
     if (!workspace || !device_status) return KV_ERR_INVALID_ARG;

@@ -51,7 +51,6 @@ constexpr int kSoftWarps = 8;       // 4 per lane
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;     // O of lane L at column kOCol + 128 L
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kBlockBytes = 128 * 128;   // [128 rows][64 bf16], 128 B swizzle
 constexpr float kRescaleLog2 = 8.f;
 
@@ -62,7 +61,7 @@ struct Layout {
     static constexpr int kK = kQ + 2 * kOp;
     static constexpr int kV = kK + kKStages * kOp;
     static constexpr int kBars = kV + kVStages * kOp;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 4 * 2;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 4 * 2 + 1;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -193,6 +192,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *p_full = s_full + 2;         // [lane]: P written (4 softmax warps)
     uint64_t *o_final = p_full + 2;        // [lane]: the lane's last P V of the item is done
     uint64_t *o_empty = o_final + 2;       // [lane]: O read out (4 softmax warps)
+    uint64_t *mma_done = o_empty + 2;      // the MMA thread's last MMAs are done (exit)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
@@ -215,6 +215,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&o_final[L], 1);
             mbar_init(&o_empty[L], kSoftWarps / 2);
         }
+        mbar_init(mma_done, 1);
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -236,6 +237,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             long long tcount = 0, icount = 0;   // tiles loaded (both rings), items
+            long long qcount = 0, kiss = 0, viss = 0;   // Q, K and V loads issued
             bool ok = true;
             // L2 prefetch cursor: walks the same (item, tile) sequence as the loads,
             // kPrefetchTiles tiles ahead of them, so the smem rings' loads hit L2.
@@ -269,7 +271,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const UnitInfo U = unit_info(P, it.u, P.cu);
                 const LaneWork w0 = lane_work(A, it, 0), w1 = lane_work(A, it, 1);
                 const bool two_q = A.parts == 1 && w1.steps > 0;
-                ok = mbar_wait(q_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
+                ok = mbar_wait(q_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, P.wait_ns);
                 if (!ok) break;
                 mbar_arrive_expect_tx(q_full, (two_q ? 2 : 1) * Ly::kOp);
                 for (int L = 0; L < (two_q ? 2 : 1); ++L) {
@@ -279,6 +281,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         tma_load_2d(smem + Ly::kQ + L * Ly::kOp + kb * kBlockBytes, &tm_q,
                                     q_full, kb * 64, qy);
                 }
+                ++qcount;
                 // K tiles run `lead` tiles ahead of V tiles: the MMA thread needs
                 // K of the next tile of each lane before V of the current one
                 const int ntiles = it.t1 - it.t0;
@@ -290,13 +293,14 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
                         pf_step();
                         ok = mbar_wait(&k_empty[s], (uint32_t)((kc / kKStages) & 1) ^ 1u,
-                                       abort_flag, kWaitNs);
+                                       abort_flag, P.wait_ns);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
 #pragma unroll
                         for (int kb = 0; kb < D / 64; ++kb)
                             tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, &tm_k,
                                         &k_full[s], kb * 64, ky);
+                        ++kiss;
                     }
                     const int iv = i - lead;
                     if (iv >= 0 && iv < ntiles) {
@@ -304,13 +308,14 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         const int s = (int)(vc % kVStages);
                         const int vy = (int)(U.kv_row0 + (long long)(it.t0 + iv) * kTileKeys);
                         ok = mbar_wait(&v_empty[s], (uint32_t)((vc / kVStages) & 1) ^ 1u,
-                                       abort_flag, kWaitNs);
+                                       abort_flag, P.wait_ns);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
 #pragma unroll
                         for (int kb = 0; kb < D / 64; ++kb)
                             tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, &tm_v,
                                         &v_full[s], kb * 64, vy);
+                        ++viss;
                     }
                 }
                 tcount += ntiles;
@@ -320,17 +325,16 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 *abort_flag = 1;
                 post_status(A.status, KV_ERR_TIMEOUT);
             }
-            // drain: every load this thread issued lands before the CTA exits (after an
-            // abort some may not have been issued; those waits then run out)
+            // drain: the last load issued into each buffer lands before the CTA exits
+            // (the earlier ones were consumed before their buffer was refilled)
+            if (qcount > 0) mbar_drain(q_full, (uint32_t)((qcount - 1) & 1), kDrainNs);
             for (int s = 0; s < kKStages; ++s) {
-                const long long uses = tcount / kKStages + ((tcount % kKStages) > s ? 1 : 0);
-                if (uses > 0)
-                    mbar_wait(&k_full[s], (uint32_t)((uses - 1) & 1), abort_flag, kWaitNs);
+                const long long uses = kiss / kKStages + ((kiss % kKStages) > s ? 1 : 0);
+                if (uses > 0) mbar_drain(&k_full[s], (uint32_t)((uses - 1) & 1), kDrainNs);
             }
             for (int s = 0; s < kVStages; ++s) {
-                const long long uses = tcount / kVStages + ((tcount % kVStages) > s ? 1 : 0);
-                if (uses > 0)
-                    mbar_wait(&v_full[s], (uint32_t)((uses - 1) & 1), abort_flag, kWaitNs);
+                const long long uses = viss / kVStages + ((viss % kVStages) > s ? 1 : 0);
+                if (uses > 0) mbar_drain(&v_full[s], (uint32_t)((uses - 1) & 1), kDrainNs);
             }
         }
     } else if (run && warp == 1) {
@@ -347,7 +351,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const LaneWork w[2] = {lane_work(A, it, 0), lane_work(A, it, 1)};
                 // the lane whose MMAs are the last to read a tile frees its K/V stage
                 const int releaser = (A.parts == 1 && w[1].steps > 0) ? 1 : -1;
-                ok = mbar_wait(q_full, (uint32_t)(icount & 1), abort_flag, kWaitNs);
+                ok = mbar_wait(q_full, (uint32_t)(icount & 1), abort_flag, P.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 auto frees = [&](int L) { return releaser < 0 || releaser == L; };
@@ -356,7 +360,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const long long kc = tcount + w[L].first + (long long)j * w[L].stride;
                     const int s = (int)(kc % kKStages);
                     ok = ok && mbar_wait(&k_full[s], (uint32_t)((kc / kKStages) & 1), abort_flag,
-                                         kWaitNs);
+                                         P.wait_ns);
                     if (!ok) return;
                     tc_fence_after();
                     const uint64_t qa = sdesc_k_sw128(
@@ -382,11 +386,11 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const int s = (int)(vc % kVStages);
                     if (j == 0)
                         ok = ok && mbar_wait(&o_empty[L], (uint32_t)(oc[L] & 1) ^ 1u, abort_flag,
-                                             kWaitNs);
+                                             P.wait_ns);
                     ok = ok && mbar_wait(&p_full[L], (uint32_t)((sc[L] + j) & 1), abort_flag,
-                                         kWaitNs);
+                                         P.wait_ns);
                     ok = ok && mbar_wait(&v_full[s], (uint32_t)((vc / kVStages) & 1), abort_flag,
-                                         kWaitNs);
+                                         P.wait_ns);
                     if (!ok) return;
                     tc_fence_after();
                     const uint64_t vb =
@@ -429,6 +433,9 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 *abort_flag = 1;
                 post_status(A.status, KV_ERR_TIMEOUT);
             }
+            // every MMA issued completes before TMEM is freed
+            mma_commit(mma_done);
+            mbar_drain(mma_done, 0, kDrainNs);
         }
     } else if (run) {
         // ------------------------------------------------------------ softmax
@@ -461,7 +468,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             for (int j = 0; ok && j < w.steps; ++j) {
                 const int kt = (it.t0 + w.first + j * w.stride) * kTileKeys;
                 ok = __all_sync(0xffffffffu, mbar_wait(&s_full[L], (uint32_t)((sc + j) & 1),
-                                                       abort_flag, kWaitNs));
+                                                       abort_flag, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 // only tiles that reach into the window need the causal mask
@@ -557,7 +564,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             if (!ok) break;
             // item end: read O_L once the lane's last P V is done, write the partial
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&o_final[L], (uint32_t)(oc & 1), abort_flag, kWaitNs));
+                            mbar_wait(&o_final[L], (uint32_t)(oc & 1), abort_flag, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float *po = A.part_o + prow_idx * D;

@@ -30,7 +30,11 @@ struct DevProblem {
     const long long *cu;      // device cu_seqlens [R + 1]
     const long long *host_cu; // host copy (host code only; never read on the device)
     float scale_log2;         // softmax_scale * log2(e)
+    unsigned long long wait_ns;   // limit of the pipeline waits (kv_set_wait_limit_ns)
 };
+
+// Limit of the waits for a kernel's own copies and MMAs in flight before it exits.
+constexpr unsigned long long kDrainNs = 2000000000ull;
 
 struct UnitInfo {
     int r, l, h;

@@ -51,7 +51,6 @@ constexpr int kPrefetchTiles = 4;   // K/V tiles requested into L2 ahead of the 
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kBlockBytes = kChunkRows * 128;   // one [128 rows][64 bf16] swizzled box
 
 template <int D>
@@ -63,7 +62,7 @@ struct Layout {
     static constexpr int kK = kAlo + kOp;
     static constexpr int kV = kK + kStages * kOp;
     static constexpr int kBars = kV + kStages * kOp;
-    static constexpr int kNumBars = 4 * kStages + 2 + 4;
+    static constexpr int kNumBars = 4 * kStages + 2 + 4 + 1;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -233,6 +232,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
     uint64_t *qa_full = bars + 4 * kStages, *qa_empty = qa_full + 1;
     uint64_t *tm_full = qa_empty + 1, *tm_empty = tm_full + 2;
+    uint64_t *mma_done = tm_empty + 2;     // the MMA thread's last MMAs are done (exit)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
@@ -251,6 +251,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&tm_full[h], 1);
             mbar_init(&tm_empty[h], kEpiWarps);
         }
+        mbar_init(mma_done, 1);
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -274,6 +275,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             long long tcount = 0, icount = 0;
+            long long qcount = 0, kiss = 0, viss = 0;   // Q/a, K and V loads issued
             bool ok = true;
             // L2 prefetch cursor: walks the same (item, tile) sequence as the loads,
             // kPrefetchTiles tiles ahead of them, so the smem ring's loads hit L2.
@@ -305,7 +307,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
-                ok = mbar_wait(qa_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, kWaitNs);
+                ok = mbar_wait(qa_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, P.wait_ns);
                 if (!ok) break;
                 mbar_arrive_expect_tx(qa_full, 3 * Ly::kOp);
                 const int qy = (int)(U.q_row0 + it.c * kChunkRows);
@@ -316,25 +318,28 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     tma_load_2d(smem + Ly::kAhi + kb * kBlockBytes, &tm_ahi, qa_full, kb * 64, ay);
                     tma_load_2d(smem + Ly::kAlo + kb * kBlockBytes, &tm_alo, qa_full, kb * 64, ay);
                 }
+                ++qcount;
                 for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
                     const int s = (int)(tcount % kStages);
                     const uint32_t par = (uint32_t)((tcount / kStages) & 1) ^ 1u;
                     const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
                     pf_step();
-                    ok = mbar_wait(&k_empty[s], par, abort_flag, kWaitNs);
+                    ok = mbar_wait(&k_empty[s], par, abort_flag, P.wait_ns);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
                         tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, &tm_k,
                                     &k_full[s], kb * 64, ky);
-                    ok = mbar_wait(&v_empty[s], par, abort_flag, kWaitNs);
+                    ++kiss;
+                    ok = mbar_wait(&v_empty[s], par, abort_flag, P.wait_ns);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
                         tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, &tm_v,
                                     &v_full[s], kb * 64, ky);
+                    ++viss;
                 }
                 ++icount;
             }
@@ -342,14 +347,14 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 *abort_flag = 1;
                 post_status(A.status, KV_ERR_TIMEOUT);
             }
-            // drain: every load this thread issued lands before the CTA exits
+            // drain: the last load issued into each buffer lands before the CTA exits
+            // (the earlier ones were consumed before their buffer was refilled)
+            if (qcount > 0) mbar_drain(qa_full, (uint32_t)((qcount - 1) & 1), kDrainNs);
             for (int s = 0; s < kStages; ++s) {
-                const long long uses = tcount / kStages + ((tcount % kStages) > s ? 1 : 0);
-                if (uses > 0) {
-                    const uint32_t par = (uint32_t)((uses - 1) & 1);
-                    mbar_wait(&k_full[s], par, abort_flag, kWaitNs);
-                    mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
-                }
+                const long long ku = kiss / kStages + ((kiss % kStages) > s ? 1 : 0);
+                const long long vu = viss / kStages + ((viss % kStages) > s ? 1 : 0);
+                if (ku > 0) mbar_drain(&k_full[s], (uint32_t)((ku - 1) & 1), kDrainNs);
+                if (vu > 0) mbar_drain(&v_full[s], (uint32_t)((vu - 1) & 1), kDrainNs);
             }
         }
     } else if (run && warp == 1) {
@@ -360,7 +365,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
                 const uint32_t idesc = idesc_bf16_f32(128, chunk_rows_n(P, it.c));
-                ok = mbar_wait(qa_full, (uint32_t)(icount & 1), abort_flag, kWaitNs);
+                ok = mbar_wait(qa_full, (uint32_t)(icount & 1), abort_flag, P.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t qb = sdesc_k_sw128(smem_u32(smem + Ly::kQ));
@@ -371,8 +376,8 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const uint32_t par = (uint32_t)((tcount / kStages) & 1);
                     const int b = (int)(tcount & 1);          // TMEM buffer of this tile
                     ok = mbar_wait(&tm_empty[b], (uint32_t)((tcount >> 1) & 1) ^ 1u, abort_flag,
-                                   kWaitNs) &&
-                         mbar_wait(&k_full[s], par, abort_flag, kWaitNs);
+                                   P.wait_ns) &&
+                         mbar_wait(&k_full[s], par, abort_flag, P.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t d_s = tmem + b * 256;
@@ -389,7 +394,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                 mma_ss_c<true>(d_s, sdesc_add(ka, ko), sdesc_add(qb, ko), idesc);
                         }
                     mma_commit(&k_empty[s]);
-                    ok = mbar_wait(&v_full[s], par, abort_flag, kWaitNs);
+                    ok = mbar_wait(&v_full[s], par, abort_flag, P.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     mma_ss_c<false>(d_x, va, hb, idesc);
@@ -418,6 +423,9 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 *abort_flag = 1;
                 post_status(A.status, KV_ERR_TIMEOUT);
             }
+            // every MMA issued completes before TMEM is freed
+            mma_commit(mma_done);
+            mbar_drain(mma_done, 0, kDrainNs);
         }
     } else if (run) {
         // ------------------------------------------------------------ epilogue
@@ -451,8 +459,8 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const int b = (int)(tcount & 1);              // TMEM buffer of this tile
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&tm_full[b], (uint32_t)((tcount >> 1) & 1), abort_flag,
-                                          kWaitNs) &&
-                                    mbar_wait(&v_full[s], spar, abort_flag, kWaitNs));
+                                          P.wait_ns) &&
+                                    mbar_wait(&v_full[s], spar, abort_flag, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t s_col = tmem + lane_addr + b * 256;

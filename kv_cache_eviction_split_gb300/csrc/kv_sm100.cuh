@@ -74,17 +74,24 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Waits until the phase with the given parity completes, sleeping in between.
-// Gives up after `limit_ns` or as soon as *abort becomes non-zero; returns
-// false then.
+// Gives up after `limit_ns` or, when `abort` is given, as soon as *abort
+// becomes non-zero; returns false then.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = limit_ns < 20000u ? (uint32_t)limit_ns : 20000u;   // sleep <= limit
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (*abort) return false;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+        if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Waits (up to `limit_ns`, ignoring any abort) for this thread's own copies or
+// MMAs tracked by `bar` to land before the CTA exits or frees what they use.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    mbar_wait(bar, parity, nullptr, limit_ns);
 }
 
 // ---------------------------------------------------------------------------

@@ -36,6 +36,19 @@ def test_exports_every_declared_symbol(kv):
     assert sorted(kv.EXPORTED_SYMBOLS) == declared
 
 
+def test_wait_limit_knob_round_trip(kv):
+    default = kv.kv_get_wait_limit_ns()
+    assert default == 2_000_000_000
+    try:
+        kv.kv_set_wait_limit_ns(12345)
+        assert kv.kv_get_wait_limit_ns() == 12345
+        kv.kv_set_wait_limit_ns(0)
+        assert kv.kv_get_wait_limit_ns() == 0
+    finally:
+        kv.kv_set_wait_limit_ns(default)
+    assert kv.kv_get_wait_limit_ns() == default
+
+
 def _prob(kv, **kw):
     args = dict(lengths=[1000, 2000], num_layers=2, num_kv_heads=2, num_q_heads=8, head_dim=128,
                 window=32, num_sinks=4, device="cpu")
