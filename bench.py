@@ -233,7 +233,7 @@ def run_reference(args, wl, budgets):
 # our arm
 # ---------------------------------------------------------------------------
 # Kernels of one step and how many launches each makes (the timed region
-# launches only these).  The score passes run on the CUDA cores in fp32.
+# launches only these).
 STAGES = ["attention", "rescore", "select", "compact"]
 # attention: plan_kernel, attn_tc_kernel, attn_merge_kernel; rescore: plan_kernel,
 # rescore_tc_kernel and, when the window rows span more than one 128-row chunk,
@@ -296,6 +296,23 @@ def stage_roofline(stage, ms, wl, budgets, peaks):
         out["tensor"] = {"algorithmic_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
                          "peak_tflops": tpeak, "frac": flops / (ms * 1e-3) / 1e12 / tpeak}
     return out
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest `value` over all ranks (the timed region of the slowest rank);
+    `value` itself when there is no process group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second: every rank scores its own copy of the
+    workload (weak scaling), timed by the slowest rank."""
+    return units_per_rank * world / (ms_per_step * 1e-3)
 
 
 def gpu_uuid(torch, dev):
@@ -382,10 +399,7 @@ def main(argv=None):
     barrier()
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     st = (kv.kv_check_status(bufs.score_ws, stream), kv.kv_check_status(bufs.select_ws, stream))
     if st != (0, 0):
         raise SystemExit("device status after the timed region: %s" % (st,))
@@ -394,7 +408,7 @@ def main(argv=None):
     ms_per_step = total_ms / args.steps
     n_tot = sum(wl.seq_lengths())
     unit_tokens = n_tot * wl.num_layers * wl.num_kv_heads
-    value = unit_tokens * world / (ms_per_step * 1e-3)
+    value = whole_job_rate(unit_tokens, world, ms_per_step)
     alg_bytes = algorithmic_bytes(wl, budgets)
     hbm_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
 
