@@ -46,7 +46,6 @@ constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kPrefetchTiles = 4;   // K/V tiles requested into L2 ahead of the smem loads
 constexpr int kSoftWarps = 8;       // 4 per lane
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -239,33 +238,6 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             long long tcount = 0, icount = 0;   // tiles loaded (both rings), items
             long long qcount = 0, kiss = 0, viss = 0;   // Q, K and V loads issued
             bool ok = true;
-            // L2 prefetch cursor: walks the same (item, tile) sequence as the loads,
-            // kPrefetchTiles tiles ahead of them, so the smem rings' loads hit L2.
-            long long pf_item = blockIdx.x, pf_row0 = 0;
-            int pf_t = 0, pf_end = 0;
-            auto pf_open = [&]() {
-                if (pf_item < A.total_items) {
-                    const Item pi = decode_item(pf_item, A, P);
-                    pf_row0 = unit_info(P, pi.u, P.cu).kv_row0;
-                    pf_t = pi.t0;
-                    pf_end = pi.t1;
-                }
-            };
-            auto pf_step = [&]() {
-                if (pf_item >= A.total_items) return;
-                const int ky = (int)(pf_row0 + (long long)pf_t * kTileKeys);
-#pragma unroll
-                for (int kb = 0; kb < D / 64; ++kb) {
-                    tma_prefetch_2d(&tm_k, kb * 64, ky);
-                    tma_prefetch_2d(&tm_v, kb * 64, ky);
-                }
-                if (++pf_t >= pf_end) {
-                    pf_item += gridDim.x;
-                    pf_open();
-                }
-            };
-            pf_open();
-            for (int i = 0; i < kPrefetchTiles; ++i) pf_step();
             for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
                 const Item it = decode_item(item, A, P);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
@@ -291,7 +263,6 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         const long long kc = tcount + i;
                         const int s = (int)(kc % kKStages);
                         const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
-                        pf_step();
                         ok = mbar_wait(&k_empty[s], (uint32_t)((kc / kKStages) & 1) ^ 1u,
                                        abort_flag, P.wait_ns);
                         if (!ok) break;
