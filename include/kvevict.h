@@ -106,7 +106,10 @@ kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const 
 /*
  * Pass 1: causal window attention of every unit with split-K over the keys and
  * a merge of the splits (row max, row sum and a = sum p v); leaves them in the
- * workspace for pass 2.
+ * workspace for pass 2.  The product p v runs with p and v in fp16: V values
+ * must be finite and below 65504 in magnitude (bf16 values in that range
+ * convert exactly down to 6.1e-5; smaller magnitudes keep an absolute error
+ * below 3e-8).  A larger value posts KV_ERR_UNSUPPORTED to the status word.
  */
 kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void *k,
                              const void *v, void *workspace, size_t workspace_bytes,

@@ -19,14 +19,17 @@
 // same TMEM columns (the tensor pipe runs one thread's MMAs in order), so the
 // softmax of one lane overlaps the MMAs of the other.  A softmax thread owns one
 // row of its lane over all 128 keys of a tile: no exchange between threads.  It
-// turns S into P = 2^(s c - m) and stores P back over the S columns as two bf16
-// halves, P_hi = p truncated to bf16 and P_lo = bf16(p - P_hi) (each 16-key
-// chunk's 16 columns hold its 8 P_hi then 8 P_lo columns); O accumulates
-// P_hi V + P_lo V.  (A single bf16 P leaves a with ~2^-9 relative error, which
-// the rescoring expansion amplifies where a is close to a value row; the split
-// keeps ~16 bits of p.)  The running max is lazy: O and l are rescaled only
-// when the tile max exceeds it by more than 2^8.  When S of tile j+1 is
-// complete, P V of tile j is too, so the rescale needs no extra wait.
+// turns S into P' = 2^(s c - m + 13) and stores P' back over the S columns in
+// fp16 (two keys per column).  P V runs in fp16: the softmax warps convert each
+// V tile in shared memory from bf16 to fp16 in place first, which is exact for
+// normal values below 65504 (larger ones post KV_ERR_UNSUPPORTED).  fp16 keeps
+// 11 bits of p where bf16 keeps 8; a single bf16 P would leave a with ~2^-9
+// relative error, which the rescoring expansion amplifies where a is close to
+// a value row.  The running max is lazy: O and l are rescaled only when the
+// tile max exceeds it by more than 2^2, so P' <= 2^15 stays in fp16 range and
+// values down to 2^-37 p_max keep their mass.  l and O carry the factor 2^13,
+// removed when the partial is written.  When S of tile j+1 is complete, P V of
+// tile j is too, so the rescale needs no extra wait.
 //
 // Warp roles (320 threads): warp 0 TMA producer (the lanes' Q chunks per item;
 // K tiles through a 3-stage ring running ahead of V tiles in a 2-stage ring);
@@ -34,6 +37,8 @@
 // Work items are (unit, 16384-key split, chunk pair), walked round-robin by a
 // persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
 #include <cfloat>
+
+#include <cuda_fp16.h>
 
 #include "kv_internal.cuh"
 #include "kv_sm100.cuh"
@@ -51,7 +56,8 @@ constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;     // O of lane L at column kOCol + 128 L
 constexpr int kBlockBytes = 128 * 128;   // [128 rows][64 bf16], 128 B swizzle
-constexpr float kRescaleLog2 = 8.f;
+constexpr float kRescaleLog2 = 2.f;
+constexpr float kPScaleLog2 = 13.f;    // P' = p 2^13 in fp16
 
 template <int D>
 struct Layout {
@@ -60,7 +66,7 @@ struct Layout {
     static constexpr int kK = kQ + 2 * kOp;
     static constexpr int kV = kK + kKStages * kOp;
     static constexpr int kBars = kV + kVStages * kOp;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 4 * 2 + 1;
+    static constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 2 + 4 * 2 + 1;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -124,36 +130,20 @@ __device__ __forceinline__ LaneWork lane_work(const AttnArgs &A, const Item &it,
     return w;
 }
 
-// Packs P for 32 keys (two 16-key chunks) given as fp32 p: per chunk, 8 words of
-// P_hi (p truncated to bf16, two keys per word, the lower key in the low half)
-// then 8 words of P_lo = bf16(p - P_hi).
-__device__ __forceinline__ void pack_p32(const float (&p)[32], uint32_t (&w)[32]) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            const uint32_t b0 = __float_as_uint(p[16 * q + 2 * h]);
-            const uint32_t b1 = __float_as_uint(p[16 * q + 2 * h + 1]);
-            w[16 * q + h] = __byte_perm(b0, b1, 0x7632);
-            const float2 hi = make_float2(__uint_as_float(b0 & 0xFFFF0000u),
-                                          __uint_as_float(b1 & 0xFFFF0000u));
-            // exact: p - P_hi clears only the leading bits of p
-            const float2 lo = __ffma2_rn(hi, make_float2(-1.f, -1.f),
-                                         make_float2(p[16 * q + 2 * h], p[16 * q + 2 * h + 1]));
-            const __nv_bfloat162 lo2 = __floats2bfloat162_rn(lo.x, lo.y);
-            w[16 * q + 8 + h] = *reinterpret_cast<const uint32_t *>(&lo2);
-        }
+// Two fp32 values as fp16x2 (round to nearest), the first in the low half.
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Masked form for tiles that reach the observation window: p = 2^(s c - m) for
-// 16 keys, zero for keys after `lim` (tile-local); adds p to the row sum and
-// stores the chunk's P_hi / P_lo columns at hi_col / lo_col.
+// Masked form for tiles that reach the observation window: P' for 16 keys, zero
+// for keys after `lim` (tile-local); adds P' to the row sum and stores the 8
+// fp16x2 columns at `col`.
 __device__ __forceinline__ void soft16_masked(const float *v, int j0, int lim, float cs,
-                                              float negm, float2 &lsum, uint32_t hi_col,
-                                              uint32_t lo_col) {
+                                              float negm, float2 &lsum, uint32_t col) {
     const float2 cs2 = make_float2(cs, cs);
     const float2 nm2 = make_float2(negm, negm);
-    uint32_t whi[8], wlo[8];
+    uint32_t w[8];
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
         const int j = 2 * h;
@@ -162,16 +152,28 @@ __device__ __forceinline__ void soft16_masked(const float *v, int j0, int lim, f
         if (j0 + j > lim) p.x = 0.f;
         if (j0 + j + 1 > lim) p.y = 0.f;
         lsum = __fadd2_rn(lsum, p);
-        const uint32_t b0 = __float_as_uint(p.x), b1 = __float_as_uint(p.y);
-        whi[h] = __byte_perm(b0, b1, 0x7632);
-        const float2 lo = __ffma2_rn(make_float2(__uint_as_float(b0 & 0xFFFF0000u),
-                                                 __uint_as_float(b1 & 0xFFFF0000u)),
-                                     make_float2(-1.f, -1.f), p);
-        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(lo.x, lo.y);
-        wlo[h] = *reinterpret_cast<const uint32_t *>(&lo2);
+        w[h] = pack_half2(p.x, p.y);
     }
-    tmem_st8u(hi_col, whi);
-    tmem_st8u(lo_col, wlo);
+    tmem_st8u(col, w);
+}
+
+// Converts 16-byte groups first, first + 32, ... (count of them) of a bf16 tile in
+// shared memory to fp16 in place (same positions); true if a value overflowed.
+__device__ __forceinline__ bool tile_to_f16(uint8_t *tile, int first, int count) {
+    uint32_t bad = 0;
+    uint4 *g = reinterpret_cast<uint4 *>(tile) + first;
+    for (int i = 0; i < count; ++i) {
+        const uint4 w = g[32 * i];
+        uint32_t o[4];
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xFFFF0000u));
+            bad |= ((o[k] & 0x7C00u) == 0x7C00u) | ((o[k] & 0x7C000000u) == 0x7C000000u);
+        }
+        g[32 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    return bad != 0;
 }
 
 template <int D>
@@ -186,7 +188,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
     uint64_t *k_full = bars, *k_empty = bars + kKStages;
     uint64_t *v_full = bars + 2 * kKStages, *v_empty = v_full + kVStages;
-    uint64_t *q_full = v_empty + kVStages, *q_empty = q_full + 1;
+    uint64_t *v_conv = v_empty + kVStages;  // [stage]: V tile converted to fp16 (8 warp shares)
+    uint64_t *q_full = v_conv + kVStages, *q_empty = q_full + 1;
     uint64_t *s_full = q_empty + 1;        // [lane]: S of the lane's next tile is in TMEM
     uint64_t *p_full = s_full + 2;         // [lane]: P written (4 softmax warps)
     uint64_t *o_final = p_full + 2;        // [lane]: the lane's last P V of the item is done
@@ -205,6 +208,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
+            mbar_init(&v_conv[s], kSoftWarps);
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -312,7 +316,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(128, kTileKeys);
-            const uint32_t idesc_pv = idesc_bf16_f32_bmn(128, D);
+            const uint32_t idesc_pv = idesc_f16_f32_bmn(128, D);
             long long tcount = 0, icount = 0;
             long long sc[2] = {0, 0};   // steps issued per lane
             long long oc[2] = {0, 0};   // items in which the lane took part
@@ -351,7 +355,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     mma_commit(&s_full[L]);
                     if (frees(L)) mma_commit(&k_empty[s]);
                 };
-                // O_L (+)= P_hi V + P_lo V for step j of lane L
+                // O_L (+)= P' V for step j of lane L (fp16 operands)
                 auto issue_pv = [&](int L, int j) {
                     const long long vc = tcount + w[L].first + (long long)j * w[L].stride;
                     const int s = (int)(vc % kVStages);
@@ -360,7 +364,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                              P.wait_ns);
                     ok = ok && mbar_wait(&p_full[L], (uint32_t)((sc[L] + j) & 1), abort_flag,
                                          P.wait_ns);
-                    ok = ok && mbar_wait(&v_full[s], (uint32_t)((vc / kVStages) & 1), abort_flag,
+                    ok = ok && mbar_wait(&v_conv[s], (uint32_t)((vc / kVStages) & 1), abort_flag,
                                          P.wait_ns);
                     if (!ok) return;
                     tc_fence_after();
@@ -369,17 +373,15 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const uint32_t pcol = tmem + 128 * L;
                     const uint32_t d_o = tmem + kOCol + 128 * L;
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int q = 0; q < kTileKeys / 16; ++q) {
-                            // keys 16q..16q+15: P_hi in columns 16q..16q+7, P_lo in 16q+8..+15
-                            const uint32_t a = pcol + q * 16 + part * 8;
-                            const uint64_t bd = sdesc_add(vb, q * 16 * 128);
-                            if (j == 0 && part == 0 && q == 0)
-                                mma_ts_c<false>(d_o, a, bd, idesc_pv);
-                            else
-                                mma_ts_c<true>(d_o, a, bd, idesc_pv);
-                        }
+                    for (int q = 0; q < kTileKeys / 16; ++q) {
+                        // keys 16q..16q+15: fp16x2 columns 8q..8q+7
+                        const uint32_t a = pcol + q * 8;
+                        const uint64_t bd = sdesc_add(vb, q * 16 * 128);
+                        if (j == 0 && q == 0)
+                            mma_ts_c<false>(d_o, a, bd, idesc_pv);
+                        else
+                            mma_ts_c<true>(d_o, a, bd, idesc_pv);
+                    }
                     if (frees(L)) mma_commit(&v_empty[s]);
                 };
                 const int nmax = max(w[0].steps, w[1].steps);
@@ -418,11 +420,37 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         const uint32_t o_base = tmem + lane_addr + kOCol + 128 * L;
         const float cs = P.scale_log2;
         long long sc = 0, oc = 0;
+        long long tbase = 0;   // tiles of this CTA's earlier items (V stage and parity)
         bool ok = true;
+        // This warp's share of converting the V tile of item tile ti to fp16: when
+        // both lanes use every tile all 8 softmax warps take an eighth of it;
+        // otherwise the 4 warps of the lane that uses the tile take a quarter each
+        // (and arrive twice each at the 8-count barrier).
+        bool both = false;
+        auto convert_v = [&](int ti) -> bool {
+            const long long vc = tbase + ti;
+            const int s = (int)(vc % kVStages);
+            const bool ok2 = __all_sync(0xffffffffu,
+                                        mbar_wait(&v_full[s], (uint32_t)((vc / kVStages) & 1),
+                                                  abort_flag, P.wait_ns));
+            if (!ok2) return false;
+            uint8_t *tile = smem + Ly::kV + s * Ly::kOp;
+            constexpr int kGroups = Ly::kOp / 16;
+            const int share = both ? kGroups / 8 : kGroups / 4;
+            const int cw = both ? warp - 2 : (warp - 2) & 3;
+            if (tile_to_f16(tile, cw * share + lane, share / 32))
+                post_status(A.status, KV_ERR_UNSUPPORTED);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cnt(&v_conv[s], both ? 1u : 2u);
+            return true;
+        };
         for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
             const Item it = decode_item(item, A, P);
             const LaneWork w = lane_work(A, it, L);
             const UnitInfo U = unit_info(P, it.u, P.cu);
+            const long long item_tiles = it.t1 - it.t0;
+            both = A.parts == 1 && lane_work(A, it, 1).steps > 0;
             const int row = w.chunk * kChunkRows + rr;
             const bool row_valid = row < P.rows;
             const int slot = A.parts == 1 ? it.split : 2 * it.split + L;
@@ -431,13 +459,17 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             if (w.steps == 0) {
                 // no tile for this lane: an empty partial (l = 0) for the merge to skip
                 if (A.parts == 2 && row_valid) A.part_ml[prow_idx] = make_float2(-INFINITY, 0.f);
+                tbase += item_tiles;
                 continue;
             }
+            ok = convert_v(w.first);
+            if (!ok) break;
             const int pos = U.n - P.w + (row % P.w);      // last key this row sees
             const int pos_min = U.n - P.w;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; ok && j < w.steps; ++j) {
-                const int kt = (it.t0 + w.first + j * w.stride) * kTileKeys;
+                const int ti = w.first + j * w.stride;
+                const int kt = (it.t0 + ti) * kTileKeys;
                 ok = __all_sync(0xffffffffu, mbar_wait(&s_full[L], (uint32_t)((sc + j) & 1),
                                                        abort_flag, P.wait_ns));
                 if (!ok) break;
@@ -490,7 +522,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     l *= factor;
                     m_used = m_tile;
                 }
-                const float negm = m_used == -INFINITY ? 0.f : -m_used;
+                // P' = 2^(s c - m + 13); with m = -inf (every key masked so far) p = 0
+                const float negm = m_used == -INFINITY ? 0.f : kPScaleLog2 - m_used;
                 float2 lsum = make_float2(0.f, 0.f);
                 if (!boundary) {
                     const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(negm, negm);
@@ -503,27 +536,26 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         tmem_ld_wait();
                         reg_fence(cur);
                         if (c < 3) tmem_ld32(s_base + 32 * (c + 1), nxt);
-                        float p[32];
+                        // keys 32c..32c+31 -> fp16x2 columns 16c..16c+15: only columns of
+                        // keys already read are overwritten
+                        uint32_t pw[16];
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
                             const float2 t = __ffma2_rn(make_float2(cur[i], cur[i + 1]), cs2, nm2);
-                            p[i] = ex2_approx(t.x);
-                            p[i + 1] = ex2_approx(t.y);
-                            lsum = __fadd2_rn(lsum, make_float2(p[i], p[i + 1]));
+                            const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+                            lsum = __fadd2_rn(lsum, make_float2(p0, p1));
+                            pw[i / 2] = pack_half2(p0, p1);
                         }
-                        uint32_t pw[32];
-                        pack_p32(p, pw);
-                        tmem_st32u(s_base + 32 * c, pw);
+                        tmem_st16u(s_base + 16 * c, pw);
                     }
                 } else {
 #pragma unroll 1
                     for (int c = 0; c < kTileKeys / 16; ++c) {
                         float sv[16];
-                        const uint32_t col = s_base + 16 * c;
-                        tmem_ld16(col, sv);
+                        tmem_ld16(s_base + 16 * c, sv);
                         tmem_ld_wait();
                         reg_fence(sv);
-                        soft16_masked(sv, 16 * c, lim, cs, negm, lsum, col, col + 8);
+                        soft16_masked(sv, 16 * c, lim, cs, negm, lsum, s_base + 8 * c);
                     }
                 }
                 l += lsum.x + lsum.y;
@@ -531,6 +563,11 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[L]);
+                // the lane's next tile: convert its V while S of that tile computes
+                if (j + 1 < w.steps) {
+                    ok = convert_v(ti + w.stride);
+                    if (!ok) break;
+                }
             }
             if (!ok) break;
             // item end: read O_L once the lane's last P V is done, write the partial
@@ -538,6 +575,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                             mbar_wait(&o_final[L], (uint32_t)(oc & 1), abort_flag, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
+            // O and l carry P's factor 2^13; the partial is written without it
+            constexpr float kUnscale = 1.f / 8192.f;
             float *po = A.part_o + prow_idx * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -549,15 +588,17 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
                         *reinterpret_cast<float4 *>(po + 32 * c + i) =
-                            make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                            make_float4(o[i] * kUnscale, o[i + 1] * kUnscale,
+                                        o[i + 2] * kUnscale, o[i + 3] * kUnscale);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_empty[L]);
-            if (row_valid) A.part_ml[prow_idx] = make_float2(m_used, l);
+            if (row_valid) A.part_ml[prow_idx] = make_float2(m_used, l * kUnscale);
             sc += w.steps;
             ++oc;
+            tbase += item_tiles;
         }
         if (!ok) {
             *abort_flag = 1;

@@ -39,6 +39,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Arrives `count` times at once.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(count)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -202,6 +209,17 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
         : "memory");
 }
 
+// Stores 16 consecutive 32-bit columns (raw bits) for the warp's 32 lanes.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+
 // 32 TMEM lanes x 32 consecutive 32-bit columns: thread i receives lane
 // (base lane + i), columns col .. col+31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -358,6 +376,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // Same with the B operand MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
     return idesc_bf16_f32(M, N) | (1u << 16);
+}
+
+// As idesc_bf16_f32_bmn with fp16 A and B (type field 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) {
+    return (1u << 4)                                    // D: f32
+           | (1u << 16)                                 // B: MN-major
+           | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -48,3 +48,22 @@ def test_expired_waits_report_timeout_and_context_recovers(cuda_lib, wl):
         big = S >= parity.SCORE_ATOL
         rel = np.abs(g[big] - S[big]) / S[big]
         assert rel.max() <= parity.SCORE_RTOL
+
+
+def test_value_outside_fp16_range_reports_unsupported(cuda_lib):
+    """The attention pass multiplies p by v in fp16; a V value of magnitude
+    65504 or more cannot be represented and is reported, not silently used."""
+    import torch
+    from synth.device import DeviceWorkload
+    kv = cuda_lib
+    wl = synth.small_variant(synth.LONG_128K, 5003)
+    dw = DeviceWorkload(wl)
+    prob = kv.Problem.for_workload(wl)
+    ws = torch.zeros(kv.kv_score_workspace_size(prob), dtype=torch.uint8, device="cuda")
+    scores = torch.zeros((wl.num_layers, wl.num_kv_heads, dw.N_tot), dtype=torch.float32,
+                         device="cuda")
+    kv.kv_score(prob, dw.q, dw.k, dw.v, scores, ws)
+    assert kv.kv_check_status(ws) == kv.KV_OK
+    dw.v[1, 0, 777, 5] = 1.0e5
+    kv.kv_score(prob, dw.q, dw.k, dw.v, scores, ws)
+    assert kv.kv_check_status(ws) == kv.KV_ERR_UNSUPPORTED
