@@ -93,6 +93,7 @@ ScoreWs score_ws_layout(const DevProblem &P, void *base) {
     const size_t keys = (size_t)P.L * P.H * (size_t)P.N_tot;
     ws.part_scores = reinterpret_cast<float *>(
         take(ws.chunks > 1 ? (size_t)ws.chunks * keys * sizeof(float) : 0));
+    ws.v2 = reinterpret_cast<float *>(take(keys * sizeof(float)));
     ws.total = off;
     return ws;
 }

@@ -75,6 +75,7 @@ struct AttnArgs {
     const int32_t *plan;       // [units + 1] prefix of key splits per unit
     float2 *part_ml;           // [units][max_splits * parts][rows]
     float *part_o;             // [units][max_splits * parts][rows][d]
+    float *v2;                 // [L*H*N_tot] ||v_j||^2, written while converting V
     long long total_items;
     int pairs;                 // items per split: chunk pairs, or 1 with a single chunk
     int parts;                 // partials per split: 1 (chunk pairs) or 2 (alternate tiles)
@@ -157,23 +158,42 @@ __device__ __forceinline__ void soft16_masked(const float *v, int j0, int lim, f
     tmem_st8u(col, w);
 }
 
-// Converts 16-byte groups first, first + 32, ... (count of them) of a bf16 tile in
-// shared memory to fp16 in place (same positions); true if a value overflowed.
-__device__ __forceinline__ bool tile_to_f16(uint8_t *tile, int first, int count) {
-    uint32_t bad = 0;
-    uint4 *g = reinterpret_cast<uint4 *>(tile) + first;
-    for (int i = 0; i < count; ++i) {
-        const uint4 w = g[32 * i];
-        uint32_t o[4];
+// Adds the squares of the two bf16 halves of `w` to `acc` (fp32 products of bf16
+// are exact; one rounding per addition).
+__device__ __forceinline__ void sq_acc_bf16x2(float &acc, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, lo, lo, %0;\n\tfma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+}
+
+// Converts half of one key row of a swizzled [128][D] bf16 tile (`row`, 16-byte
+// chunks [half * D/16, (half + 1) * D/16) across the 64-column blocks) to fp16 in
+// place, and returns the sum of the squares of its bf16 values; `bad` is set if
+// a value overflowed fp16.
+template <int D>
+__device__ __forceinline__ float row_half_to_f16(uint8_t *tile, int row, int half, bool &bad) {
+    constexpr int kChunks = D / 16;            // 16-byte chunks per half row
+    float acc[2] = {0.f, 0.f};
+    uint32_t over = 0;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        const int c = half * kChunks + i;      // logical chunk of the row
+        uint4 *g = reinterpret_cast<uint4 *>(tile + (c >> 3) * kBlockBytes + row * 128 +
+                                             (((c & 7) ^ (row & 7)) << 4));
+        const uint4 w = *g;
         const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
+            sq_acc_bf16x2(acc[k & 1], in[k]);
             o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xFFFF0000u));
-            bad |= ((o[k] & 0x7C00u) == 0x7C00u) | ((o[k] & 0x7C000000u) == 0x7C000000u);
+            over |= ((o[k] & 0x7C00u) == 0x7C00u) | ((o[k] & 0x7C000000u) == 0x7C000000u);
         }
-        g[32 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        *g = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    return bad != 0;
+    bad = bad || over != 0;
+    return acc[0] + acc[1];
 }
 
 template <int D>
@@ -422,11 +442,15 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         long long sc = 0, oc = 0;
         long long tbase = 0;   // tiles of this CTA's earlier items (V stage and parity)
         bool ok = true;
-        // This warp's share of converting the V tile of item tile ti to fp16: when
-        // both lanes use every tile all 8 softmax warps take an eighth of it;
-        // otherwise the 4 warps of the lane that uses the tile take a quarter each
-        // (and arrive twice each at the 8-count barrier).
+        // This warp's share of converting the V tile of item tile ti to fp16, which
+        // also yields ||v_j||^2 of its keys (written for the rescoring pass): when
+        // both lanes use every tile the 8 softmax warps take 16 keys each, otherwise
+        // the 4 warps of the lane that uses the tile take 32 each (and arrive twice
+        // each at the 8-count barrier).  Two threads share a key row (lane, lane^16).
         bool both = false;
+        int it_t0 = 0;
+        long long v2_row0 = 0;   // first key of the item's unit in ||v||^2
+        int unit_n = 0;
         auto convert_v = [&](int ti) -> bool {
             const long long vc = tbase + ti;
             const int s = (int)(vc % kVStages);
@@ -435,11 +459,17 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                                   abort_flag, P.wait_ns));
             if (!ok2) return false;
             uint8_t *tile = smem + Ly::kV + s * Ly::kOp;
-            constexpr int kGroups = Ly::kOp / 16;
-            const int share = both ? kGroups / 8 : kGroups / 4;
+            const int keys = both ? 16 : 32;
             const int cw = both ? warp - 2 : (warp - 2) & 3;
-            if (tile_to_f16(tile, cw * share + lane, share / 32))
-                post_status(A.status, KV_ERR_UNSUPPORTED);
+            bool bad = false;
+            for (int k0 = 0; k0 < keys; k0 += 16) {
+                const int row = cw * keys + k0 + (lane & 15);
+                float q = row_half_to_f16<D>(tile, row, lane >> 4, bad);
+                q += __shfl_xor_sync(0xffffffffu, q, 16);
+                const int j = (it_t0 + ti) * kTileKeys + row;   // key of the unit
+                if (lane < 16 && j < unit_n) A.v2[v2_row0 + j] = q;
+            }
+            if (bad) post_status(A.status, KV_ERR_UNSUPPORTED);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive_cnt(&v_conv[s], both ? 1u : 2u);
@@ -451,6 +481,9 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const long long item_tiles = it.t1 - it.t0;
             both = A.parts == 1 && lane_work(A, it, 1).steps > 0;
+            v2_row0 = U.kv_row0;
+            unit_n = U.n;
+            it_t0 = it.t0;
             const int row = w.chunk * kChunkRows + rr;
             const bool row_valid = row < P.rows;
             const int slot = A.parts == 1 ? it.split : 2 * it.split + L;
@@ -626,6 +659,7 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     A.plan = ws.plan;
     A.part_ml = ws.part_ml;
     A.part_o = ws.part_o;
+    A.v2 = ws.v2;
     A.chunks = ws.chunks;
     A.parts = ws.parts;
     A.pairs = ws.parts == 1 ? (ws.chunks + 1) / 2 : 1;

@@ -67,6 +67,7 @@ struct ScoreWs {
     __nv_bfloat16 *a_lo;      // [units][a_rows][d]  bf16(a - a_hi); rows >= rows are zero
     int32_t *plan;            // [units + 1] pass-2 work plan
     float *part_scores;       // [chunks][L*H*N_tot] when chunks > 1
+    float *v2;                // [L*H*N_tot] ||v_j||^2 of every key (written by pass 1)
     int a_rows;               // chunks * 128
     int chunks;               // ceil(rows / 128)
     int parts;                // pass-1 partials per split: 2 with one chunk, else 1

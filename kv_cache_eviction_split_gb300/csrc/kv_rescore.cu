@@ -27,7 +27,8 @@
 //   warp 1      TMEM owner and MMA issuer (one thread): per tile S = K Q^T and
 //               X = V a_hi^T + V a_lo^T over all rows of the chunk, into one of
 //               two TMEM buffers, so tile i+1 computes while tile i is scored
-//               and a K/V stage frees as soon as its MMAs complete
+//               and a K/V stage frees as soon as its MMAs complete (||v_j||^2
+//               comes from pass 1, which computes it while converting V)
 //   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) + 16 h .. +15
 //               (h = 0 for warps 2-5, 1 for 6-9) over all rows of the chunk;
 //               the four threads that share a key add their sums by shuffles
@@ -71,6 +72,7 @@ struct RescoreArgs {
     const int32_t *plan;       // [units + 1] prefix of key-tile blocks per unit
     const float2 *stat_ml;     // [units][rows] (m in log2 units, l)
     const float *stat_a2;      // [units][rows]
+    const float *v2;           // [L*H*N_tot] ||v_j||^2 (from pass 1)
     float *out;                // scores, or chunk partials [chunks][L*H*N_tot]
     long long out_stride;      // elements between chunk partials
     long long total_items;
@@ -106,39 +108,6 @@ __device__ __forceinline__ Item decode_item(long long item, const RescoreArgs &A
 __device__ __forceinline__ int chunk_rows_n(const DevProblem &P, int c) {
     const int rc = min(kChunkRows, P.rows - c * kChunkRows);
     return ((rc + 31) / 32) * 32;
-}
-
-// Adds the squares of the two bf16 halves of `w` to `acc` (fp32 products of bf16
-// are exact; one rounding per addition).
-__device__ __forceinline__ void sq_acc_bf16x2(float &acc, uint32_t w) {
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
-        "fma.rn.f32.bf16 %0, lo, lo, %0;\n\tfma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(w));
-}
-
-// Part of ||v||^2 of one row of a swizzled [128][D] bf16 tile: the 16-byte
-// chunks {part, part + 4} of each 64-column block.  The four threads that share
-// a row take part = 0..3; which of the two chunks comes first alternates with
-// the row's parity, so the 8 threads of a quarter-warp (two rows) read 8
-// different bank groups.
-template <int D>
-__device__ __forceinline__ float row_sqnorm_part(const uint8_t *tile, int row, int part) {
-    float acc[2] = {0.f, 0.f};
-#pragma unroll
-    for (int kb = 0; kb < D / 64; ++kb) {
-        const uint8_t *base = tile + kb * kBlockBytes + row * 128;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c16 = part + 4 * (h ^ (row & 1));
-            const uint4 w = *reinterpret_cast<const uint4 *>(base + ((c16 ^ (row & 7)) << 4));
-            sq_acc_bf16x2(acc[h], w.x);
-            sq_acc_bf16x2(acc[h], w.y);
-            sq_acc_bf16x2(acc[h], w.z);
-            sq_acc_bf16x2(acc[h], w.w);
-        }
-    }
-    return acc[0] + acc[1];
 }
 
 // One (row pair, key) term pair: p/(1 - p) * sqrt(x) with p = 2^(s c - m'),
@@ -243,7 +212,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1 + kEpiWarps);
+            mbar_init(&v_empty[s], 1);
         }
         mbar_init(qa_full, 1);
         mbar_init(qa_empty, 1);
@@ -453,29 +422,30 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             }
             float *out = A.out + (long long)it.c * A.out_stride + U.kv_row0;
             const int pos0 = U.n - P.w;
+            const float *u_v2 = A.v2 + U.kv_row0;
+            float vq[2];
+            {
+                const int jf = it.t_begin * kTileKeys + key0;
+                vq[0] = jf < U.n ? __ldg(u_v2 + jf) : 0.f;
+                vq[1] = jf + 8 < U.n ? __ldg(u_v2 + jf + 8) : 0.f;
+            }
             for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
-                const int s = (int)(tcount % kStages);
-                const uint32_t spar = (uint32_t)((tcount / kStages) & 1);
                 const int b = (int)(tcount & 1);              // TMEM buffer of this tile
+                // ||v||^2 of the two keys of this tile (loaded a tile ahead)
+                const float q0 = vq[0], q1 = vq[1];
+                if (t + 1 < it.t_end) {
+                    const int jn = (t + 1) * kTileKeys + key0;
+                    vq[0] = jn < U.n ? __ldg(u_v2 + jn) : 0.f;
+                    vq[1] = jn + 8 < U.n ? __ldg(u_v2 + jn + 8) : 0.f;
+                }
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&tm_full[b], (uint32_t)((tcount >> 1) & 1), abort_flag,
-                                          P.wait_ns) &&
-                                    mbar_wait(&v_full[s], spar, abort_flag, P.wait_ns));
+                                          P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t s_col = tmem + lane_addr + b * 256;
                 const uint32_t x_col = s_col + 128;
                 float sA[16], xA[16];
-                // ||v||^2 of the two keys, each from four threads' parts
-                const uint8_t *vt = smem + Ly::kV + s * Ly::kOp;
-                float q0 = row_sqnorm_part<D>(vt, key0, part);
-                float q1 = row_sqnorm_part<D>(vt, key0 + 8, part);
-                q0 += __shfl_xor_sync(0xffffffffu, q0, 1);
-                q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
-                q0 += __shfl_xor_sync(0xffffffffu, q0, 2);
-                q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&v_empty[s]);
                 const float2 v2[2] = {make_float2(q0, q0), make_float2(q1, q1)};
                 const int j0 = t * kTileKeys + key0;
                 const bool boundary = t * kTileKeys + kTileKeys - 1 > pos0;
@@ -558,6 +528,7 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
     A.plan = ws.plan;
     A.stat_ml = ws.stat_ml;
     A.stat_a2 = ws.stat_a2;
+    A.v2 = ws.v2;
     A.out = chunks == 1 ? scores : ws.part_scores;
     A.out_stride = kv_rows;
     A.total_items = blocks * chunks;
