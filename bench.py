@@ -245,8 +245,8 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # current kernels on the default workload (profiles/dram_traffic_long_32L_8kv_n131072.md).
 # Only valid for that workload and these kernel versions; None elsewhere.
 TRAFFIC_WORKLOAD = DEFAULT_WORKLOAD
-TRAFFIC = {"attn_tc_kernel": None,      # changed since the last capture
-           "rescore_tc_kernel": None,   # changed since the last capture
+TRAFFIC = {"attn_tc_kernel": 17206244864 + 400259840,
+           "rescore_tc_kernel": 17659765504 + 267694336,
            "select_kernel": 668149504 + 8272640,
            "compact_kernel": 1731538176 + 1657757952}
 
