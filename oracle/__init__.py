@@ -58,6 +58,9 @@ def _load():
         lib.oracle_unit_scores.argtypes = [ci, ci, ci, ci, ctypes.c_double, u16p, u16p, u16p,
                                            f64p]
         lib.oracle_select.argtypes = [ci, ci, ci, ci, f64p, i32p]
+        lib.oracle_unit_scores_rule.argtypes = [ci, ci, ci, ci, ctypes.c_double, ci, u16p, u16p,
+                                                u16p, f64p]
+        lib.oracle_max_pool.argtypes = [ci, ci, f64p, f64p]
         for f in (lib.oracle_window_attention, lib.oracle_unit_scores, lib.oracle_select):
             f.restype = ci
         _lib = lib
@@ -117,6 +120,45 @@ def unit_scores(q: np.ndarray, k: np.ndarray, v: np.ndarray, G: int, w: int,
     if rc != 0:
         raise ValueError("oracle_unit_scores failed (%d)" % rc)
     return S
+
+
+# aggregation rules: 0 = DropKV removal score (unit_scores), 1 = its squared form,
+# 2 = attention sum
+RULE_DROPKV, RULE_DROPKV_SQUARED, RULE_ATTN_SUM = 0, 1, 2
+
+
+def unit_scores_rule(q: np.ndarray, k: np.ndarray, v: np.ndarray, G: int, w: int, rule: int,
+                     scale: float | None = None) -> np.ndarray:
+    """Score of every key of one unit under `rule`, fp64 [n].
+
+    rule 0: unit_scores.  rule 1: sum over the window rows of (p/(1-p))^2 *
+    ||a - v_j||^2 (DropKV, "Methodology in Plain English": accumulated over the
+    window and squared).  rule 2: sum of p over the window rows and heads
+    (PyramidKV guide, "Observation Window and Aggregated Attention Eviction").
+    """
+    if rule == RULE_DROPKV:
+        return unit_scores(q, k, v, G, w, scale)
+    q, k, v, n, d = _unit_args(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    S = np.zeros(n)
+    rc = _load().oracle_unit_scores_rule(n, d, G, w, scale, int(rule), _ptr(q, ctypes.c_uint16),
+                                         _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+                                         _ptr(S, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_unit_scores_rule failed (%d)" % rc)
+    return S
+
+
+def max_pool(S: np.ndarray, kernel: int) -> np.ndarray:
+    """out[j] = max of S over the `kernel` positions centred on j, clipped to the unit
+    (DropKV page: kernel 11; BellowsKV blog: 13)."""
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    out = np.empty_like(S)
+    rc = _load().oracle_max_pool(S.shape[0], int(kernel), _ptr(S, ctypes.c_double),
+                                 _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_max_pool failed (%d)" % rc)
+    return out
 
 
 def select(S: np.ndarray, w: int, sinks: int, b: int) -> np.ndarray:

@@ -142,6 +142,85 @@ int oracle_unit_scores(int n, int d, int G, int w, double scale,
     return rc;
 }
 
+/*
+ * The other aggregation rules of one unit, over the same rows and keys as
+ * oracle_unit_scores (row i sees keys 0..n-w+(i%w)):
+ *   rule 1, squared (DropKV "Methodology in Plain English": the per-token
+ *     shift accumulated over the observation window and squared):
+ *       S[j] = sum_i (p_ij / (1 - p_ij))^2 * ||a_i - v_j||_2^2
+ *   rule 2, attention sum (PyramidKV guide, "Observation Window and
+ *     Aggregated Attention Eviction": the attention weights of the window
+ *     queries summed over queries and heads):
+ *       S[j] = sum_i p_ij
+ * Returns 0; -1 on bad sizes, rule or allocation failure; -2 if rule 1 meets
+ * some p_ij == 1.
+ */
+int oracle_unit_scores_rule(int n, int d, int G, int w, double scale, int rule,
+                            const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            double *S) {
+    if (n < 1 || d < 1 || G < 1 || w < 1 || w > n || rule < 1 || rule > 2) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!s || !a) { free(s); free(a); return -1; }
+    for (int j = 0; j < n; ++j) S[j] = 0.0;
+    const int R = G * w;
+    int rc = 0;
+    for (int i = 0; i < R && rc == 0; ++i) {
+        const int pos = n - w + (i % w);
+        const uint16_t *qrow = q + (size_t)i * d;
+        const double mx = row_logits(pos, d, scale, qrow, k, s);
+        double sum = 0.0;
+        for (int j = 0; j <= pos; ++j) {
+            s[j] = exp(s[j] - mx);
+            sum += s[j];
+        }
+        if (rule == 2) {
+            for (int j = 0; j <= pos; ++j) S[j] += s[j] / sum;
+            continue;
+        }
+        for (int c = 0; c < d; ++c) a[c] = 0.0;
+        for (int j = 0; j <= pos; ++j) {
+            const double p = s[j] / sum;
+            const uint16_t *vj = v + (size_t)j * d;
+            for (int c = 0; c < d; ++c) a[c] += p * bf16_value(vj[c]);
+        }
+        for (int j = 0; j <= pos; ++j) {
+            const double p = s[j] / sum;
+            if (!(p < 1.0)) { rc = -2; break; }
+            const uint16_t *vj = v + (size_t)j * d;
+            double dist2 = 0.0;
+            for (int c = 0; c < d; ++c) {
+                const double diff = a[c] - bf16_value(vj[c]);
+                dist2 += diff * diff;
+            }
+            const double r = p / (1.0 - p);
+            S[j] += r * r * dist2;
+        }
+    }
+    free(s);
+    free(a);
+    return rc;
+}
+
+/*
+ * Max pooling of one unit's scores (DropKV page: "a max-pool over neighbouring
+ * scores", kernel size 11; BellowsKV blog: each token takes the maximum score
+ * in a 13-position window centred on it): out[j] = max S[i] over
+ * i in [j - r, j + r] within [0, n), r = (kernel - 1) / 2.  kernel must be odd.
+ * Returns 0; -1 on bad sizes.
+ */
+int oracle_max_pool(int n, int kernel, const double *S, double *out) {
+    if (n < 1 || kernel < 1 || kernel % 2 == 0) return -1;
+    const int r = (kernel - 1) / 2;
+    for (int j = 0; j < n; ++j) {
+        double mx = -INFINITY;
+        for (int i = j - r; i <= j + r; ++i)
+            if (i >= 0 && i < n && S[i] > mx) mx = S[i];
+        out[j] = mx;
+    }
+    return 0;
+}
+
 typedef struct { double score; int32_t idx; } ranked;
 
 static int rank_cmp(const void *x, const void *y) {

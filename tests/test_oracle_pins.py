@@ -6,9 +6,12 @@ definition the DropKV page derives its closed form from), against a hand
 closed form for two keys, and against invariants (softmax rows sum to one,
 causality).  Selection is checked against a brute-force sort and its
 invariants; budgets against the sums and ratios RippleKV and PyramidKV state.
+The squared and attention-sum aggregation rules are checked against literal
+token deletion and a direct softmax, closed forms and the row-sum invariant;
+max pooling against a sliding-window brute force and scipy's maximum filter.
 A final group compiles mutated copies of the oracle (a dropped factor, a
-squared norm, a lost causal mask, a wrong tie-break) and checks that some pin
-rejects each.
+squared norm, a lost causal mask, a wrong tie-break, a short pooling window)
+and checks that some pin rejects each.
 """
 import math
 import os
@@ -154,6 +157,113 @@ def test_single_visible_key_is_rejected():
 
 
 # --------------------------------------------------------------------------
+# pins of the other aggregation rules and of max pooling
+# --------------------------------------------------------------------------
+def brute_force_rule_scores(q, k, v, G, w, rule):
+    """rule 1: sum over rows of the SQUARED removal shift, by literal deletion;
+    rule 2: sum over rows of the softmax weight, from a direct softmax."""
+    Q, K, V = _f64(q).reshape(G * w, -1), _f64(k), _f64(v)
+    n, d = K.shape
+    scale = 1.0 / math.sqrt(d)
+    S = np.zeros(n)
+    for i in range(G * w):
+        pos = n - w + i % w
+        keys = list(range(pos + 1))
+        a_full, p = _softmax_out(Q[i], K, V, keys, scale)
+        for j in keys:
+            if rule == oracle.RULE_ATTN_SUM:
+                S[j] += p[j]
+                continue
+            rest = [t for t in keys if t != j]
+            a_minus, _ = _softmax_out(Q[i], K, V, rest, scale)
+            S[j] += float(np.sum((a_minus - a_full) ** 2))
+    return S
+
+
+@pytest.mark.parametrize("rule", [oracle.RULE_DROPKV_SQUARED, oracle.RULE_ATTN_SUM])
+@pytest.mark.parametrize("G,w,n", [(1, 1, 13), (2, 3, 11), (4, 4, 24)])
+def test_rule_scores_match_brute_force(rule, G, w, n):
+    rng = np.random.default_rng(1000 * rule + G * 100 + w * 10 + n)
+    d = 8
+    q, k, v = _bf16(rng, (G * w, d), 2.0), _bf16(rng, (n, d)), _bf16(rng, (n, d))
+    S = oracle.unit_scores_rule(q, k, v, G=G, w=w, rule=rule)
+    ref = brute_force_rule_scores(q, k, v, G, w, rule)
+    np.testing.assert_allclose(S, ref, rtol=1e-10, atol=1e-300)
+
+
+def test_attention_sum_totals_rows():
+    """Each window row's weights sum to one, so sum_j S_j = G * w."""
+    rng = np.random.default_rng(21)
+    G, w, n, d = 4, 8, 300, 32
+    q, k, v = _bf16(rng, (G * w, d), 3.0), _bf16(rng, (n, d), 3.0), _bf16(rng, (n, d))
+    S = oracle.unit_scores_rule(q, k, v, G, w, oracle.RULE_ATTN_SUM)
+    assert S.sum() == pytest.approx(G * w, rel=1e-13)
+    assert np.all(S >= 0)
+    # keys after the first window slot are seen by fewer rows
+    assert np.all(S[n - w + 1:] <= G * 1.0 + 1e-12)
+
+
+def test_rule_two_key_closed_forms():
+    """n=2, one query: squared S_0 = (p_0 ||v_1 - v_0||)^2; attention sum S_0 = p_0."""
+    rng = np.random.default_rng(22)
+    d = 16
+    q, k, v = _bf16(rng, (1, d)), _bf16(rng, (2, d)), _bf16(rng, (2, d))
+    Q, K, V = _f64(q)[0], _f64(k), _f64(v)
+    p0 = 1.0 / (1.0 + math.exp((Q @ K[1] - Q @ K[0]) / 4.0))
+    gap2 = float(((V[1] - V[0]) ** 2).sum())
+    sq = oracle.unit_scores_rule(q, k, v, 1, 1, oracle.RULE_DROPKV_SQUARED)
+    at = oracle.unit_scores_rule(q, k, v, 1, 1, oracle.RULE_ATTN_SUM)
+    assert sq[0] == pytest.approx(p0 * p0 * gap2, rel=1e-12)
+    assert sq[1] == pytest.approx((1 - p0) ** 2 * gap2, rel=1e-12)
+    assert at[0] == pytest.approx(p0, rel=1e-13) and at[1] == pytest.approx(1 - p0, rel=1e-12)
+
+
+def test_squared_rule_ranks_like_dropkv_for_one_row():
+    """One row: the squared rule is the DropKV score squared, so the ranking is the same."""
+    rng = np.random.default_rng(23)
+    n, d = 200, 16
+    q, k, v = _bf16(rng, (1, d), 2.0), _bf16(rng, (n, d)), _bf16(rng, (n, d))
+    base = oracle.unit_scores(q, k, v, 1, 1)
+    sq = oracle.unit_scores_rule(q, k, v, 1, 1, oracle.RULE_DROPKV_SQUARED)
+    np.testing.assert_allclose(sq, base ** 2, rtol=1e-12)
+    assert list(oracle.select(sq, 1, 4, 50)) == list(oracle.select(base, 1, 4, 50))
+
+
+def test_squared_rule_rejects_single_visible_key():
+    rng = np.random.default_rng(24)
+    q, k, v = _bf16(rng, (3, 4)), _bf16(rng, (3, 4)), _bf16(rng, (3, 4))
+    with pytest.raises(ValueError):
+        oracle.unit_scores_rule(q, k, v, 1, 3, oracle.RULE_DROPKV_SQUARED)
+    # the attention sum has no 1 - p and is defined there
+    S = oracle.unit_scores_rule(q, k, v, 1, 3, oracle.RULE_ATTN_SUM)
+    assert S.sum() == pytest.approx(3.0, rel=1e-14)
+
+
+@pytest.mark.parametrize("n,kernel", [(1, 1), (1, 13), (5, 3), (40, 11), (40, 13), (97, 7)])
+def test_max_pool_matches_brute_force(n, kernel):
+    rng = np.random.default_rng(n * 7 + kernel)
+    S = rng.standard_normal(n)
+    r = kernel // 2
+    ref = np.array([S[max(0, j - r):j + r + 1].max() for j in range(n)])
+    np.testing.assert_array_equal(oracle.max_pool(S, kernel), ref)
+
+
+def test_max_pool_library_and_special_cases():
+    """Agrees with scipy's maximum filter (edge padding repeats a value already in the
+    clipped window); kernel 1 is the identity; a kernel wider than 2n-1 is the global max."""
+    scipy_nd = pytest.importorskip("scipy.ndimage")
+    rng = np.random.default_rng(25)
+    S = rng.standard_normal(300)
+    for kernel in (3, 11, 13):
+        np.testing.assert_array_equal(oracle.max_pool(S, kernel),
+                                      scipy_nd.maximum_filter1d(S, kernel, mode="nearest"))
+    np.testing.assert_array_equal(oracle.max_pool(S, 1), S)
+    np.testing.assert_array_equal(oracle.max_pool(S[:20], 41), np.full(20, S[:20].max()))
+    with pytest.raises(ValueError):
+        oracle.max_pool(S, 4)
+
+
+# --------------------------------------------------------------------------
 # selection pins
 # --------------------------------------------------------------------------
 def brute_select(S, w, sinks, b):
@@ -268,8 +378,13 @@ MUTATIONS = {
                    "const int pos = n - 1;\n        const uint16_t *qrow = q + (size_t)i * d;\n        const double mx = row_logits(pos, d, scale, qrow, k, s);\n        double sum = 0.0;\n        for (int j = 0; j <= pos; ++j) {\n            s[j] = exp(s[j] - mx);\n            sum += s[j];\n        }\n        for (int c = 0; c < d; ++c) a[c] = 0.0;"),
     "tie_to_higher_index": ("return (a->idx > b->idx) - (a->idx < b->idx);",
                             "return (a->idx < b->idx) - (a->idx > b->idx);"),
-    "sign_of_v": ("const double diff = a[c] - bf16_value(vj[c]);",
-                  "const double diff = a[c] + bf16_value(vj[c]);"),
+    "sign_of_v": ("const double diff = a[c] - bf16_value(vj[c]);\n                dist2 += diff * diff;\n            }\n            S[j] += p / (1.0 - p)",
+                  "const double diff = a[c] + bf16_value(vj[c]);\n                dist2 += diff * diff;\n            }\n            S[j] += p / (1.0 - p)"),
+    "squared_rule_unsquared_ratio": ("S[j] += r * r * dist2;", "S[j] += r * dist2;"),
+    "squared_rule_sign_of_v": ("const double diff = a[c] - bf16_value(vj[c]);\n                dist2 += diff * diff;\n            }\n            const double r",
+                               "const double diff = a[c] + bf16_value(vj[c]);\n                dist2 += diff * diff;\n            }\n            const double r"),
+    "attn_sum_unnormalised": ("S[j] += s[j] / sum;", "S[j] += s[j];"),
+    "pool_radius_short": ("for (int i = j - r; i <= j + r; ++i)", "for (int i = j - r; i < j + r; ++i)"),
 }
 
 
@@ -289,7 +404,11 @@ def test_pins_reject_planted_mistake(name, tmp_path, monkeypatch):
     pins = [lambda: test_single_query_removal_identity(17, 8),
             lambda: test_window_and_group_removal_identity(2, 3, 11),
             lambda: test_two_key_closed_form(),
-            lambda: test_select_tie_break_lower_index()]
+            lambda: test_select_tie_break_lower_index(),
+            lambda: test_rule_scores_match_brute_force(oracle.RULE_DROPKV_SQUARED, 2, 3, 11),
+            lambda: test_rule_two_key_closed_forms(),
+            lambda: test_attention_sum_totals_rows(),
+            lambda: test_max_pool_matches_brute_force(40, 11)]
     failed = 0
     for pin in pins:
         try:
