@@ -10,6 +10,12 @@ Prints one JSON line.  `value` counts unit-tokens (tokens x layers x KV heads,
 each scored, selected and compacted) per second over all ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--score-rule dropkv|squared|attn_sum] [--pool KERNEL]
+
+--score-rule picks what kv_score sums (the DropKV removal score by default;
+its squared form; the SnapKV/PyramidKV attention sum) and --pool adds the
+max pooling of the scores before selection (kernel 11 on the DropKV page, 13
+on the BellowsKV blog); both default to the DropKV step without pooling.
 
 --impl reference times the fp64 CPU oracle (the only reference arm: the
 pages ship no code) on a bounded sample of the same workload.
@@ -36,6 +42,7 @@ if ROOT not in sys.path:
 METRIC = "KV tokens scored+selected+compacted/s at n=128K; achieved HBM GB/s vs GB300 peak"
 UNIT = "unit-tokens/s"
 DEFAULT_WORKLOAD = "long_32L_8kv_32q_d128_n131072_pyramid10"
+SCORE_RULES = {"dropkv": 0, "squared": 1, "attn_sum": 2}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -51,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=0, help="oracle sample size (0: one per core)")
+    ap.add_argument("--score-rule", choices=sorted(SCORE_RULES), default="dropkv")
+    ap.add_argument("--pool", type=int, default=1, help="max-pool kernel before selection (1: none)")
     return ap.parse_args(argv)
 
 
@@ -176,16 +185,18 @@ def oracle_inputs(wl, budgets, units, rows_per_unit=None):
     return inputs
 
 
-def oracle_time(wl, inputs, threads):
-    """Times the oracle (score + select + gather) over prepared inputs, one unit per
-    thread; returns (seconds, unit-token equivalents).  An input with fewer than
-    G*w query rows counts as that fraction of a unit."""
+def oracle_time(wl, inputs, threads, rule=0, pool=1):
+    """Times the oracle (score under `rule`, pooling if pool > 1, select, gather) over
+    prepared inputs, one unit per thread; returns (seconds, unit-token equivalents).
+    An input with fewer than G*w query rows counts as that fraction of a unit."""
     import oracle
     w = wl.window
 
     def one(args):
         q, k, v, b = args
-        S = oracle.unit_scores(q, k, v, max(1, q.shape[0] // w), w)
+        S = oracle.unit_scores_rule(q, k, v, max(1, q.shape[0] // w), w, rule)
+        if pool > 1:
+            S = oracle.pool_unit(S, w, pool)
         idx = oracle.select(S, w, wl.num_sinks, b)
         oracle.compact(k, v, idx)
         return k.shape[0] * q.shape[0] / wl.rows
@@ -207,8 +218,9 @@ def run_reference(args, wl, budgets):
     inputs = oracle_inputs(wl, budgets, units, rows_per_unit=rows)
     times = []
     work = 0.0
+    rule = SCORE_RULES[args.score_rule]
     for s in range(args.warmup + args.steps):
-        dt, work = oracle_time(wl, inputs, cores)
+        dt, work = oracle_time(wl, inputs, cores, rule, args.pool)
         if s >= args.warmup:
             times.append(dt)
     t = sum(times) / len(times)
@@ -220,7 +232,7 @@ def run_reference(args, wl, budgets):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name},
+            "config": bench_config_tag(wl, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -234,16 +246,18 @@ def run_reference(args, wl, budgets):
 # ---------------------------------------------------------------------------
 # Kernels of one step and how many launches each makes (the timed region
 # launches only these).
-STAGES = ["attention", "rescore", "select", "compact"]
+STAGES = ["attention", "rescore", "pool", "select", "compact"]
 # attention: plan_kernel, attn_tc_kernel, attn_merge_kernel; rescore: plan_kernel,
 # rescore_tc_kernel and, when the window rows span more than one 128-row chunk,
 # chunk_sum_kernel.
-LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "select": 1, "compact": 1}
+# pool: pool_kernel, only with --pool > 1.
+LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "pool": 1, "select": 1, "compact": 1}
 STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
-                 "select": "select_kernel", "compact": "compact_kernel"}
+                 "pool": "pool_kernel", "select": "select_kernel", "compact": "compact_kernel"}
 # DRAM bytes (read + write) per launch from the single-pass ncu capture of the
 # current kernels on the default workload (profiles/dram_traffic_long_32L_8kv_n131072.md).
-# Only valid for that workload and these kernel versions; None elsewhere.
+# Only valid for that workload, the DropKV rule without pooling, and these kernel
+# versions; None elsewhere.
 TRAFFIC_WORKLOAD = DEFAULT_WORKLOAD
 TRAFFIC = {"attn_tc_kernel": 17206244864 + 400259840,
            "rescore_tc_kernel": 17659765504 + 267694336,
@@ -267,10 +281,18 @@ def product_budgets(kv, wl):
     return np.asarray(rows, dtype=np.int32)
 
 
-def stage_roofline(stage, ms, wl, budgets, peaks):
+def bench_config_tag(wl, args):
+    tag = {"workload": wl.name}
+    if args.score_rule != "dropkv" or args.pool > 1:
+        tag.update(score_rule=args.score_rule, pool_kernel=args.pool)
+    return tag
+
+
+def stage_roofline(stage, ms, wl, budgets, peaks, rule=0):
     """Roofline of one stage's kernel from its algorithmic bytes (and, for the two
     scoring passes, their algorithmic tensor flops: two d-long dot products per
-    (window row, visible key) pair each)."""
+    (window row, visible key) pair each, one for the attention sum, which needs
+    only q.k).  The attention sum needs no V: its passes read K only."""
     d = wl.head_dim
     units = wl.num_units
     n_tot = sum(wl.seq_lengths())
@@ -279,10 +301,13 @@ def stage_roofline(stage, ms, wl, budgets, peaks):
     kv = kv_cache_bytes(L, H, d, n_tot)
     q = wl.num_requests * L * wl.num_q_heads * wl.window * d * 2
     keys = n_tot * L * H
+    kv_pass = kv // 2 if rule == SCORE_RULES["attn_sum"] else kv
     if stage == "attention":
-        nbytes = kv + q                        # K, V and the window queries, once
+        nbytes = kv_pass + q                   # K, V and the window queries, once
     elif stage == "rescore":
-        nbytes = kv + q + keys * 4             # ... plus one fp32 score per key
+        nbytes = kv_pass + q + keys * 4        # ... plus one fp32 score per key
+    elif stage == "pool":
+        nbytes = keys * 4 * 2                  # every score read and written once
     elif stage == "select":
         nbytes = keys * 4 + rows * 4 + 8 * (units + 1) * 2
     else:
@@ -291,7 +316,7 @@ def stage_roofline(stage, ms, wl, budgets, peaks):
     out = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "frac": achieved / peaks["hbm_gbs"], "algorithmic_bytes": nbytes}
     if stage in ("attention", "rescore"):
-        flops = pass_pairs(wl) * 4 * d
+        flops = pass_pairs(wl) * (2 if rule == SCORE_RULES["attn_sum"] else 4) * d
         tpeak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
         out["tensor"] = {"algorithmic_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
                          "peak_tflops": tpeak, "frac": flops / (ms * 1e-3) / 1e12 / tpeak}
@@ -353,9 +378,12 @@ def main(argv=None):
 
     budgets = product_budgets(kv, wl)
     dw = DeviceWorkload(wl, device=dev)
-    prob = kv.Problem.for_workload(wl, device=dev)
+    rule = SCORE_RULES[args.score_rule]
+    pool = args.pool
+    prob = kv.Problem.for_workload(wl, device=dev, score_rule=rule, pool_kernel=pool)
     bufs = kv.Buffers(prob, budgets)
     stream = torch.cuda.current_stream(dev)
+    ranked = bufs.pooled if pool > 1 else bufs.scores
 
     def step(ev=None):
         if ev is not None:
@@ -366,14 +394,18 @@ def main(argv=None):
         kv.kv_score_rescore(prob, dw.q, dw.k, dw.v, bufs.scores, bufs.score_ws, stream)
         if ev is not None:
             ev[2].record(stream)
-        kv.kv_select_topk(prob, bufs.scores, bufs.budgets, bufs.offsets, bufs.sel,
-                          bufs.select_ws, stream)
+        if pool > 1:
+            kv.kv_pool_scores(prob, pool, bufs.scores, bufs.pooled, stream)
         if ev is not None:
             ev[3].record(stream)
+        kv.kv_select_topk(prob, ranked, bufs.budgets, bufs.offsets, bufs.sel,
+                          bufs.select_ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
         kv.kv_compact(prob, dw.k, dw.v, bufs.sel, bufs.offsets, bufs.total_rows, bufs.k_out,
                       bufs.v_out, stream)
         if ev is not None:
-            ev[4].record(stream)
+            ev[5].record(stream)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -389,7 +421,8 @@ def main(argv=None):
     if args.steps <= 0:
         per = (time.perf_counter() - t_w0) / max(args.warmup, 1)
         args.steps = int(min(2000, max(20, math.ceil(2.0 / max(per, 1e-4)))))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -412,19 +445,23 @@ def main(argv=None):
     alg_bytes = algorithmic_bytes(wl, budgets)
     hbm_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
 
-    dominant = max(("attention", "rescore", "select", "compact"), key=lambda s: stage_ms[s])
-    roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks)
-    traffic = TRAFFIC.get(STAGE_KERNELS[dominant]) if wl.name == TRAFFIC_WORKLOAD else None
+    stages = [s for s in STAGES if s != "pool" or pool > 1]
+    if pool <= 1:
+        stage_ms.pop("pool")
+    dominant = max(stages, key=lambda s: stage_ms[s])
+    roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule)
+    traffic = TRAFFIC.get(STAGE_KERNELS[dominant]) \
+        if wl.name == TRAFFIC_WORKLOAD and rule == 0 and pool <= 1 else None
     roof.update({"kernel": STAGE_KERNELS[dominant], "peak_source": peak_src,
                  "traffic": traffic, "stage_ms": stage_ms[dominant],
-                 "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks)["frac"]
-                                for s in STAGES}})
+                 "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
+                                                  rule)["frac"] for s in stages}})
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "layers": wl.num_layers,
+            "config": {**bench_config_tag(wl, args), "layers": wl.num_layers,
                        "kv_heads": wl.num_kv_heads, "q_heads": wl.num_q_heads,
                        "head_dim": wl.head_dim, "n": wl.seq_lengths(), "window": wl.window,
                        "budget": "%s, mean %s tokens/head" % (wl.budget_policy,
@@ -439,7 +476,7 @@ def main(argv=None):
                     "peak_source": peak_src},
             "stages_ms": stage_ms,
             "roofline": roof,
-            "gpu_launches": args.steps * (sum(LAUNCHES_PER_STEP.values())
+            "gpu_launches": args.steps * (sum(LAUNCHES_PER_STEP[s] for s in stages)
                                           + (1 if wl.rows > 128 else 0)),
             "clocks": clocks}
 
@@ -452,12 +489,13 @@ def main(argv=None):
         cores = os.cpu_count() or 1
         n_units = args.cpu_units or min(cores, 16, wl.num_units)
         thr = min(cores, n_units)
-        dt, work = oracle_time(wl, oracle_inputs(wl, ob, list(range(n_units))), thr)
+        dt, work = oracle_time(wl, oracle_inputs(wl, ob, list(range(n_units))), thr, rule, pool)
         line["cpu_baseline"] = {"value": work / dt, "unit": UNIT,
                                 "cores": thr, "kind": "oracle",
                                 "sample": "%d full units (of %d) of the same workload, one "
-                                          "thread each, fp64 score + select + gather"
-                                          % (n_units, wl.num_units)}
+                                          "thread each, fp64 score (%s)%s + select + gather"
+                                          % (n_units, wl.num_units, args.score_rule,
+                                             " + pool %d" % pool if pool > 1 else "")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -4,6 +4,9 @@
  * Three steps run on one GPU, each asynchronous on the caller's stream:
  *
  *   kv_score        per-token DropKV removal score of every cached key
+ *                   (or, by kv_problem.score_rule, its squared form or the
+ *                   SnapKV/PyramidKV attention sum)
+ *   kv_pool_scores  optional 1-D max pooling of the scores before selection
  *   kv_select_topk  budgeted per-(request, layer, KV head) selection
  *   kv_compact      ragged gather of the kept K/V rows
  *
@@ -19,6 +22,16 @@
  *    (window attention with split-K and a merge, then a rescoring pass that
  *    expands ||a - v||^2 = ||a||^2 - 2 a.v + ||v||^2, the expansion the same
  *    section describes), never materialising the n x w attention matrix.
+ *  - Other aggregation rules (score_rule).  KV_SCORE_DROPKV_SQUARED: the same
+ *    page, "Methodology in Plain English", accumulates the shift over the
+ *    window squared: S_j = sum (p_j / (1 - p_j))^2 * ||a - v_j||_2^2.
+ *    KV_SCORE_ATTN_SUM: the PyramidKV guide, "Observation Window and
+ *    Aggregated Attention Eviction": S_j = sum of the attention weights p_j of
+ *    the window queries over queries and heads.  Both sum over the same rows.
+ *  - Pooling.  DropKV, "Methodology in Plain English" (a max-pool over
+ *    neighbouring scores, after SnapKV; kernel size 11 in its evaluation) and
+ *    the BellowsKV blog (the maximum score in a 13-position window centred on
+ *    each token).
  *  - Selection.  Same page, "Methodology in Plain English" (keep the highest
  *    scores, pin the recent w) and the PyramidKV guide, "Observation Window
  *    and Aggregated Attention Eviction" (always keep the first 4 sinks).
@@ -78,6 +91,13 @@ typedef enum kv_status {
     KV_ERR_UNSUPPORTED = 6   /* shape outside what the kernels handle */
 } kv_status;
 
+/* What kv_score sums over the window rows r that see key j (kv_problem.score_rule). */
+typedef enum kv_score_rule {
+    KV_SCORE_DROPKV = 0,          /* p_rj / (1 - p_rj) * ||a_r - v_j||_2 (DropKV)       */
+    KV_SCORE_DROPKV_SQUARED = 1,  /* (p_rj / (1 - p_rj))^2 * ||a_r - v_j||_2^2          */
+    KV_SCORE_ATTN_SUM = 2         /* p_rj (observation-window attention sum)            */
+} kv_score_rule;
+
 typedef struct kv_problem {
     int32_t num_requests;            /* R >= 0 (0: every call is a no-op) */
     int32_t num_layers;              /* L >= 1 */
@@ -86,7 +106,7 @@ typedef struct kv_problem {
     int32_t head_dim;                /* d: 64 or 128 */
     int32_t window;                  /* w >= 1 */
     int32_t num_sinks;               /* s >= 0 (4 in the method) */
-    int32_t reserved;                /* must be 0 */
+    int32_t score_rule;              /* kv_score_rule (0: the DropKV score) */
     const int64_t *seq_offsets_host; /* [R+1] cu_seqlens, host memory; n_r >= s + w, n_r < 2^31 */
     const int64_t *seq_offsets_dev;  /* the same [R+1] values, device memory */
     float softmax_scale;             /* logit scale, normally 1/sqrt(d); > 0 */
@@ -97,8 +117,9 @@ kv_status kv_score_workspace_size(const kv_problem *p, size_t *bytes);
 
 /*
  * Full scoring step: kv_score_attention then kv_score_rescore on one stream.
- * scores receives one fp32 score per key of every unit, >= 0 (or +inf when a
- * window row puts all of its attention on one key).
+ * scores receives one fp32 score per key of every unit under p->score_rule,
+ * >= 0 (the two DropKV rules give +inf when a window row puts all of its
+ * attention on one key; the attention sum is at most G * w).
  */
 kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const void *v,
                    float *scores, void *workspace, size_t workspace_bytes, void *stream);
@@ -119,6 +140,21 @@ kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void 
 kv_status kv_score_rescore(const kv_problem *p, const void *q_win, const void *k,
                            const void *v, float *scores, void *workspace,
                            size_t workspace_bytes, void *stream);
+
+/*
+ * Max pooling of the scores, one unit at a time, over the keys outside the
+ * observation window (the SnapKV convention the DropKV page follows: the w
+ * window keys are kept anyway and are not pooled into their neighbours):
+ *   scores_out[j] = max of scores_in[i], i in [j - r, j + r] within [0, n_r - w),
+ *                   r = (kernel - 1) / 2, for j in [0, n_r - w);
+ *   scores_out[j] = scores_in[j] for the window keys j in [n_r - w, n_r).
+ * kernel: odd, 1..255 (11 on the DropKV page, 13 on the BellowsKV blog; 1
+ * copies).  scores_in / scores_out: device f32 [L][H][N_tot], 16-byte
+ * aligned, not overlapping (KV_ERR_INVALID_ARG otherwise).  The result feeds
+ * kv_select_topk unchanged (pooled scores are still >= 0).
+ */
+kv_status kv_pool_scores(const kv_problem *p, int32_t kernel, const float *scores_in,
+                         float *scores_out, void *stream);
 
 /*
  * Host helper: offsets[u+1] = offsets[u] + budgets[u] for the R*L*H units,

@@ -25,16 +25,19 @@ from . import _build
 __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attention",
            "kv_score_rescore", "kv_make_offsets", "kv_select_topk", "kv_compact",
            "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
-           "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "EXPORTED_SYMBOLS", "evict"]
+           "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores", "EXPORTED_SYMBOLS",
+           "evict", "KV_SCORE_DROPKV", "KV_SCORE_DROPKV_SQUARED", "KV_SCORE_ATTN_SUM"]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
     KV_ERR_UNSUPPORTED = range(7)
+# kv_problem.score_rule
+KV_SCORE_DROPKV, KV_SCORE_DROPKV_SQUARED, KV_SCORE_ATTN_SUM = range(3)
 
 EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_score_rescore", "kv_make_offsets", "kv_select_workspace_size",
                     "kv_select_topk", "kv_compact", "kv_check_status", "kv_status_string",
                     "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc",
-                    "kv_set_wait_limit_ns", "kv_get_wait_limit_ns")
+                    "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores")
 
 
 class KvError(RuntimeError):
@@ -47,7 +50,7 @@ class _KvProblem(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("num_layers", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("num_sinks", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("num_sinks", ctypes.c_int32), ("score_rule", ctypes.c_int32),
                 ("seq_offsets_host", ctypes.POINTER(ctypes.c_int64)),
                 ("seq_offsets_dev", ctypes.c_void_p), ("softmax_scale", ctypes.c_float)]
 
@@ -86,6 +89,7 @@ def load(path: Optional[str] = None):
         "kv_budgets_pyramid": [i32, i32, f64, f64, f64, ctypes.POINTER(i32)],
         "kv_budgets_ripple": [i32, i32, ctypes.POINTER(f64), f64, f64, ctypes.POINTER(i32)],
         "kv_score_noalloc": [P, vp, vp, vp, vp, vp],
+        "kv_pool_scores": [P, i32, vp, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -135,6 +139,8 @@ class Problem:
     num_sinks: int = 4
     softmax_scale: Optional[float] = None
     device: object = "cuda"
+    score_rule: int = KV_SCORE_DROPKV   # what kv_score sums (KV_SCORE_*)
+    pool_kernel: int = 1                # evict(): max-pool width before selection (1: none)
 
     def __post_init__(self):
         import torch
@@ -144,7 +150,8 @@ class Problem:
             torch.zeros(1, dtype=torch.int64, device=self.device)
         scale = self.softmax_scale if self.softmax_scale is not None else 1.0 / math.sqrt(self.head_dim)
         self._c = _KvProblem(len(self.lengths), self.num_layers, self.num_kv_heads,
-                             self.num_q_heads, self.head_dim, self.window, self.num_sinks, 0,
+                             self.num_q_heads, self.head_dim, self.window, self.num_sinks,
+                             int(self.score_rule),
                              self.cu_host.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                              self.cu_dev.data_ptr(), float(scale))
 
@@ -165,9 +172,11 @@ class Problem:
         return int(self.cu_host[-1])
 
     @classmethod
-    def for_workload(cls, wl, device="cuda") -> "Problem":
+    def for_workload(cls, wl, device="cuda", score_rule: int = KV_SCORE_DROPKV,
+                     pool_kernel: int = 1) -> "Problem":
         return cls(wl.seq_lengths(), wl.num_layers, wl.num_kv_heads, wl.num_q_heads,
-                   wl.head_dim, wl.window, wl.num_sinks, device=device)
+                   wl.head_dim, wl.window, wl.num_sinks, device=device, score_rule=score_rule,
+                   pool_kernel=pool_kernel)
 
 
 # ---------------------------------------------------------------------------
@@ -207,6 +216,11 @@ def kv_score_noalloc(prob, q, k, v, scores, stream=None):
     """kv_score with the library's own fixed scratch (no workspace argument)."""
     _check(load().kv_score_noalloc(prob.c, _ptr(q), _ptr(k), _ptr(v), _ptr(scores),
                                    _stream(stream)), "kv_score_noalloc")
+
+
+def kv_pool_scores(prob, kernel: int, scores_in, scores_out, stream=None):
+    _check(load().kv_pool_scores(prob.c, int(kernel), _ptr(scores_in), _ptr(scores_out),
+                                 _stream(stream)), "kv_pool_scores")
 
 
 def kv_make_offsets(prob, budgets_host: np.ndarray) -> np.ndarray:
@@ -295,12 +309,18 @@ class Buffers:
         self.sel = torch.empty(max(self.total_rows, 1), dtype=torch.int32, device=dev)
         self.k_out = torch.empty((max(self.total_rows, 1), d), dtype=torch.bfloat16, device=dev)
         self.v_out = torch.empty_like(self.k_out)
+        self.pooled = torch.empty_like(self.scores) if prob.pool_kernel > 1 else None
 
 
 def evict(prob: Problem, q, k, v, bufs: Buffers, stream=None):
-    """Score, select and compact on `stream`; returns (sel_idx, k_out, v_out, offsets)."""
+    """Score (and pool, if prob.pool_kernel > 1), select and compact on `stream`;
+    returns (sel_idx, k_out, v_out, offsets)."""
     kv_score(prob, q, k, v, bufs.scores, bufs.score_ws, stream)
-    kv_select_topk(prob, bufs.scores, bufs.budgets, bufs.offsets, bufs.sel, bufs.select_ws, stream)
+    ranked = bufs.scores
+    if prob.pool_kernel > 1:
+        kv_pool_scores(prob, prob.pool_kernel, bufs.scores, bufs.pooled, stream)
+        ranked = bufs.pooled
+    kv_select_topk(prob, ranked, bufs.budgets, bufs.offsets, bufs.sel, bufs.select_ws, stream)
     kv_compact(prob, k, v, bufs.sel, bufs.offsets, bufs.total_rows, bufs.k_out, bufs.v_out, stream)
     n = bufs.total_rows
     return bufs.sel[:n], bufs.k_out[:n], bufs.v_out[:n], bufs.offsets

@@ -25,7 +25,8 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
     if (!p) return KV_ERR_INVALID_ARG;
     if (p->num_requests < 0 || p->num_layers < 1 || p->num_kv_heads < 1 ||
         p->num_q_heads < p->num_kv_heads || p->num_q_heads % p->num_kv_heads != 0 ||
-        p->window < 1 || p->num_sinks < 0 || p->reserved != 0)
+        p->window < 1 || p->num_sinks < 0 || p->score_rule < KV_SCORE_DROPKV ||
+        p->score_rule > KV_SCORE_ATTN_SUM)
         return KV_ERR_INVALID_ARG;
     if (!(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale)) return KV_ERR_INVALID_ARG;
     if (p->head_dim != 64 && p->head_dim != 128) return KV_ERR_UNSUPPORTED;
@@ -39,6 +40,7 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
     P->d = p->head_dim;
     P->w = p->window;
     P->sinks = p->num_sinks;
+    P->rule = p->score_rule;
     P->rows = (int)(G * p->window);
     P->cu = reinterpret_cast<const long long *>(p->seq_offsets_dev);
     P->host_cu = reinterpret_cast<const long long *>(p->seq_offsets_host);
@@ -165,6 +167,22 @@ kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const 
     st = kv_score_attention(p, q_win, k, v, workspace, workspace_bytes, stream);
     if (st != KV_OK) return st;
     return kv_score_rescore(p, q_win, k, v, scores, workspace, workspace_bytes, stream);
+}
+
+kv_status kv_pool_scores(const kv_problem *p, int32_t kernel, const float *scores_in,
+                         float *scores_out, void *stream) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK) return st;
+    if (kernel < 1 || kernel > 255 || kernel % 2 == 0) return KV_ERR_INVALID_ARG;
+    if (P.units == 0) return KV_OK;
+    if (!scores_in || !scores_out || !aligned16(scores_in) || !aligned16(scores_out))
+        return KV_ERR_INVALID_ARG;
+    const uintptr_t bytes = (uintptr_t)P.L * P.H * (uintptr_t)P.N_tot * sizeof(float);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(scores_in);
+    const uintptr_t b = reinterpret_cast<uintptr_t>(scores_out);
+    if (a < b + bytes && b < a + bytes) return KV_ERR_INVALID_ARG;
+    return map_cuda(launch_pool(P, kernel, scores_in, scores_out, (cudaStream_t)stream));
 }
 
 kv_status kv_make_offsets(const kv_problem *p, const int32_t *budgets_host, int64_t *offsets_host) {

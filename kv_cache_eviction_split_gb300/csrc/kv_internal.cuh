@@ -22,6 +22,7 @@ constexpr size_t kHeaderBytes = 256;
 // Problem description passed by value to every kernel.
 struct DevProblem {
     int R, L, H, Hq, G, d, w, sinks;
+    int rule;                 // kv_score_rule
     int rows;                 // G * w
     int max_n;                // longest request
     int max_splits;           // ceil(max_n / kSplitKeys)
@@ -93,6 +94,8 @@ cudaError_t launch_attention(const DevProblem &P, const __nv_bfloat16 *q, const 
 cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const __nv_bfloat16 *v, float *scores, const ScoreWs &ws,
                            cudaStream_t s);
+cudaError_t launch_pool(const DevProblem &P, int kernel, const float *in, float *out,
+                        cudaStream_t s);
 cudaError_t launch_select(const DevProblem &P, const float *scores, const int32_t *budgets,
                           const int64_t *offsets, int32_t *sel, int *status, cudaStream_t s);
 cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __nv_bfloat16 *v,

@@ -1,6 +1,7 @@
 // kv_rescore.cu -- pass 2 of the DropKV score on the tcgen05 tensor cores.
 //
-// For every key j of a unit and every window row r that sees it:
+// For every key j of a unit and every window row r that sees it (score rule
+// KV_SCORE_DROPKV):
 //     s   = q_r . k_j                         (tensor core, fp32 in TMEM)
 //     X   = (a_hi_r + a_lo_r) . v_j           (tensor core, two bf16 MMAs)
 //     p   = 2^(s * scale * log2 e - m_r - log2 l_r)     (= e / l_r)
@@ -10,6 +11,13 @@
 // (DropKV, Key Contributions 1 and Methodology in Plain English).  a = a_hi +
 // a_lo is the pass-1 output split into two bf16 halves, so the expansion keeps
 // ~16 bits of a instead of bf16's 8.
+//
+// The other rules change only the term: KV_SCORE_DROPKV_SQUARED adds the
+// square of the same term, (p/(1-p))^2 x (DropKV, "Methodology in Plain
+// English": the window sum taken squared), and KV_SCORE_ATTN_SUM adds p alone
+// (PyramidKV guide, "Observation Window and Aggregated Attention Eviction").
+// The attention sum needs neither V nor a: its kernel loads only Q and K,
+// issues only S = K Q^T and uses the freed shared memory for four K stages.
 //
 // Orientation is key-major: one MMA tile is 128 keys (M, TMEM lanes) by the
 // rows of a 128-row chunk of the unit's window rows (N).  The epilogue reads
@@ -47,23 +55,25 @@ using namespace sm100;
 constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
 constexpr int kTilesPerItem = 64;
-constexpr int kStages = 2;
 constexpr int kPrefetchTiles = 4;   // K/V tiles requested into L2 ahead of the smem loads
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBlockBytes = kChunkRows * 128;   // one [128 rows][64 bf16] swizzled box
 
-template <int D>
+template <int D, int RULE>
 struct Layout {
+    static constexpr bool kX = RULE != KV_SCORE_ATTN_SUM;  // X = a . v (and V) needed
     static constexpr int kOp = (D / 64) * kBlockBytes;     // one [128][D] bf16 operand
+    static constexpr int kKSt = kX ? 2 : 4;                // K stages
+    static constexpr int kVSt = kX ? 2 : 0;                // V stages
     static constexpr int kQ = 0;
     static constexpr int kAhi = kQ + kOp;
-    static constexpr int kAlo = kAhi + kOp;
-    static constexpr int kK = kAlo + kOp;
-    static constexpr int kV = kK + kStages * kOp;
-    static constexpr int kBars = kV + kStages * kOp;
-    static constexpr int kNumBars = 4 * kStages + 2 + 4 + 1;
+    static constexpr int kAlo = kAhi + (kX ? kOp : 0);
+    static constexpr int kK = kAlo + (kX ? kOp : 0);
+    static constexpr int kV = kK + kKSt * kOp;
+    static constexpr int kBars = kV + kVSt * kOp;
+    static constexpr int kNumBars = 2 * kKSt + 2 * (kVSt > 0 ? kVSt : 1) + 2 + 4 + 1;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -110,10 +120,12 @@ __device__ __forceinline__ int chunk_rows_n(const DevProblem &P, int c) {
     return ((rc + 31) / 32) * 32;
 }
 
-// One (row pair, key) term pair: p/(1 - p) * sqrt(x) with p = 2^(s c - m'),
+// One (row pair, key) term pair.  p = 2^(s c - m'); `vis` = 0 drops a row that
+// does not see the key.  KV_SCORE_DROPKV adds p/(1 - p) * sqrt(x) with
 // x = max(||a||^2 - 2X + ||v||^2, 0), written as p * x * rsqrt((1 - p)^2 x + tiny)
-// so one MUFU op gives sqrt(x)/(1-p) and x = 0 gives 0.  `vis` = 0 drops a row
-// that does not see the key.
+// so one MUFU op gives sqrt(x)/(1-p) and x = 0 gives 0; the squared rule adds
+// the square of that term; the attention sum adds p.
+template <int RULE>
 __device__ __forceinline__ void term_pair(float2 sp, float2 xp, float2 nm, float2 a2, float2 v2,
                                           float cscale, float2 &acc, bool vis0 = true,
                                           bool vis1 = true) {
@@ -121,19 +133,30 @@ __device__ __forceinline__ void term_pair(float2 sp, float2 xp, float2 nm, float
     float2 pr = make_float2(ex2_approx(t.x), ex2_approx(t.y));
     if (!vis0) pr.x = 0.f;
     if (!vis1) pr.y = 0.f;
-    const float2 den = __ffma2_rn(pr, make_float2(-1.f, -1.f), make_float2(1.f, 1.f));
-    const float2 av = __fadd2_rn(a2, v2);
-    float2 x = __ffma2_rn(xp, make_float2(-2.f, -2.f), av);
-    x.x = fmaxf(x.x, 0.f);
-    x.y = fmaxf(x.y, 0.f);
-    const float2 y = __ffma2_rn(__fmul2_rn(den, den), x, make_float2(1e-30f, 1e-30f));
-    const float2 px = __fmul2_rn(pr, x);
-    acc = __ffma2_rn(px, make_float2(rsqrt_approx(y.x), rsqrt_approx(y.y)), acc);
+    if constexpr (RULE == KV_SCORE_ATTN_SUM) {
+        acc = __fadd2_rn(acc, pr);
+    } else {
+        const float2 den = __ffma2_rn(pr, make_float2(-1.f, -1.f), make_float2(1.f, 1.f));
+        const float2 av = __fadd2_rn(a2, v2);
+        float2 x = __ffma2_rn(xp, make_float2(-2.f, -2.f), av);
+        x.x = fmaxf(x.x, 0.f);
+        x.y = fmaxf(x.y, 0.f);
+        const float2 y = __ffma2_rn(__fmul2_rn(den, den), x, make_float2(1e-30f, 1e-30f));
+        const float2 px = __fmul2_rn(pr, x);
+        const float2 rs = make_float2(rsqrt_approx(y.x), rsqrt_approx(y.y));
+        if constexpr (RULE == KV_SCORE_DROPKV_SQUARED) {
+            const float2 tr = __fmul2_rn(px, rs);
+            acc = __ffma2_rn(tr, tr, acc);
+        } else {
+            acc = __ffma2_rn(px, rs, acc);
+        }
+    }
 }
 
 // Adds the terms of one 32-column group for the thread's two keys: sv / xv are
 // 16x256b.x4 loads of S and X (v[4r], v[4r+1]: key 0, rows 2 part + 8r + {0,1};
 // v[4r+2], v[4r+3]: key 1, the same rows).  Every row sees both keys.
+template <int RULE>
 __device__ __forceinline__ void rescore_x4(const float (&sv)[16], const float (&xv)[16],
                                            const float2 *nm, const float2 *a2, float cscale,
                                            const float2 (&v2)[2], float2 (&acc)[2]) {
@@ -141,9 +164,9 @@ __device__ __forceinline__ void rescore_x4(const float (&sv)[16], const float (&
     for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int k = 0; k < 2; ++k)
-            term_pair(make_float2(sv[4 * r + 2 * k], sv[4 * r + 2 * k + 1]),
-                      make_float2(xv[4 * r + 2 * k], xv[4 * r + 2 * k + 1]), nm[r], a2[r], v2[k],
-                      cscale, acc[k]);
+            term_pair<RULE>(make_float2(sv[4 * r + 2 * k], sv[4 * r + 2 * k + 1]),
+                            make_float2(xv[4 * r + 2 * k], xv[4 * r + 2 * k + 1]), nm[r], a2[r],
+                            v2[k], cscale, acc[k]);
 }
 
 // -m' = -(m + log2 l) and ||a||^2 of one unit-local row; padding rows (>= rows)
@@ -165,6 +188,7 @@ __device__ __forceinline__ void row_stats(const float2 *ml, const float *a2, int
 // Recomputes the row statistics from the unit's arrays (row0 = unit-local row of
 // pair 0): this path runs for one or two tiles per unit, in a loop of its own so
 // the masks stay out of the unrolled code of the other tiles.
+template <int RULE>
 __device__ __forceinline__ void rescore_x4_window(const float (&sv)[16], const float (&xv)[16],
                                                const float2 *ml, const float *a2g, int rows,
                                                int row0, int w, const int (&jrel)[2],
@@ -178,28 +202,31 @@ __device__ __forceinline__ void rescore_x4_window(const float (&sv)[16], const f
         const int rm0 = row % w;
         const int rm1 = rm0 + 1 == w ? 0 : rm0 + 1;
         for (int k = 0; k < 2; ++k)
-            term_pair(make_float2(sv[4 * r + 2 * k], sv[4 * r + 2 * k + 1]),
-                      make_float2(xv[4 * r + 2 * k], xv[4 * r + 2 * k + 1]),
-                      make_float2(n0, n1), make_float2(q0, q1), v2[k], cscale, acc[k],
-                      jrel[k] <= rm0, jrel[k] <= rm1);
+            term_pair<RULE>(make_float2(sv[4 * r + 2 * k], sv[4 * r + 2 * k + 1]),
+                            make_float2(xv[4 * r + 2 * k], xv[4 * r + 2 * k + 1]),
+                            make_float2(n0, n1), make_float2(q0, q1), v2[k], cscale, acc[k],
+                            jrel[k] <= rm0, jrel[k] <= rm1);
     }
 }
 
-template <int D>
+template <int D, int RULE>
 __global__ void __launch_bounds__(kThreads, 1)
 rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_ahi,
                   const __grid_constant__ CUtensorMap tm_alo, const RescoreArgs A) {
-    using Ly = Layout<D>;
+    using Ly = Layout<D, RULE>;
+    constexpr bool kX = Ly::kX;
+    constexpr int kKSt = Ly::kKSt;
+    constexpr int kVSt = kX ? Ly::kVSt : 1;   // barrier slots (unused without X)
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
-    uint64_t *k_full = bars, *k_empty = bars + kStages;
-    uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
-    uint64_t *qa_full = bars + 4 * kStages, *qa_empty = qa_full + 1;
+    uint64_t *k_full = bars, *k_empty = bars + kKSt;
+    uint64_t *v_full = bars + 2 * kKSt, *v_empty = v_full + kVSt;
+    uint64_t *qa_full = v_empty + kVSt, *qa_empty = qa_full + 1;
     uint64_t *tm_full = qa_empty + 1, *tm_empty = tm_full + 2;
     uint64_t *mma_done = tm_empty + 2;     // the MMA thread's last MMAs are done (exit)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
@@ -208,9 +235,11 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     if (threadIdx.x == 0) {
         *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
         if (*abort_flag) post_status(A.status, KV_ERR_UNSUPPORTED);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKSt; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kVSt; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
@@ -264,7 +293,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int kb = 0; kb < D / 64; ++kb) {
                     tma_prefetch_2d(&tm_k, kb * 64, ky);
-                    tma_prefetch_2d(&tm_v, kb * 64, ky);
+                    if constexpr (kX) tma_prefetch_2d(&tm_v, kb * 64, ky);
                 }
                 if (++pf_t >= pf_end) {
                     pf_item += gridDim.x;
@@ -278,19 +307,23 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const UnitInfo U = unit_info(P, it.u, P.cu);
                 ok = mbar_wait(qa_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, P.wait_ns);
                 if (!ok) break;
-                mbar_arrive_expect_tx(qa_full, 3 * Ly::kOp);
+                mbar_arrive_expect_tx(qa_full, (kX ? 3 : 1) * Ly::kOp);
                 const int qy = (int)(U.q_row0 + it.c * kChunkRows);
                 const int ay = (int)(it.u * A.a_rows + it.c * kChunkRows);
 #pragma unroll
                 for (int kb = 0; kb < D / 64; ++kb) {
                     tma_load_2d(smem + Ly::kQ + kb * kBlockBytes, &tm_q, qa_full, kb * 64, qy);
-                    tma_load_2d(smem + Ly::kAhi + kb * kBlockBytes, &tm_ahi, qa_full, kb * 64, ay);
-                    tma_load_2d(smem + Ly::kAlo + kb * kBlockBytes, &tm_alo, qa_full, kb * 64, ay);
+                    if constexpr (kX) {
+                        tma_load_2d(smem + Ly::kAhi + kb * kBlockBytes, &tm_ahi, qa_full, kb * 64,
+                                    ay);
+                        tma_load_2d(smem + Ly::kAlo + kb * kBlockBytes, &tm_alo, qa_full, kb * 64,
+                                    ay);
+                    }
                 }
                 ++qcount;
                 for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
-                    const int s = (int)(tcount % kStages);
-                    const uint32_t par = (uint32_t)((tcount / kStages) & 1) ^ 1u;
+                    const int s = (int)(tcount % kKSt);
+                    const uint32_t par = (uint32_t)((tcount / kKSt) & 1) ^ 1u;
                     const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
                     pf_step();
                     ok = mbar_wait(&k_empty[s], par, abort_flag, P.wait_ns);
@@ -301,14 +334,18 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, &tm_k,
                                     &k_full[s], kb * 64, ky);
                     ++kiss;
-                    ok = mbar_wait(&v_empty[s], par, abort_flag, P.wait_ns);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
+                    if constexpr (kX) {
+                        const int sv = (int)(tcount % kVSt);
+                        const uint32_t pv = (uint32_t)((tcount / kVSt) & 1) ^ 1u;
+                        ok = mbar_wait(&v_empty[sv], pv, abort_flag, P.wait_ns);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&v_full[sv], Ly::kOp);
 #pragma unroll
-                    for (int kb = 0; kb < D / 64; ++kb)
-                        tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, &tm_v,
-                                    &v_full[s], kb * 64, ky);
-                    ++viss;
+                        for (int kb = 0; kb < D / 64; ++kb)
+                            tma_load_2d(smem + Ly::kV + sv * Ly::kOp + kb * kBlockBytes, &tm_v,
+                                        &v_full[sv], kb * 64, ky);
+                        ++viss;
+                    }
                 }
                 ++icount;
             }
@@ -319,10 +356,12 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             // drain: the last load issued into each buffer lands before the CTA exits
             // (the earlier ones were consumed before their buffer was refilled)
             if (qcount > 0) mbar_drain(qa_full, (uint32_t)((qcount - 1) & 1), kDrainNs);
-            for (int s = 0; s < kStages; ++s) {
-                const long long ku = kiss / kStages + ((kiss % kStages) > s ? 1 : 0);
-                const long long vu = viss / kStages + ((viss % kStages) > s ? 1 : 0);
+            for (int s = 0; s < kKSt; ++s) {
+                const long long ku = kiss / kKSt + ((kiss % kKSt) > s ? 1 : 0);
                 if (ku > 0) mbar_drain(&k_full[s], (uint32_t)((ku - 1) & 1), kDrainNs);
+            }
+            for (int s = 0; s < kVSt; ++s) {
+                const long long vu = viss / kVSt + ((viss % kVSt) > s ? 1 : 0);
                 if (vu > 0) mbar_drain(&v_full[s], (uint32_t)((vu - 1) & 1), kDrainNs);
             }
         }
@@ -341,8 +380,8 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const uint64_t hb = sdesc_k_sw128(smem_u32(smem + Ly::kAhi));
                 const uint64_t lb = sdesc_k_sw128(smem_u32(smem + Ly::kAlo));
                 for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
-                    const int s = (int)(tcount % kStages);
-                    const uint32_t par = (uint32_t)((tcount / kStages) & 1);
+                    const int s = (int)(tcount % kKSt);
+                    const uint32_t par = (uint32_t)((tcount / kKSt) & 1);
                     const int b = (int)(tcount & 1);          // TMEM buffer of this tile
                     ok = mbar_wait(&tm_empty[b], (uint32_t)((tcount >> 1) & 1) ^ 1u, abort_flag,
                                    P.wait_ns) &&
@@ -352,7 +391,6 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     const uint32_t d_s = tmem + b * 256;
                     const uint32_t d_x = d_s + 128;
                     const uint64_t ka = sdesc_k_sw128(smem_u32(smem + Ly::kK + s * Ly::kOp));
-                    const uint64_t va = sdesc_k_sw128(smem_u32(smem + Ly::kV + s * Ly::kOp));
                     mma_ss_c<false>(d_s, ka, qb, idesc);
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
@@ -363,27 +401,35 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                                 mma_ss_c<true>(d_s, sdesc_add(ka, ko), sdesc_add(qb, ko), idesc);
                         }
                     mma_commit(&k_empty[s]);
-                    ok = mbar_wait(&v_full[s], par, abort_flag, P.wait_ns);
-                    if (!ok) break;
-                    tc_fence_after();
-                    mma_ss_c<false>(d_x, va, hb, idesc);
+                    if constexpr (kX) {
+                        const int sv = (int)(tcount % kVSt);
+                        const uint32_t pv = (uint32_t)((tcount / kVSt) & 1);
+                        ok = mbar_wait(&v_full[sv], pv, abort_flag, P.wait_ns);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t va = sdesc_k_sw128(smem_u32(smem + Ly::kV + sv * Ly::kOp));
+                        mma_ss_c<false>(d_x, va, hb, idesc);
 #pragma unroll
-                    for (int kb = 0; kb < D / 64; ++kb)
+                        for (int kb = 0; kb < D / 64; ++kb)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t ko = kb * kBlockBytes + kk * 32;
-                            if (kb | kk)
-                                mma_ss_c<true>(d_x, sdesc_add(va, ko), sdesc_add(hb, ko), idesc);
-                        }
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t ko = kb * kBlockBytes + kk * 32;
+                                if (kb | kk)
+                                    mma_ss_c<true>(d_x, sdesc_add(va, ko), sdesc_add(hb, ko),
+                                                   idesc);
+                            }
 #pragma unroll
-                    for (int kb = 0; kb < D / 64; ++kb)
+                        for (int kb = 0; kb < D / 64; ++kb)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t ko = kb * kBlockBytes + kk * 32;
-                            mma_ss_c<true>(d_x, sdesc_add(va, ko), sdesc_add(lb, ko), idesc);
-                        }
-                    mma_commit(&tm_full[b]);
-                    mma_commit(&v_empty[s]);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t ko = kb * kBlockBytes + kk * 32;
+                                mma_ss_c<true>(d_x, sdesc_add(va, ko), sdesc_add(lb, ko), idesc);
+                            }
+                        mma_commit(&tm_full[b]);
+                        mma_commit(&v_empty[sv]);
+                    } else {
+                        mma_commit(&tm_full[b]);
+                    }
                 }
                 mma_commit(qa_empty);
                 ++icount;
@@ -423,8 +469,8 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             float *out = A.out + (long long)it.c * A.out_stride + U.kv_row0;
             const int pos0 = U.n - P.w;
             const float *u_v2 = A.v2 + U.kv_row0;
-            float vq[2];
-            {
+            float vq[2] = {0.f, 0.f};
+            if constexpr (kX) {
                 const int jf = it.t_begin * kTileKeys + key0;
                 vq[0] = jf < U.n ? __ldg(u_v2 + jf) : 0.f;
                 vq[1] = jf + 8 < U.n ? __ldg(u_v2 + jf + 8) : 0.f;
@@ -433,7 +479,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const int b = (int)(tcount & 1);              // TMEM buffer of this tile
                 // ||v||^2 of the two keys of this tile (loaded a tile ahead)
                 const float q0 = vq[0], q1 = vq[1];
-                if (t + 1 < it.t_end) {
+                if (kX && t + 1 < it.t_end) {
                     const int jn = (t + 1) * kTileKeys + key0;
                     vq[0] = jn < U.n ? __ldg(u_v2 + jn) : 0.f;
                     vq[1] = jn + 8 < U.n ? __ldg(u_v2 + jn + 8) : 0.f;
@@ -456,23 +502,23 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     for (int g = 0; g < 4; ++g) {
                         if (g < groups) {
                             tmem_ld16x256_x4(s_col + g * 32, sA);
-                            tmem_ld16x256_x4(x_col + g * 32, xA);
+                            if constexpr (kX) tmem_ld16x256_x4(x_col + g * 32, xA);
                             tmem_ld_wait();
                             reg_fence(sA);
-                            reg_fence(xA);
-                            rescore_x4(sA, xA, nm + 4 * g, a2 + 4 * g, cscale, v2, acc);
+                            if constexpr (kX) reg_fence(xA);
+                            rescore_x4<RULE>(sA, xA, nm + 4 * g, a2 + 4 * g, cscale, v2, acc);
                         }
                     }
                 } else {
 #pragma unroll 1
                     for (int g = 0; g < groups; ++g) {
                         tmem_ld16x256_x4(s_col + g * 32, sA);
-                        tmem_ld16x256_x4(x_col + g * 32, xA);
+                        if constexpr (kX) tmem_ld16x256_x4(x_col + g * 32, xA);
                         tmem_ld_wait();
                         reg_fence(sA);
-                        reg_fence(xA);
-                        rescore_x4_window(sA, xA, u_ml, u_a2, P.rows, row_first + 32 * g, P.w,
-                                          jrel, cscale, v2, acc);
+                        if constexpr (kX) reg_fence(xA);
+                        rescore_x4_window<RULE>(sA, xA, u_ml, u_a2, P.rows, row_first + 32 * g,
+                                                P.w, jrel, cscale, v2, acc);
                     }
                 }
                 tc_fence_before();
@@ -510,7 +556,7 @@ __global__ void chunk_sum_kernel(const float *__restrict__ part, long long strid
     }
 }
 
-template <int D>
+template <int D, int RULE>
 cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                       const __nv_bfloat16 *v, float *scores, const ScoreWs &ws, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mhi, mlo;
@@ -538,11 +584,13 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int smem = Layout<D>::kTotal;
-    cudaFuncSetAttribute(rescore_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = Layout<D, RULE>::kTotal;
+    cudaFuncSetAttribute(rescore_tc_kernel<D, RULE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem);
     const long long grid = std::min<long long>(sms, A.total_items);
     if (grid > 0)
-        rescore_tc_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, mhi, mlo, A);
+        rescore_tc_kernel<D, RULE>
+            <<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, mhi, mlo, A);
     if (chunks > 1)
         chunk_sum_kernel<<<sms * 8, 256, 0, st>>>(ws.part_scores, kv_rows, chunks, scores);
     return cudaGetLastError();
@@ -553,8 +601,17 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
 cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const __nv_bfloat16 *v, float *scores, const ScoreWs &ws,
                            cudaStream_t s) {
-    return P.d == 64 ? rescore_d<64>(P, q, k, v, scores, ws, s)
-                     : rescore_d<128>(P, q, k, v, scores, ws, s);
+    switch (P.rule) {
+        case KV_SCORE_DROPKV_SQUARED:
+            return P.d == 64 ? rescore_d<64, KV_SCORE_DROPKV_SQUARED>(P, q, k, v, scores, ws, s)
+                             : rescore_d<128, KV_SCORE_DROPKV_SQUARED>(P, q, k, v, scores, ws, s);
+        case KV_SCORE_ATTN_SUM:
+            return P.d == 64 ? rescore_d<64, KV_SCORE_ATTN_SUM>(P, q, k, v, scores, ws, s)
+                             : rescore_d<128, KV_SCORE_ATTN_SUM>(P, q, k, v, scores, ws, s);
+        default:
+            return P.d == 64 ? rescore_d<64, KV_SCORE_DROPKV>(P, q, k, v, scores, ws, s)
+                             : rescore_d<128, KV_SCORE_DROPKV>(P, q, k, v, scores, ws, s);
+    }
 }
 
 }  // namespace kvevict

@@ -161,6 +161,18 @@ def max_pool(S: np.ndarray, kernel: int) -> np.ndarray:
     return out
 
 
+def pool_unit(S: np.ndarray, w: int, kernel: int) -> np.ndarray:
+    """Pooling of one unit's scores in the SnapKV convention the DropKV page follows: the
+    keys outside the observation window, [0, n - w), are max-pooled among themselves; the
+    w window keys (kept by selection anyway) are copied."""
+    S = np.asarray(S, dtype=np.float64)
+    out = S.copy()
+    c = S.shape[0] - w
+    if c > 0:
+        out[:c] = max_pool(S[:c], kernel)
+    return out
+
+
 def select(S: np.ndarray, w: int, sinks: int, b: int) -> np.ndarray:
     """Kept indices of one unit, ascending int32 [b] (sinks + top middle + window)."""
     S = np.ascontiguousarray(S, dtype=np.float64)

@@ -10,7 +10,13 @@ the host from the same seed (no oracle input is read back from the GPU):
   GPU's own scores, and equality with the oracle's selection on oracle scores
   except for tokens within 1e-3 relative of the oracle's k-th score;
 * compaction: the packed rows equal the input rows at the GPU's indices, bit
-  for bit.
+  for bit;
+* pooling (when a pool kernel is set): the pooled scores equal the oracle's
+  pooling of the GPU's own raw scores bit for bit (a max of fp32 values is
+  exact), and the oracle's pooling of oracle scores within the score
+  tolerance; selection is then checked on the pooled scores.
+
+Every score rule is checked the same way against oracle.unit_scores_rule.
 """
 from __future__ import annotations
 
@@ -44,12 +50,14 @@ def product_budgets(kv, wl, profile=None) -> np.ndarray:
 class GpuRun:
     """The three C-ABI calls on one workload, results kept on the device."""
 
-    def __init__(self, kv, wl, budgets=None, dw=None):
+    def __init__(self, kv, wl, budgets=None, dw=None, score_rule=0, pool_kernel=1):
         import torch
         from synth.device import DeviceWorkload
         self.wl = wl
+        self.rule = score_rule
+        self.pool = pool_kernel
         self.dw = dw or DeviceWorkload(wl)
-        self.prob = kv.Problem.for_workload(wl)
+        self.prob = kv.Problem.for_workload(wl, score_rule=score_rule, pool_kernel=pool_kernel)
         prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
         self.profile = prof
         if budgets is None:
@@ -67,6 +75,9 @@ class GpuRun:
         u = wl.unit_index(r, l, h)
         n = int(cu[r + 1] - cu[r])
         scores = b.scores[l, h, int(cu[r]):int(cu[r + 1])].cpu().numpy()
+        if b.pooled is not None:
+            pooled = b.pooled[l, h, int(cu[r]):int(cu[r + 1])].cpu().numpy()
+            scores = (scores, pooled)
         o0, o1 = int(b.offsets_host[u]), int(b.offsets_host[u + 1])
         sel = b.sel[o0:o1].cpu().numpy()
         kout = b.k_out[o0:o1].cpu().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
@@ -74,24 +85,40 @@ class GpuRun:
         return n, scores, sel, kout, vout, int(self.budgets.reshape(-1)[u])
 
 
-def oracle_unit(wl, dw, r, l, h):
+def oracle_unit(wl, dw, r, l, h, rule=0):
     q, k, v = dw.unit_host(r, l, h)
-    S = oracle.unit_scores(q, k, v, wl.group, wl.window)
+    S = oracle.unit_scores_rule(q, k, v, wl.group, wl.window, rule)
     return q, k, v, S
+
+
+def _check_scores(g, S, what):
+    big = S >= SCORE_ATOL
+    rel = np.abs(g[big].astype(np.float64) - S[big]) / S[big]
+    assert np.all(np.isfinite(g)), "non-finite GPU score"
+    max_rel = float(rel.max()) if rel.size else 0.0
+    assert max_rel <= SCORE_RTOL, "%s: score rel err %.3g" % (what, max_rel)
+    assert np.all(np.abs(g[~big].astype(np.float64) - S[~big]) <= SCORE_ATOL)
+    return max_rel
 
 
 def check_unit(run: GpuRun, r, l, h, oracle_out=None):
     """Asserts parity of one unit; returns a small dict of error figures."""
     wl = run.wl
     n, g_scores, g_sel, kout, vout, b = run.unit_results(r, l, h)
-    q, k, v, S = oracle_out if oracle_out is not None else oracle_unit(wl, run.dw, r, l, h)
+    q, k, v, S = oracle_out if oracle_out is not None else \
+        oracle_unit(wl, run.dw, r, l, h, run.rule)
+    where = "unit (%d,%d,%d)" % (r, l, h)
     # scores
-    big = S >= SCORE_ATOL
-    rel = np.abs(g_scores[big].astype(np.float64) - S[big]) / S[big]
-    assert np.all(np.isfinite(g_scores)), "non-finite GPU score"
-    max_rel = float(rel.max()) if rel.size else 0.0
-    assert max_rel <= SCORE_RTOL, "unit (%d,%d,%d): score rel err %.3g" % (r, l, h, max_rel)
-    assert np.all(np.abs(g_scores[~big].astype(np.float64) - S[~big]) <= SCORE_ATOL)
+    if isinstance(g_scores, tuple):
+        g_raw, g_scores = g_scores
+        max_rel = _check_scores(g_raw, S, where)
+        np.testing.assert_array_equal(
+            g_scores, oracle.pool_unit(g_raw.astype(np.float64), wl.window, run.pool),
+            err_msg="%s: pooling of the GPU's own scores" % where)
+        S = oracle.pool_unit(S, wl.window, run.pool)
+        _check_scores(g_scores, S, where + " pooled")
+    else:
+        max_rel = _check_scores(g_scores, S, where)
     # selection: the GPU's rule on its own scores is exact
     mine = oracle.select(g_scores.astype(np.float64), wl.window, wl.num_sinks, b)
     np.testing.assert_array_equal(g_sel, mine, err_msg="selection rule on GPU scores")
@@ -118,7 +145,8 @@ def check_units(run: GpuRun, units, threads=None):
     wl = run.wl
     threads = threads or min(len(units), os.cpu_count() or 1)
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        futs = {u: ex.submit(oracle_unit, wl, run.dw, *wl.unit_coords(u)) for u in units}
+        futs = {u: ex.submit(oracle_unit, wl, run.dw, *wl.unit_coords(u), run.rule)
+                for u in units}
         out = {}
         for u in units:
             out[u] = check_unit(run, *wl.unit_coords(u), oracle_out=futs[u].result())

@@ -113,3 +113,26 @@ def test_config_budgets_equal_oracle(kv):
         prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
         np.testing.assert_array_equal(parity.product_budgets(kv, wl, prof),
                                       oracle.segment_budgets(wl, prof))
+
+
+def test_score_rule_and_pool_argument_checks(kv):
+    lib = kv.load()
+    for rule in (kv.KV_SCORE_DROPKV, kv.KV_SCORE_DROPKV_SQUARED, kv.KV_SCORE_ATTN_SUM):
+        assert kv.kv_score_workspace_size(_prob(kv, score_rule=rule)) > 0
+    for bad in (-1, 3):
+        with pytest.raises(kv.KvError) as e:
+            kv.kv_score_workspace_size(_prob(kv, score_rule=bad))
+        assert e.value.code == kv.KV_ERR_INVALID_ARG
+    p = _prob(kv)
+    nbytes = 2 * 2 * 3000 * 4          # L * H * N_tot floats
+    a, b = 1 << 24, (1 << 24) + (1 << 20)
+    for kernel in (0, 2, 12, 257):      # even, or outside 1..255
+        assert lib.kv_pool_scores(p.c, kernel, a, b, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_pool_scores(p.c, 11, None, b, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_pool_scores(p.c, 11, a + 4, b, None) == kv.KV_ERR_INVALID_ARG
+    # overlapping input and output ranges
+    assert lib.kv_pool_scores(p.c, 11, a, a, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_pool_scores(p.c, 11, a, a + nbytes - 16, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_pool_scores(p.c, 11, a + nbytes - 16, a, None) == kv.KV_ERR_INVALID_ARG
+    empty = _prob(kv, lengths=[])
+    assert lib.kv_pool_scores(empty.c, 11, None, None, None) == kv.KV_OK

@@ -263,6 +263,18 @@ def test_max_pool_library_and_special_cases():
         oracle.max_pool(S, 4)
 
 
+def test_pool_unit_keeps_window_out_of_the_pool():
+    """The window keys are copied and never raise a candidate's pooled score."""
+    S = np.zeros(30)
+    S[25:] = 100.0          # window w = 5, large scores
+    S[3] = 2.0
+    out = oracle.pool_unit(S, 5, 11)
+    np.testing.assert_array_equal(out[25:], S[25:])
+    np.testing.assert_array_equal(out[:9], 2.0)        # 3 +- 5, clipped at 0
+    np.testing.assert_array_equal(out[9:25], 0.0)      # nothing leaks from the window
+    np.testing.assert_array_equal(oracle.pool_unit(S[:5], 5, 11), S[:5])   # no candidates
+
+
 # --------------------------------------------------------------------------
 # selection pins
 # --------------------------------------------------------------------------
