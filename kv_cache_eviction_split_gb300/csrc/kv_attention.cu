@@ -31,6 +31,9 @@
 // removed when the partial is written.  When S of tile j+1 is complete, P V of
 // tile j is too, so the rescale needs no extra wait.
 //
+// The attention-sum rule needs only m and l: attn_stats_kernel (below) computes
+// them from K alone.
+//
 // Warp roles (320 threads): warp 0 TMA producer (the lanes' Q chunks per item;
 // K tiles through a 3-stage ring running ahead of V tiles in a 2-stage ring);
 // warp 1 TMEM owner and MMA issuer; warps 2-5 softmax of lane 0, 6-9 of lane 1.
@@ -129,6 +132,18 @@ __device__ __forceinline__ LaneWork lane_work(const AttnArgs &A, const Item &it,
         w.stride = 2;
     }
     return w;
+}
+
+// Maximum of 32 values as a tree of 3-input maxima: depth 4 instead of a
+// 16-long dependency chain.
+__device__ __forceinline__ float max32_tree(const float (&v)[32]) {
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) a[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    a[10] = fmaxf(v[30], v[31]);
+    const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]);
+    const float b2 = fmax3(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+    return fmaxf(fmax3(b0, b1, b2), b3);
 }
 
 // Two fp32 values as fp16x2 (round to nearest), the first in the low half.
@@ -512,14 +527,16 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 const int lim = row_valid ? pos - kt : -1;
                 float mx = -INFINITY;
                 if (!boundary) {
+                    float sa[32], sb[32];
+                    tmem_ld32(s_base, sa);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        float sv[32];
-                        tmem_ld32(s_base + 32 * c, sv);
+                        float(&cur)[32] = (c & 1) ? sb : sa;
+                        float(&nxt)[32] = (c & 1) ? sa : sb;
                         tmem_ld_wait();
-                        reg_fence(sv);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) mx = fmax3(mx, sv[i], sv[i + 1]);
+                        reg_fence(cur);
+                        if (c < 3) tmem_ld32(s_base + 32 * (c + 1), nxt);
+                        mx = fmaxf(mx, max32_tree(cur));
                     }
                 } else {
 #pragma unroll 1
@@ -572,14 +589,18 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                         // keys 32c..32c+31 -> fp16x2 columns 16c..16c+15: only columns of
                         // keys already read are overwritten
                         uint32_t pw[16];
+                        float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                        make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
                             const float2 t = __ffma2_rn(make_float2(cur[i], cur[i + 1]), cs2, nm2);
                             const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
-                            lsum = __fadd2_rn(lsum, make_float2(p0, p1));
+                            ps[(i / 2) & 3] = __fadd2_rn(ps[(i / 2) & 3], make_float2(p0, p1));
                             pw[i / 2] = pack_half2(p0, p1);
                         }
                         tmem_st16u(s_base + 16 * c, pw);
+                        lsum = __fadd2_rn(lsum, __fadd2_rn(__fadd2_rn(ps[0], ps[1]),
+                                                           __fadd2_rn(ps[2], ps[3])));
                     }
                 } else {
 #pragma unroll 1
@@ -645,6 +666,307 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// Row statistics only (score rule KV_SCORE_ATTN_SUM).  The attention sum needs
+// per window row just m and l (PyramidKV guide, "Observation Window and
+// Aggregated Attention Eviction": S_j sums the softmax weights, which need the
+// row's normaliser and nothing else), so this pass streams K alone: per tile
+// S_L = Q_L K^T into one of two TMEM buffers of lane L, and the softmax warps
+// keep a running (m, l) per row with one ex2 per (row, key).  Same items,
+// lanes and partial layout as attn_tc_kernel; the merge reads only (m, l).
+// Warp roles: warp 0 producer (Q per item, K through a 4-stage ring), warp 1
+// TMEM owner and MMA issuer, warps 2-5 rows of lane 0, 6-9 rows of lane 1.
+// ---------------------------------------------------------------------------
+constexpr int kStatKSt = 4;
+constexpr float kStatLazyLog2 = 8.f;   // m is raised only when a chunk max exceeds it by 2^8
+
+template <int D>
+struct StatLayout {
+    static constexpr int kOp = (D / 64) * kBlockBytes;
+    static constexpr int kQ = 0;                          // Q of lane 0, then lane 1
+    static constexpr int kK = kQ + 2 * kOp;
+    static constexpr int kBars = kK + kStatKSt * kOp;
+    static constexpr int kNumBars = 2 * kStatKSt + 2 + 4 + 4 + 1;
+    static constexpr int kMisc = kBars + kNumBars * 8;
+    static constexpr int kTotal = kMisc + 16;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_stats_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k, const AttnArgs A) {
+    using Ly = StatLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
+    uint64_t *k_full = bars, *k_empty = bars + kStatKSt;
+    uint64_t *q_full = bars + 2 * kStatKSt, *q_empty = q_full + 1;
+    uint64_t *s_full = q_empty + 1;        // [2 L + b]: S in buffer b of lane L
+    uint64_t *s_free = s_full + 4;         // [2 L + b]: buffer read (4 warps)
+    uint64_t *mma_done = s_free + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
+        if (*abort_flag) post_status(A.status, KV_ERR_UNSUPPORTED);
+        for (int s = 0; s < kStatKSt; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], kSoftWarps / 2);
+        }
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool run = *abort_flag == 0;
+
+
+    if (run && warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            long long tcount = 0, icount = 0, qcount = 0, kiss = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+                const Item it = decode_item(item, A, P);
+                const UnitInfo U = unit_info(P, it.u, P.cu);
+                const LaneWork w0 = lane_work(A, it, 0), w1 = lane_work(A, it, 1);
+                const bool two_q = A.parts == 1 && w1.steps > 0;
+                ok = mbar_wait(q_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, P.wait_ns);
+                if (!ok) break;
+                mbar_arrive_expect_tx(q_full, (two_q ? 2 : 1) * Ly::kOp);
+                for (int L = 0; L < (two_q ? 2 : 1); ++L) {
+                    const int qy = (int)(U.q_row0 + (L ? w1.chunk : w0.chunk) * kChunkRows);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kQ + L * Ly::kOp + kb * kBlockBytes, &tm_q,
+                                    q_full, kb * 64, qy);
+                }
+                ++qcount;
+                const int ntiles = it.t1 - it.t0;
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const long long kc = tcount + i;
+                    const int s = (int)(kc % kStatKSt);
+                    const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
+                    ok = mbar_wait(&k_empty[s], (uint32_t)((kc / kStatKSt) & 1) ^ 1u, abort_flag,
+                                   P.wait_ns);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, &tm_k,
+                                    &k_full[s], kb * 64, ky);
+                    ++kiss;
+                }
+                tcount += ntiles;
+                ++icount;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
+            if (qcount > 0) mbar_drain(q_full, (uint32_t)((qcount - 1) & 1), kDrainNs);
+            for (int s = 0; s < kStatKSt; ++s) {
+                const long long uses = kiss / kStatKSt + ((kiss % kStatKSt) > s ? 1 : 0);
+                if (uses > 0) mbar_drain(&k_full[s], (uint32_t)((uses - 1) & 1), kDrainNs);
+            }
+        }
+    } else if (run && warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(128, kTileKeys);
+            long long tcount = 0, icount = 0;
+            long long sc[2] = {0, 0};   // S tiles issued per lane (buffer and parity)
+            bool ok = true;
+            for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+                const Item it = decode_item(item, A, P);
+                const LaneWork w[2] = {lane_work(A, it, 0), lane_work(A, it, 1)};
+                const int releaser = (A.parts == 1 && w[1].steps > 0) ? 1 : -1;
+                ok = mbar_wait(q_full, (uint32_t)(icount & 1), abort_flag, P.wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                const int nmax = max(w[0].steps, w[1].steps);
+                for (int j = 0; ok && j < nmax; ++j)
+                    for (int L = 0; ok && L < 2; ++L) {
+                        if (j >= w[L].steps) continue;
+                        const long long cnt = sc[L] + j;
+                        const int b = (int)(cnt & 1);
+                        const long long kc = tcount + w[L].first + (long long)j * w[L].stride;
+                        const int s = (int)(kc % kStatKSt);
+                        ok = mbar_wait(&s_free[2 * L + b], (uint32_t)((cnt >> 1) & 1) ^ 1u,
+                                       abort_flag, P.wait_ns) &&
+                             mbar_wait(&k_full[s], (uint32_t)((kc / kStatKSt) & 1), abort_flag,
+                                       P.wait_ns);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t qa = sdesc_k_sw128(
+                            smem_u32(smem + Ly::kQ + (A.parts == 1 ? L : 0) * Ly::kOp));
+                        const uint64_t kb0 = sdesc_k_sw128(smem_u32(smem + Ly::kK + s * Ly::kOp));
+                        const uint32_t d_s = tmem + 256 * L + 128 * b;
+#pragma unroll
+                        for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t ko = kb * kBlockBytes + kk * 32;
+                                if (kb | kk)
+                                    mma_ss_c<true>(d_s, sdesc_add(qa, ko), sdesc_add(kb0, ko),
+                                                   idesc_s);
+                                else
+                                    mma_ss_c<false>(d_s, qa, kb0, idesc_s);
+                            }
+                        mma_commit(&s_full[2 * L + b]);
+                        if (releaser < 0 || releaser == L) mma_commit(&k_empty[s]);
+                    }
+                mma_commit(q_empty);
+                sc[0] += w[0].steps;
+                sc[1] += w[1].steps;
+                tcount += it.t1 - it.t0;
+                ++icount;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
+            mma_commit(mma_done);
+            mbar_drain(mma_done, 0, kDrainNs);
+        }
+    } else if (run) {
+        // ------------------------------------------------------------ row statistics
+        const int L = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int rr = quarter * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const float cs = P.scale_log2;
+        const float2 cs2 = make_float2(cs, cs);
+        long long sc = 0;
+        bool ok = true;
+        for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+            const Item it = decode_item(item, A, P);
+            const LaneWork w = lane_work(A, it, L);
+            const UnitInfo U = unit_info(P, it.u, P.cu);
+            const int row = w.chunk * kChunkRows + rr;
+            const bool row_valid = row < P.rows;
+            const int slot = A.parts == 1 ? it.split : 2 * it.split + L;
+            const size_t prow_idx =
+                ((size_t)it.u * P.max_splits * A.parts + slot) * P.rows + row;
+            if (w.steps == 0) {
+                if (A.parts == 2 && row_valid) A.part_ml[prow_idx] = make_float2(-INFINITY, 0.f);
+                continue;
+            }
+            const int pos = U.n - P.w + (row % P.w);
+            const int pos_min = U.n - P.w;
+            float m = -INFINITY, l = 0.f;
+            // one 32-key chunk: raise m lazily, then l += sum of 2^(s c - m)
+            auto chunk32 = [&](const float (&v)[32]) {
+                const float mt = max32_tree(v) * cs;
+                const bool up = mt > m + kStatLazyLog2;
+                l *= up ? ex2_approx(m - mt) : 1.f;
+                m = up ? mt : m;
+                const float2 nm2 = make_float2(-m, -m);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float2 t = __ffma2_rn(make_float2(v[i], v[i + 1]), cs2, nm2);
+                    acc[(i / 2) & 3] = __fadd2_rn(acc[(i / 2) & 3],
+                                                  make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                }
+                const float2 a01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                l += a01.x + a01.y;
+            };
+            for (int j = 0; ok && j < w.steps; ++j) {
+                const int ti = w.first + j * w.stride;
+                const int kt = (it.t0 + ti) * kTileKeys;
+                const long long cnt = sc + j;
+                const int b = (int)(cnt & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[2 * L + b],
+                                                       (uint32_t)((cnt >> 1) & 1), abort_flag,
+                                                       P.wait_ns));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t s_base = tmem + lane_addr + 256 * L + 128 * b;
+                if (kt + kTileKeys - 1 <= pos_min) {
+                    // every row of the chunk sees every key of the tile
+                    float sa[32], sb[32];
+                    tmem_ld32(s_base, sa);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float(&cur)[32] = (c & 1) ? sb : sa;
+                        float(&nxt)[32] = (c & 1) ? sa : sb;
+                        tmem_ld_wait();
+                        reg_fence(cur);
+                        if (c < 3) {
+                            tmem_ld32(s_base + 32 * (c + 1), nxt);
+                        } else {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&s_free[2 * L + b]);
+                        }
+                        chunk32(cur);
+                    }
+                } else {
+                    // the tile reaches the window: key kt + i is seen when i <= lim
+                    const int lim = row_valid ? pos - kt : -1;
+#pragma unroll 1
+                    for (int c = 0; c < kTileKeys / 16; ++c) {
+                        float sv[16];
+                        tmem_ld16(s_base + 16 * c, sv);
+                        tmem_ld_wait();
+                        reg_fence(sv);
+                        if (c == kTileKeys / 16 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&s_free[2 * L + b]);
+                        }
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            mx = fmaxf(mx, 16 * c + i > lim ? -INFINITY : sv[i]);
+                        const float mt = mx * cs;
+                        const bool up = mt > m + kStatLazyLog2;
+                        l *= up ? ex2_approx(m - mt) : 1.f;
+                        m = up ? mt : m;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc += 16 * c + i > lim ? 0.f : ex2_approx(fmaf(sv[i], cs, -m));
+                        l += acc;
+                    }
+                }
+            }
+            if (!ok) break;
+            if (row_valid) A.part_ml[prow_idx] = make_float2(m, l);
+            sc += w.steps;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            post_status(A.status, KV_ERR_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
 template <int D>
 cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                         const __nv_bfloat16 *v, const ScoreWs &ws, cudaStream_t st) {
@@ -668,9 +990,16 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long grid = std::min<long long>(sms, A.total_items);
+    if (P.rule == KV_SCORE_ATTN_SUM) {
+        const int smem = StatLayout<D>::kTotal;
+        cudaFuncSetAttribute(attn_stats_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+        if (grid > 0) attn_stats_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, A);
+        return cudaGetLastError();
+    }
     const int smem = Layout<D>::kTotal;
     cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    const long long grid = std::min<long long>(sms, A.total_items);
     if (grid > 0) attn_tc_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
     return cudaGetLastError();
 }

@@ -8,9 +8,9 @@
 // anyway and are copied unchanged.
 //
 // HBM-bound: one read and one write of every score.  A CTA takes a tile of
-// 2048 packed tokens of one (layer, KV head) score row plus a halo of r on
-// each side into shared memory with coalesced loads; each thread pools 8
-// consecutive tokens from registers (one request and all candidates: no
+// 4096 packed tokens of one (layer, KV head) score row plus a halo of r on
+// each side into shared memory with coalesced loads (16 per thread in flight);
+// each thread pools 16 consecutive tokens from registers (one request and all candidates: no
 // masks), or, near a request end or the window, with per-token bounds; the
 // results go back through shared memory so the stores are coalesced too.
 #include <cfloat>
@@ -21,7 +21,7 @@ namespace kvevict {
 namespace {
 
 constexpr int kPoolThreads = 256;
-constexpr int kPoolPer = 8;
+constexpr int kPoolPer = 16;
 constexpr int kPoolTile = kPoolThreads * kPoolPer;   // tokens per CTA
 constexpr int kMaxRadius = 127;                      // kernel <= 255
 constexpr int kXs = kPoolTile + 2 * kMaxRadius + 8;  // halo + float4 over-read
@@ -39,7 +39,7 @@ __device__ __forceinline__ int find_request(const long long *cu, int R, long lon
 // RAD >= 0: radius known at compile time, windows read into registers;
 // RAD < 0: radius `rad_rt`, windows read from shared memory.
 template <int RAD>
-__global__ void __launch_bounds__(kPoolThreads)
+__global__ void __launch_bounds__(kPoolThreads, 4)
 pool_kernel(const DevProblem P, int rad_rt, const float *__restrict__ in, float *__restrict__ out,
             long long tiles_per_row) {
     __shared__ __align__(16) float xs[kXs];
@@ -52,10 +52,20 @@ pool_kernel(const DevProblem P, int rad_rt, const float *__restrict__ in, float 
     float *rout = out + row * N;
     const int tid = threadIdx.x;
 
-    // xs[s] = score of packed token t0 - rad + s (-inf outside the row)
-    for (int s = tid; s < kXs; s += kPoolThreads) {
+    // xs[s] = score of packed token t0 - rad + s (-inf outside the row): every load
+    // of the thread is issued before the first shared-memory store
+    constexpr int kLoads = (kXs + kPoolThreads - 1) / kPoolThreads;
+    float ld[kLoads];
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+        const int s = tid + q * kPoolThreads;
         const long long t = t0 - rad + s;
-        xs[s] = (s < kPoolTile + 2 * rad && t >= 0 && t < N) ? rin[t] : -INFINITY;
+        ld[q] = (s < kPoolTile + 2 * rad && t >= 0 && t < N) ? __ldg(rin + t) : -INFINITY;
+    }
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+        const int s = tid + q * kPoolThreads;
+        if (s < kXs) xs[s] = ld[q];
     }
     __syncthreads();
 
@@ -125,8 +135,9 @@ pool_kernel(const DevProblem P, int rad_rt, const float *__restrict__ in, float 
             }
         }
         float4 *yv = reinterpret_cast<float4 *>(ys + kPoolPer * tid);
-        yv[0] = make_float4(y[0], y[1], y[2], y[3]);
-        yv[1] = make_float4(y[4], y[5], y[6], y[7]);
+#pragma unroll
+        for (int q = 0; q < kPoolPer / 4; ++q)
+            yv[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
     }
     __syncthreads();
     for (int s = tid; s < kPoolTile; s += kPoolThreads) {

@@ -17,7 +17,7 @@
 // English": the window sum taken squared), and KV_SCORE_ATTN_SUM adds p alone
 // (PyramidKV guide, "Observation Window and Aggregated Attention Eviction").
 // The attention sum needs neither V nor a: its kernel loads only Q and K,
-// issues only S = K Q^T and uses the freed shared memory for four K stages.
+// issues only S = K Q^T, and runs four K stages and four TMEM buffers.
 //
 // Orientation is key-major: one MMA tile is 128 keys (M, TMEM lanes) by the
 // rows of a 128-row chunk of the unit's window rows (N).  The epilogue reads
@@ -73,7 +73,9 @@ struct Layout {
     static constexpr int kK = kAlo + (kX ? kOp : 0);
     static constexpr int kV = kK + kKSt * kOp;
     static constexpr int kBars = kV + kVSt * kOp;
-    static constexpr int kNumBars = 2 * kKSt + 2 * (kVSt > 0 ? kVSt : 1) + 2 + 4 + 1;
+    static constexpr int kBufs = kX ? 2 : 4;               // TMEM buffers (S, X) or S
+    static constexpr int kBufCols = kX ? 256 : 128;
+    static constexpr int kNumBars = 2 * kKSt + 2 * (kVSt > 0 ? kVSt : 1) + 2 + 2 * kBufs + 1;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -227,8 +229,9 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *k_full = bars, *k_empty = bars + kKSt;
     uint64_t *v_full = bars + 2 * kKSt, *v_empty = v_full + kVSt;
     uint64_t *qa_full = v_empty + kVSt, *qa_empty = qa_full + 1;
-    uint64_t *tm_full = qa_empty + 1, *tm_empty = tm_full + 2;
-    uint64_t *mma_done = tm_empty + 2;     // the MMA thread's last MMAs are done (exit)
+    constexpr int kBufs = Ly::kBufs;
+    uint64_t *tm_full = qa_empty + 1, *tm_empty = tm_full + kBufs;
+    uint64_t *mma_done = tm_empty + kBufs;   // the MMA thread's last MMAs are done (exit)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Ly::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
@@ -246,6 +249,10 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         mbar_init(qa_full, 1);
         mbar_init(qa_empty, 1);
         for (int h = 0; h < 2; ++h) {
+            mbar_init(&tm_full[h], 1);
+            mbar_init(&tm_empty[h], kEpiWarps);
+        }
+        for (int h = 2; h < kBufs; ++h) {
             mbar_init(&tm_full[h], 1);
             mbar_init(&tm_empty[h], kEpiWarps);
         }
@@ -382,13 +389,13 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
                     const int s = (int)(tcount % kKSt);
                     const uint32_t par = (uint32_t)((tcount / kKSt) & 1);
-                    const int b = (int)(tcount & 1);          // TMEM buffer of this tile
-                    ok = mbar_wait(&tm_empty[b], (uint32_t)((tcount >> 1) & 1) ^ 1u, abort_flag,
+                    const int b = (int)(tcount % kBufs);      // TMEM buffer of this tile
+                    ok = mbar_wait(&tm_empty[b], (uint32_t)((tcount / kBufs) & 1) ^ 1u, abort_flag,
                                    P.wait_ns) &&
                          mbar_wait(&k_full[s], par, abort_flag, P.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t d_s = tmem + b * 256;
+                    const uint32_t d_s = tmem + b * Ly::kBufCols;
                     const uint32_t d_x = d_s + 128;
                     const uint64_t ka = sdesc_k_sw128(smem_u32(smem + Ly::kK + s * Ly::kOp));
                     mma_ss_c<false>(d_s, ka, qb, idesc);
@@ -476,7 +483,7 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 vq[1] = jf + 8 < U.n ? __ldg(u_v2 + jf + 8) : 0.f;
             }
             for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
-                const int b = (int)(tcount & 1);              // TMEM buffer of this tile
+                const int b = (int)(tcount % kBufs);          // TMEM buffer of this tile
                 // ||v||^2 of the two keys of this tile (loaded a tile ahead)
                 const float q0 = vq[0], q1 = vq[1];
                 if (kX && t + 1 < it.t_end) {
@@ -485,11 +492,11 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                     vq[1] = jn + 8 < U.n ? __ldg(u_v2 + jn + 8) : 0.f;
                 }
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&tm_full[b], (uint32_t)((tcount >> 1) & 1), abort_flag,
+                                mbar_wait(&tm_full[b], (uint32_t)((tcount / kBufs) & 1), abort_flag,
                                           P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t s_col = tmem + lane_addr + b * 256;
+                const uint32_t s_col = tmem + lane_addr + b * Ly::kBufCols;
                 const uint32_t x_col = s_col + 128;
                 float sA[16], xA[16];
                 const float2 v2[2] = {make_float2(q0, q0), make_float2(q1, q1)};

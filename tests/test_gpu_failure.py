@@ -18,16 +18,19 @@ pytestmark = pytest.mark.gpu
 DEFAULT_NS = 2_000_000_000
 
 
+@pytest.mark.parametrize("rule", [0, 2], ids=["dropkv", "attn_sum"])
 @pytest.mark.parametrize("wl", [
     synth.small_variant(synth.LONG_128K, 5003),      # two row chunks per unit
     synth.small_variant(synth.LLAMA8B_32K, 4999),    # one row chunk, alternate tiles
 ], ids=lambda w: w.name)
-def test_expired_waits_report_timeout_and_context_recovers(cuda_lib, wl):
+def test_expired_waits_report_timeout_and_context_recovers(cuda_lib, wl, rule):
+    """Both pass-1 kernels (attention, and row statistics for the attention sum) and
+    both rescoring variants."""
     import torch
     from synth.device import DeviceWorkload
     kv = cuda_lib
     dw = DeviceWorkload(wl)
-    prob = kv.Problem.for_workload(wl)
+    prob = kv.Problem.for_workload(wl, score_rule=rule)
     ws = torch.zeros(kv.kv_score_workspace_size(prob), dtype=torch.uint8, device="cuda")
     scores = torch.zeros((wl.num_layers, wl.num_kv_heads, dw.N_tot), dtype=torch.float32,
                          device="cuda")
@@ -43,7 +46,7 @@ def test_expired_waits_report_timeout_and_context_recovers(cuda_lib, wl):
     assert kv.kv_check_status(ws) == kv.KV_OK
     cu = dw.cu_host
     for (r, l, h) in [(0, 0, 0), (0, wl.num_layers - 1, wl.num_kv_heads - 1)]:
-        _, _, _, S = parity.oracle_unit(wl, dw, r, l, h)
+        _, _, _, S = parity.oracle_unit(wl, dw, r, l, h, rule)
         g = scores[l, h, int(cu[r]):int(cu[r + 1])].cpu().numpy().astype(np.float64)
         big = S >= parity.SCORE_ATOL
         rel = np.abs(g[big] - S[big]) / S[big]
