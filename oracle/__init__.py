@@ -287,3 +287,45 @@ def offsets(budgets: np.ndarray) -> np.ndarray:
 def compact(k: np.ndarray, v: np.ndarray, idx: np.ndarray):
     """Rows of k and v at the kept indices (a plain gather of the bf16 bits)."""
     return k[idx], v[idx]
+
+
+# --------------------------------------------------------------------------
+# per-head budgets (AdaDropKV) and block eviction (BellowsKV)
+# --------------------------------------------------------------------------
+def head_budgets(S_heads: np.ndarray, w: int, sinks: int, b_heads) -> np.ndarray:
+    """Per-head budgets of one (request, layer), int32 [H].
+
+    DropKV page, Key Contributions ("Adaptive head budgets"): DropKV scores with
+    AdaKV's head budget allocation.  Reading: the layer keeps sum(b_heads) tokens;
+    every head keeps its sinks and window, and the remaining slots go to the
+    largest middle-candidate scores [sinks, n - w) over all heads together, equal
+    scores to the lower head, then the lower index.  A head's budget is its sinks
+    + window + the slots it won.
+    """
+    S = np.asarray(S_heads, dtype=np.float64)
+    H, n = S.shape
+    b_heads = [int(b) for b in b_heads]
+    if len(b_heads) != H or any(b < sinks + w or b > n for b in b_heads):
+        raise ValueError("head_budgets: budgets outside [sinks + w, n]")
+    k = sum(b_heads) - H * (sinks + w)
+    mid = np.arange(sinks, n - w)
+    vals = S[:, sinks:n - w].reshape(-1)
+    hh = np.repeat(np.arange(H), mid.size)
+    jj = np.tile(mid, H)
+    order = np.lexsort((jj, hh, -vals))          # score desc, then head, then index
+    counts = np.bincount(hh[order[:k]], minlength=H)
+    return (sinks + w + counts).astype(np.int32)
+
+
+def block_scores(S_block: np.ndarray) -> np.ndarray:
+    """BellowsKV blog, eviction operator: a token's block score is its score summed
+    over all layers and heads of the block.  S_block [layers][heads][n] -> [n]."""
+    S = np.asarray(S_block, dtype=np.float64)
+    return S.reshape(-1, S.shape[-1]).sum(axis=0)
+
+
+def block_budget(n: int, w: int, sinks: int, q: float) -> int:
+    """BellowsKV blog, eviction operator: the first `sinks` and last `w` positions
+    are kept, and the fraction q of the remaining positions with the highest
+    scores survives (rounded down)."""
+    return sinks + w + int(math.floor(q * (n - sinks - w)))

@@ -276,6 +276,69 @@ def test_pool_unit_keeps_window_out_of_the_pool():
 
 
 # --------------------------------------------------------------------------
+# per-head budgets (AdaDropKV) and block eviction (BellowsKV) pins
+# --------------------------------------------------------------------------
+def brute_head_budgets(S, w, sinks, b_heads):
+    """Picks the k layer-wide winners one at a time: the largest remaining middle score,
+    ties to the lower head, then the lower index."""
+    H, n = S.shape
+    k = sum(b_heads) - H * (sinks + w)
+    taken = set()
+    counts = [0] * H
+    for _ in range(k):
+        best = None
+        for h in range(H):
+            for j in range(sinks, n - w):
+                if (h, j) in taken:
+                    continue
+                if best is None or S[h, j] > S[best] or (S[h, j] == S[best] and (h, j) < best):
+                    best = (h, j)
+        taken.add(best)
+        counts[best[0]] += 1
+    return [sinks + w + c for c in counts], taken
+
+
+@pytest.mark.parametrize("H,n,w,sinks,b", [(4, 40, 4, 4, 12), (3, 25, 2, 0, 10), (2, 30, 8, 4, 30),
+                                           (5, 17, 1, 4, 5), (1, 50, 4, 4, 20)])
+def test_head_budgets_match_brute_force(H, n, w, sinks, b):
+    rng = np.random.default_rng(H * 1000 + n)
+    S = rng.integers(0, 5, (H, n)).astype(np.float64)      # many cross-head ties
+    got = oracle.head_budgets(S, w, sinks, [b] * H)
+    ref, taken = brute_head_budgets(S, w, sinks, [b] * H)
+    assert list(got) == ref
+    assert int(got.sum()) == H * b and got.min() >= sinks + w and got.max() <= n
+    # each head's own top-b_h selection is exactly the head's share of the layer winners
+    for h in range(H):
+        sel = set(oracle.select(S[h], w, sinks, int(got[h])).tolist())
+        mid = {j for j in sel if sinks <= j < n - w}
+        assert mid == {j for (hh, j) in taken if hh == h}
+
+
+def test_head_budgets_special_cases():
+    # one head: nothing to redistribute
+    S = np.random.default_rng(1).random((1, 64))
+    assert list(oracle.head_budgets(S, 8, 4, [30])) == [30]
+    # equal scores everywhere: the lower heads win the ties and fill up first
+    S = np.ones((3, 20))
+    assert list(oracle.head_budgets(S, 2, 2, [10, 10, 10])) == [20, 6, 4]
+    # a head whose every candidate beats the others takes all it can
+    S = np.zeros((2, 30))
+    S[1] = 1.0
+    assert list(oracle.head_budgets(S, 4, 4, [12, 12])) == [8, 16]
+    with pytest.raises(ValueError):
+        oracle.head_budgets(S, 4, 4, [7, 12])
+
+
+def test_block_scores_and_budget():
+    rng = np.random.default_rng(3)
+    S = rng.random((2, 3, 50))
+    np.testing.assert_allclose(oracle.block_scores(S), S[0].sum(0) + S[1].sum(0), rtol=1e-15)
+    assert oracle.block_budget(1000, 64, 4, 0.1) == 4 + 64 + 93   # floor(0.1 * 932)
+    assert oracle.block_budget(68, 64, 4, 0.5) == 68
+    assert oracle.block_budget(1000, 64, 4, 1.0) == 1000
+
+
+# --------------------------------------------------------------------------
 # selection pins
 # --------------------------------------------------------------------------
 def brute_select(S, w, sinks, b):
