@@ -10,12 +10,14 @@ Prints one JSON line.  `value` counts unit-tokens (tokens x layers x KV heads,
 each scored, selected and compacted) per second over all ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--score-rule dropkv|squared|attn_sum] [--pool KERNEL]
+                  [--score-rule dropkv|squared|attn_sum] [--pool KERNEL] [--head-budgets]
 
 --score-rule picks what kv_score sums (the DropKV removal score by default;
 its squared form; the SnapKV/PyramidKV attention sum) and --pool adds the
 max pooling of the scores before selection (kernel 11 on the DropKV page, 13
-on the BellowsKV blog); both default to the DropKV step without pooling.
+on the BellowsKV blog); --head-budgets redistributes each layer's budget over
+its heads from the scores (AdaDropKV) before selection.  All default to the
+DropKV step without pooling and with the policy's per-layer budgets.
 
 --impl reference times the fp64 CPU oracle (the only reference arm: the
 pages ship no code) on a bounded sample of the same workload.
@@ -60,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-units", type=int, default=0, help="oracle sample size (0: one per core)")
     ap.add_argument("--score-rule", choices=sorted(SCORE_RULES), default="dropkv")
     ap.add_argument("--pool", type=int, default=1, help="max-pool kernel before selection (1: none)")
+    ap.add_argument("--head-budgets", action="store_true",
+                    help="per-head budgets from the scores before selection")
     return ap.parse_args(argv)
 
 
@@ -246,23 +250,40 @@ def run_reference(args, wl, budgets):
 # ---------------------------------------------------------------------------
 # Kernels of one step and how many launches each makes (the timed region
 # launches only these).
-STAGES = ["attention", "rescore", "pool", "select", "compact"]
+STAGES = ["attention", "rescore", "pool", "heads", "select", "compact"]
 # attention: plan_kernel, attn_tc_kernel, attn_merge_kernel; rescore: plan_kernel,
 # rescore_tc_kernel and, when the window rows span more than one 128-row chunk,
 # chunk_sum_kernel.
-# pool: pool_kernel, only with --pool > 1.
-LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "pool": 1, "select": 1, "compact": 1}
+# pool: pool_kernel, only with --pool > 1; heads: head_budget_kernel, only with
+# --head-budgets.
+LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "pool": 1, "heads": 1, "select": 1,
+                     "compact": 1}
 STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
-                 "pool": "pool_kernel", "select": "select_kernel", "compact": "compact_kernel"}
-# DRAM bytes (read + write) per launch from the single-pass ncu capture of the
-# current kernels on the default workload (profiles/dram_traffic_long_32L_8kv_n131072.md).
-# Only valid for that workload, the DropKV rule without pooling, and these kernel
-# versions; None elsewhere.
-TRAFFIC_WORKLOAD = DEFAULT_WORKLOAD
-TRAFFIC = {"attn_tc_kernel": 17206244864 + 400259840,
-           "rescore_tc_kernel": 17659765504 + 267694336,
-           "select_kernel": 668149504 + 8272640,
-           "compact_kernel": 1731538176 + 1657757952}
+                 "pool": "pool_kernel", "heads": "head_budget_kernel", "select": "select_kernel",
+                 "compact": "compact_kernel"}
+# DRAM bytes (read + write) per launch from single-pass ncu captures of the current
+# kernels (profiles/dram_traffic_long_32L_8kv_n131072.md and
+# profiles/launch_list_attn_sum_pool11_long_32L_8kv_n131072.md), keyed by
+# (workload, score rule, pool kernel); None for any other combination.
+TRAFFIC = {
+    (DEFAULT_WORKLOAD, "dropkv", 1): {
+        "attn_tc_kernel": 17206244864 + 400259840,
+        "rescore_tc_kernel": 17659765504 + 267694336,
+        "select_kernel": 668149504 + 8272640,
+        "compact_kernel": 1731538176 + 1657757952},
+    (DEFAULT_WORKLOAD, "attn_sum", 11): {
+        "attn_stats_kernel": 8607008000 + 4206336,
+        "rescore_tc_kernel": 8636366848 + 266142208,
+        "pool_kernel": 134264320 + 84282624,
+        "select_kernel": 668098816 + 8056320,
+        "compact_kernel": 1731947776 + 1657752576},
+}
+
+
+def stage_kernel(stage, rule):
+    if stage == "attention" and rule == SCORE_RULES["attn_sum"]:
+        return "attn_stats_kernel"
+    return STAGE_KERNELS[stage]
 
 
 def product_budgets(kv, wl):
@@ -283,8 +304,9 @@ def product_budgets(kv, wl):
 
 def bench_config_tag(wl, args):
     tag = {"workload": wl.name}
-    if args.score_rule != "dropkv" or args.pool > 1:
-        tag.update(score_rule=args.score_rule, pool_kernel=args.pool)
+    if args.score_rule != "dropkv" or args.pool > 1 or args.head_budgets:
+        tag.update(score_rule=args.score_rule, pool_kernel=args.pool,
+                   head_budgets=bool(args.head_budgets))
     return tag
 
 
@@ -308,6 +330,8 @@ def stage_roofline(stage, ms, wl, budgets, peaks, rule=0):
         nbytes = kv_pass + q + keys * 4        # ... plus one fp32 score per key
     elif stage == "pool":
         nbytes = keys * 4 * 2                  # every score read and written once
+    elif stage == "heads":
+        nbytes = keys * 4 + units * (4 + 8) * 2   # scores read once; budgets, offsets
     elif stage == "select":
         nbytes = keys * 4 + rows * 4 + 8 * (units + 1) * 2
     else:
@@ -380,10 +404,14 @@ def main(argv=None):
     dw = DeviceWorkload(wl, device=dev)
     rule = SCORE_RULES[args.score_rule]
     pool = args.pool
-    prob = kv.Problem.for_workload(wl, device=dev, score_rule=rule, pool_kernel=pool)
+    heads = args.head_budgets
+    prob = kv.Problem.for_workload(wl, device=dev, score_rule=rule, pool_kernel=pool,
+                                   head_budgets=heads)
     bufs = kv.Buffers(prob, budgets)
     stream = torch.cuda.current_stream(dev)
     ranked = bufs.pooled if pool > 1 else bufs.scores
+    sel_b, sel_o = (bufs.head_budgets, bufs.head_offsets) if heads else (bufs.budgets,
+                                                                         bufs.offsets)
 
     def step(ev=None):
         if ev is not None:
@@ -398,14 +426,18 @@ def main(argv=None):
             kv.kv_pool_scores(prob, pool, bufs.scores, bufs.pooled, stream)
         if ev is not None:
             ev[3].record(stream)
-        kv.kv_select_topk(prob, ranked, bufs.budgets, bufs.offsets, bufs.sel,
-                          bufs.select_ws, stream)
+        if heads:
+            kv.kv_head_budgets(prob, ranked, bufs.budgets, bufs.offsets, bufs.head_budgets,
+                               bufs.head_offsets, bufs.select_ws, stream)
         if ev is not None:
             ev[4].record(stream)
-        kv.kv_compact(prob, dw.k, dw.v, bufs.sel, bufs.offsets, bufs.total_rows, bufs.k_out,
-                      bufs.v_out, stream)
+        kv.kv_select_topk(prob, ranked, sel_b, sel_o, bufs.sel, bufs.select_ws, stream)
         if ev is not None:
             ev[5].record(stream)
+        kv.kv_compact(prob, dw.k, dw.v, bufs.sel, sel_o, bufs.total_rows, bufs.k_out,
+                      bufs.v_out, stream)
+        if ev is not None:
+            ev[6].record(stream)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -445,14 +477,15 @@ def main(argv=None):
     alg_bytes = algorithmic_bytes(wl, budgets)
     hbm_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
 
-    stages = [s for s in STAGES if s != "pool" or pool > 1]
-    if pool <= 1:
-        stage_ms.pop("pool")
+    stages = [s for s in STAGES if (s != "pool" or pool > 1) and (s != "heads" or heads)]
+    for s in list(stage_ms):
+        if s not in stages:
+            stage_ms.pop(s)
     dominant = max(stages, key=lambda s: stage_ms[s])
     roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule)
-    traffic = TRAFFIC.get(STAGE_KERNELS[dominant]) \
-        if wl.name == TRAFFIC_WORKLOAD and rule == 0 and pool <= 1 else None
-    roof.update({"kernel": STAGE_KERNELS[dominant], "peak_source": peak_src,
+    kernel = stage_kernel(dominant, rule)
+    traffic = None if heads else TRAFFIC.get((wl.name, args.score_rule, pool), {}).get(kernel)
+    roof.update({"kernel": kernel, "peak_source": peak_src,
                  "traffic": traffic, "stage_ms": stage_ms[dominant],
                  "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
                                                   rule)["frac"] for s in stages}})
@@ -493,9 +526,11 @@ def main(argv=None):
         line["cpu_baseline"] = {"value": work / dt, "unit": UNIT,
                                 "cores": thr, "kind": "oracle",
                                 "sample": "%d full units (of %d) of the same workload, one "
-                                          "thread each, fp64 score (%s)%s + select + gather"
+                                          "thread each, fp64 score (%s)%s + select + gather%s"
                                           % (n_units, wl.num_units, args.score_rule,
-                                             " + pool %d" % pool if pool > 1 else "")}
+                                             " + pool %d" % pool if pool > 1 else "",
+                                             " (per-head budgets not in the sample: they "
+                                             "need whole layers)" if heads else "")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

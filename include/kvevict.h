@@ -7,6 +7,7 @@
  *                   (or, by kv_problem.score_rule, its squared form or the
  *                   SnapKV/PyramidKV attention sum)
  *   kv_pool_scores  optional 1-D max pooling of the scores before selection
+ *   kv_head_budgets optional per-head budgets from the scores (AdaDropKV)
  *   kv_select_topk  budgeted per-(request, layer, KV head) selection
  *   kv_compact      ragged gather of the kept K/V rows
  *
@@ -164,7 +165,7 @@ kv_status kv_pool_scores(const kv_problem *p, int32_t kernel, const float *score
 kv_status kv_make_offsets(const kv_problem *p, const int32_t *budgets_host,
                           int64_t *offsets_host);
 
-/* Bytes of workspace kv_select_topk needs. */
+/* Bytes of workspace kv_select_topk and kv_head_budgets need. */
 kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes);
 
 /*
@@ -180,6 +181,31 @@ kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes);
 kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
                          const int64_t *offsets_dev, int32_t *sel_idx, void *workspace,
                          size_t workspace_bytes, void *stream);
+
+/*
+ * Per-head budgets from the scores (DropKV page, Key Contributions "Adaptive
+ * head budgets": DropKV scoring combined with AdaKV's head budget allocation).
+ * For every (request, layer), the layer keeps as many tokens as budgets_dev
+ * gives its H heads together; every head keeps its s sinks and w window
+ * tokens, and the remaining slots go to the largest middle-candidate scores
+ * [s, n_r - w) of all H heads together, equal scores to the lower head, then
+ * the lower index.  budgets_out_dev[u] = s + w + the slots head u won;
+ * offsets_out_dev = their exclusive scan (the per-layer totals, and so
+ * offsets_dev[R*L*H], are unchanged).  Then kv_select_topk with the output
+ * budgets keeps exactly the layer-wide winners, and kv_compact uses the output
+ * offsets.
+ * scores: as kv_score (or kv_pool_scores) writes them; budgets_dev, offsets_dev:
+ * device [R*L*H] and [R*L*H + 1] as for kv_select_topk; outputs: device arrays
+ * of the same sizes, distinct from the inputs.  workspace: at least
+ * kv_select_workspace_size bytes (its status word is kv_select_topk's; the rest
+ * is scratch).  A layer whose input budgets are out of range or
+ * disagree with offsets_dev gets them copied through and posts KV_ERR_BUDGET.
+ * H * max n_r must be below 2^32 (KV_ERR_UNSUPPORTED otherwise).
+ */
+kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
+                          const int64_t *offsets_dev, int32_t *budgets_out_dev,
+                          int64_t *offsets_out_dev, void *workspace, size_t workspace_bytes,
+                          void *stream);
 
 /*
  * k_out[offsets[u] + i] = k[row of unit u, token sel_idx[offsets[u] + i]],

@@ -25,7 +25,8 @@ from . import _build
 __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attention",
            "kv_score_rescore", "kv_make_offsets", "kv_select_topk", "kv_compact",
            "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
-           "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores", "EXPORTED_SYMBOLS",
+           "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores", "kv_head_budgets",
+           "EXPORTED_SYMBOLS",
            "evict", "KV_SCORE_DROPKV", "KV_SCORE_DROPKV_SQUARED", "KV_SCORE_ATTN_SUM"]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
@@ -37,7 +38,8 @@ EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_score_rescore", "kv_make_offsets", "kv_select_workspace_size",
                     "kv_select_topk", "kv_compact", "kv_check_status", "kv_status_string",
                     "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc",
-                    "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores")
+                    "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores",
+                    "kv_head_budgets")
 
 
 class KvError(RuntimeError):
@@ -90,6 +92,7 @@ def load(path: Optional[str] = None):
         "kv_budgets_ripple": [i32, i32, ctypes.POINTER(f64), f64, f64, ctypes.POINTER(i32)],
         "kv_score_noalloc": [P, vp, vp, vp, vp, vp],
         "kv_pool_scores": [P, i32, vp, vp, vp],
+        "kv_head_budgets": [P, vp, vp, vp, vp, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -141,6 +144,7 @@ class Problem:
     device: object = "cuda"
     score_rule: int = KV_SCORE_DROPKV   # what kv_score sums (KV_SCORE_*)
     pool_kernel: int = 1                # evict(): max-pool width before selection (1: none)
+    head_budgets: bool = False          # evict(): per-head budgets from the scores (AdaDropKV)
 
     def __post_init__(self):
         import torch
@@ -173,10 +177,10 @@ class Problem:
 
     @classmethod
     def for_workload(cls, wl, device="cuda", score_rule: int = KV_SCORE_DROPKV,
-                     pool_kernel: int = 1) -> "Problem":
+                     pool_kernel: int = 1, head_budgets: bool = False) -> "Problem":
         return cls(wl.seq_lengths(), wl.num_layers, wl.num_kv_heads, wl.num_q_heads,
                    wl.head_dim, wl.window, wl.num_sinks, device=device, score_rule=score_rule,
-                   pool_kernel=pool_kernel)
+                   pool_kernel=pool_kernel, head_budgets=head_budgets)
 
 
 # ---------------------------------------------------------------------------
@@ -221,6 +225,14 @@ def kv_score_noalloc(prob, q, k, v, scores, stream=None):
 def kv_pool_scores(prob, kernel: int, scores_in, scores_out, stream=None):
     _check(load().kv_pool_scores(prob.c, int(kernel), _ptr(scores_in), _ptr(scores_out),
                                  _stream(stream)), "kv_pool_scores")
+
+
+def kv_head_budgets(prob, scores, budgets_dev, offsets_dev, budgets_out, offsets_out, workspace,
+                    stream=None):
+    _check(load().kv_head_budgets(prob.c, _ptr(scores), _ptr(budgets_dev), _ptr(offsets_dev),
+                                  _ptr(budgets_out), _ptr(offsets_out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "kv_head_budgets")
 
 
 def kv_make_offsets(prob, budgets_host: np.ndarray) -> np.ndarray:
@@ -310,17 +322,25 @@ class Buffers:
         self.k_out = torch.empty((max(self.total_rows, 1), d), dtype=torch.bfloat16, device=dev)
         self.v_out = torch.empty_like(self.k_out)
         self.pooled = torch.empty_like(self.scores) if prob.pool_kernel > 1 else None
+        # per-head budgets and their offsets (written on the device by kv_head_budgets)
+        self.head_budgets = torch.empty_like(self.budgets) if prob.head_budgets else None
+        self.head_offsets = torch.empty_like(self.offsets) if prob.head_budgets else None
 
 
 def evict(prob: Problem, q, k, v, bufs: Buffers, stream=None):
-    """Score (and pool, if prob.pool_kernel > 1), select and compact on `stream`;
-    returns (sel_idx, k_out, v_out, offsets)."""
+    """Score (pool, if prob.pool_kernel > 1; per-head budgets, if prob.head_budgets),
+    select and compact on `stream`; returns (sel_idx, k_out, v_out, offsets)."""
     kv_score(prob, q, k, v, bufs.scores, bufs.score_ws, stream)
     ranked = bufs.scores
     if prob.pool_kernel > 1:
         kv_pool_scores(prob, prob.pool_kernel, bufs.scores, bufs.pooled, stream)
         ranked = bufs.pooled
-    kv_select_topk(prob, ranked, bufs.budgets, bufs.offsets, bufs.sel, bufs.select_ws, stream)
-    kv_compact(prob, k, v, bufs.sel, bufs.offsets, bufs.total_rows, bufs.k_out, bufs.v_out, stream)
+    budgets, offsets = bufs.budgets, bufs.offsets
+    if prob.head_budgets:
+        kv_head_budgets(prob, ranked, bufs.budgets, bufs.offsets, bufs.head_budgets,
+                        bufs.head_offsets, bufs.select_ws, stream)
+        budgets, offsets = bufs.head_budgets, bufs.head_offsets
+    kv_select_topk(prob, ranked, budgets, offsets, bufs.sel, bufs.select_ws, stream)
+    kv_compact(prob, k, v, bufs.sel, offsets, bufs.total_rows, bufs.k_out, bufs.v_out, stream)
     n = bufs.total_rows
-    return bufs.sel[:n], bufs.k_out[:n], bufs.v_out[:n], bufs.offsets
+    return bufs.sel[:n], bufs.k_out[:n], bufs.v_out[:n], offsets

@@ -206,7 +206,7 @@ kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes) {
     kv_status st = make_problem(p, &P);
     if (st != KV_OK) return st;
     if (!bytes) return KV_ERR_INVALID_ARG;
-    *bytes = kHeaderBytes;
+    *bytes = kHeaderBytes + head_budget_ws_bytes(P);
     return KV_OK;
 }
 
@@ -223,6 +223,29 @@ kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t
     if (workspace_bytes < kHeaderBytes) return KV_ERR_WORKSPACE;
     return map_cuda(launch_select(P, scores, budgets_dev, offsets_dev, sel_idx,
                                   static_cast<int *>(workspace), (cudaStream_t)stream));
+}
+
+kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
+                          const int64_t *offsets_dev, int32_t *budgets_out_dev,
+                          int64_t *offsets_out_dev, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK || P.units == 0) return st;
+    if (!scores || !budgets_dev || !offsets_dev || !budgets_out_dev || !offsets_out_dev ||
+        !workspace)
+        return KV_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(budgets_dev) || !aligned16(offsets_dev) ||
+        !aligned16(budgets_out_dev) || !aligned16(offsets_out_dev) || !aligned16(workspace))
+        return KV_ERR_INVALID_ARG;
+    if (budgets_out_dev == budgets_dev || offsets_out_dev == offsets_dev) return KV_ERR_INVALID_ARG;
+    if (workspace_bytes < kHeaderBytes + head_budget_ws_bytes(P)) return KV_ERR_WORKSPACE;
+    // the layer-wide counts are 32-bit
+    if ((long long)P.H * P.max_n >= (1LL << 32)) return KV_ERR_UNSUPPORTED;
+    return map_cuda(launch_head_budgets(P, scores, budgets_dev, offsets_dev, budgets_out_dev,
+                                        offsets_out_dev, static_cast<int *>(workspace),
+                                        static_cast<char *>(workspace) + kHeaderBytes,
+                                        (cudaStream_t)stream));
 }
 
 kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const int32_t *sel_idx,

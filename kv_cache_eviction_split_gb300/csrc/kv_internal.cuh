@@ -96,6 +96,12 @@ cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __
                            cudaStream_t s);
 cudaError_t launch_pool(const DevProblem &P, int kernel, const float *in, float *out,
                         cudaStream_t s);
+// Scratch bytes of the per-head budget select (after the status header).
+size_t head_budget_ws_bytes(const DevProblem &P);
+cudaError_t launch_head_budgets(const DevProblem &P, const float *scores, const int32_t *budgets,
+                                const int64_t *offsets, int32_t *budgets_out,
+                                int64_t *offsets_out, int *status, void *scratch,
+                                cudaStream_t s);
 cudaError_t launch_select(const DevProblem &P, const float *scores, const int32_t *budgets,
                           const int64_t *offsets, int32_t *sel, int *status, cudaStream_t s);
 cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __nv_bfloat16 *v,

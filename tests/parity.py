@@ -50,14 +50,16 @@ def product_budgets(kv, wl, profile=None) -> np.ndarray:
 class GpuRun:
     """The three C-ABI calls on one workload, results kept on the device."""
 
-    def __init__(self, kv, wl, budgets=None, dw=None, score_rule=0, pool_kernel=1):
+    def __init__(self, kv, wl, budgets=None, dw=None, score_rule=0, pool_kernel=1,
+                 head_budgets=False):
         import torch
         from synth.device import DeviceWorkload
         self.wl = wl
         self.rule = score_rule
         self.pool = pool_kernel
         self.dw = dw or DeviceWorkload(wl)
-        self.prob = kv.Problem.for_workload(wl, score_rule=score_rule, pool_kernel=pool_kernel)
+        self.prob = kv.Problem.for_workload(wl, score_rule=score_rule, pool_kernel=pool_kernel,
+                                            head_budgets=head_budgets)
         prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
         self.profile = prof
         if budgets is None:
@@ -68,6 +70,18 @@ class GpuRun:
         torch.cuda.synchronize()
         self.status_score = kv.kv_check_status(self.bufs.score_ws)
         self.status_select = kv.kv_check_status(self.bufs.select_ws)
+        # budgets and offsets selection and compaction used (per-head ones if computed)
+        if head_budgets:
+            self.eff_budgets = self.bufs.head_budgets.cpu().numpy().reshape(-1)
+            self.eff_offsets = self.bufs.head_offsets.cpu().numpy()
+        else:
+            self.eff_budgets = np.asarray(budgets).reshape(-1)
+            self.eff_offsets = self.bufs.offsets_host
+
+    def ranked_scores(self):
+        """The scores selection ranked (pooled if pooling ran), float32 [L][H][N]."""
+        b = self.bufs
+        return (b.pooled if b.pooled is not None else b.scores).cpu().numpy()
 
     def unit_results(self, r, l, h):
         wl, b = self.wl, self.bufs
@@ -78,11 +92,11 @@ class GpuRun:
         if b.pooled is not None:
             pooled = b.pooled[l, h, int(cu[r]):int(cu[r + 1])].cpu().numpy()
             scores = (scores, pooled)
-        o0, o1 = int(b.offsets_host[u]), int(b.offsets_host[u + 1])
+        o0, o1 = int(self.eff_offsets[u]), int(self.eff_offsets[u + 1])
         sel = b.sel[o0:o1].cpu().numpy()
         kout = b.k_out[o0:o1].cpu().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
         vout = b.v_out[o0:o1].cpu().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
-        return n, scores, sel, kout, vout, int(self.budgets.reshape(-1)[u])
+        return n, scores, sel, kout, vout, int(self.eff_budgets[u])
 
 
 def oracle_unit(wl, dw, r, l, h, rule=0):

@@ -102,3 +102,74 @@ def test_full_size_rules_sampled_units(cuda_lib, rule, kernel, wl, count):
         assert float(b.scores.max()) <= wl.group * wl.window * (1 + 1e-4)
     del run
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------
+# per-head budgets (AdaDropKV)
+# --------------------------------------------------------------------------
+def _layer_heads(run, r, l, ranked):
+    cu = run.dw.cu_host
+    return ranked[l, :, int(cu[r]):int(cu[r + 1])].astype(np.float64)
+
+
+@pytest.mark.parametrize("rule,kernel", [(0, 1), (ATTN_SUM, 11)], ids=["dropkv", "attn_sum_k11"])
+@pytest.mark.parametrize("wl", SMALL[1:], ids=lambda w: w.name)
+def test_head_budgets_small_workloads(cuda_lib, wl, rule, kernel):
+    run = _run(cuda_lib, wl, score_rule=rule, pool_kernel=kernel, head_budgets=True)
+    ranked = run.ranked_scores()
+    H, w, s = wl.num_kv_heads, wl.window, wl.num_sinks
+    inb = np.asarray(run.budgets).reshape(-1)
+    for r in range(wl.num_requests):
+        for l in range(wl.num_layers):
+            u0 = wl.unit_index(r, l, 0)
+            want = oracle.head_budgets(_layer_heads(run, r, l, ranked), w, s, inb[u0:u0 + H])
+            np.testing.assert_array_equal(run.eff_budgets[u0:u0 + H], want,
+                                          err_msg="head budgets (%d, %d)" % (r, l))
+            assert run.eff_budgets[u0:u0 + H].sum() == inb[u0:u0 + H].sum()
+    np.testing.assert_array_equal(run.eff_offsets, oracle.offsets(run.eff_budgets))
+    parity.check_units(run, list(range(wl.num_units)))
+
+
+def test_head_budgets_against_oracle_scores(cuda_lib):
+    """Layer-wide winners from the GPU scores and from the oracle's scores differ only in
+    tokens within the score tolerance of the oracle's layer threshold."""
+    wl = synth.small_variant(synth.LONG_128K, 5003)
+    run = _run(cuda_lib, wl, head_budgets=True)
+    H, w, s = wl.num_kv_heads, wl.window, wl.num_sinks
+    inb = np.asarray(run.budgets).reshape(-1)
+    ranked = run.ranked_scores()
+    for l in range(wl.num_layers):
+        u0 = wl.unit_index(0, l, 0)
+        So = np.stack([parity.oracle_unit(wl, run.dw, 0, l, h)[3] for h in range(H)])
+        Sg = _layer_heads(run, 0, l, ranked)
+        n = So.shape[1]
+        k = int(inb[u0:u0 + H].sum()) - H * (s + w)
+
+        def winners(S):
+            vals = S[:, s:n - w].reshape(-1)
+            hh = np.repeat(np.arange(H), n - w - s)
+            jj = np.tile(np.arange(s, n - w), H)
+            order = np.lexsort((jj, hh, -vals))[:k]
+            return set(zip(hh[order].tolist(), jj[order].tolist())), vals[order[-1]]
+
+        wo, theta = winners(So)
+        wg, _ = winners(Sg)
+        for (h, j) in wo ^ wg:
+            assert abs(So[h, j] - theta) <= parity.SCORE_RTOL * theta, (l, h, j)
+
+
+def test_head_budgets_bad_input_posts_status(cuda_lib):
+    import torch
+    kv = cuda_lib
+    wl = synth.small_variant(synth.LLAMA8B_32K, 4999)
+    run = _run(kv, wl)
+    b = run.bufs
+    bad = b.budgets.clone()
+    bad[0] = wl.num_sinks + wl.window - 1
+    out_b, out_o = torch.empty_like(b.budgets), torch.empty_like(b.offsets)
+    kv.kv_head_budgets(run.prob, b.scores, bad, b.offsets, out_b, out_o, b.select_ws)
+    assert kv.kv_check_status(b.select_ws) == kv.KV_ERR_BUDGET
+    # the offending layer is copied through; the others are computed
+    H = wl.num_kv_heads
+    np.testing.assert_array_equal(out_b[:H].cpu().numpy(), bad[:H].cpu().numpy())
+    assert int(out_o[-1]) == int(b.offsets[-1])
