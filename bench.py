@@ -11,6 +11,7 @@ each scored, selected and compacted) per second over all ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--score-rule dropkv|squared|attn_sum] [--pool KERNEL] [--head-budgets]
+                  [--block-layers N]
 
 --score-rule picks what kv_score sums (the DropKV removal score by default;
 its squared form; the SnapKV/PyramidKV attention sum) and --pool adds the
@@ -18,6 +19,10 @@ max pooling of the scores before selection (kernel 11 on the DropKV page, 13
 on the BellowsKV blog); --head-budgets redistributes each layer's budget over
 its heads from the scores (AdaDropKV) before selection.  All default to the
 DropKV step without pooling and with the policy's per-layer budgets.
+--block-layers N runs block eviction (BellowsKV): one selection per block of N
+layers from the scores summed over the block, pooled with --pool, keeping the
+sinks, the window and the workload's budget ratio of the rest, then every
+layer and head compacted with its block's tokens.
 
 --impl reference times the fp64 CPU oracle (the only reference arm: the
 pages ship no code) on a bounded sample of the same workload.
@@ -64,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--pool", type=int, default=1, help="max-pool kernel before selection (1: none)")
     ap.add_argument("--head-budgets", action="store_true",
                     help="per-head budgets from the scores before selection")
+    ap.add_argument("--block-layers", type=int, default=0,
+                    help="block eviction over blocks of this many layers (0: off)")
     return ap.parse_args(argv)
 
 
@@ -250,17 +257,19 @@ def run_reference(args, wl, budgets):
 # ---------------------------------------------------------------------------
 # Kernels of one step and how many launches each makes (the timed region
 # launches only these).
-STAGES = ["attention", "rescore", "pool", "heads", "select", "compact"]
+STAGES = ["attention", "rescore", "blocks", "pool", "heads", "select", "compact"]
 # attention: plan_kernel, attn_tc_kernel, attn_merge_kernel; rescore: plan_kernel,
 # rescore_tc_kernel and, when the window rows span more than one 128-row chunk,
 # chunk_sum_kernel.
 # pool: pool_kernel, only with --pool > 1; heads: head_budget_kernel, only with
 # --head-budgets.
-LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "pool": 1, "heads": 1, "select": 1,
-                     "compact": 1}
+# heads launches a memset and six kernels; blocks (block_sum_kernel) only with
+# --block-layers.
+LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "blocks": 1, "pool": 1, "heads": 6,
+                     "select": 1, "compact": 1}
 STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
-                 "pool": "pool_kernel", "heads": "head_budget_kernel", "select": "select_kernel",
-                 "compact": "compact_kernel"}
+                 "blocks": "block_sum_kernel", "pool": "pool_kernel", "heads": "hb_hist_kernel",
+                 "select": "select_kernel", "compact": "compact_kernel"}
 # DRAM bytes (read + write) per launch from single-pass ncu captures of the current
 # kernels (profiles/dram_traffic_long_32L_8kv_n131072.md and
 # profiles/launch_list_attn_sum_pool11_long_32L_8kv_n131072.md), keyed by
@@ -304,13 +313,15 @@ def product_budgets(kv, wl):
 
 def bench_config_tag(wl, args):
     tag = {"workload": wl.name}
-    if args.score_rule != "dropkv" or args.pool > 1 or args.head_budgets:
+    if args.score_rule != "dropkv" or args.pool > 1 or args.head_budgets or args.block_layers:
         tag.update(score_rule=args.score_rule, pool_kernel=args.pool,
                    head_budgets=bool(args.head_budgets))
+    if args.block_layers:
+        tag.update(block_layers=args.block_layers, keep_fraction=wl.budget_ratio)
     return tag
 
 
-def stage_roofline(stage, ms, wl, budgets, peaks, rule=0):
+def stage_roofline(stage, ms, wl, budgets, peaks, rule=0, blk=1):
     """Roofline of one stage's kernel from its algorithmic bytes (and, for the two
     scoring passes, their algorithmic tensor flops: two d-long dot products per
     (window row, visible key) pair each, one for the attention sum, which needs
@@ -320,6 +331,10 @@ def stage_roofline(stage, ms, wl, budgets, peaks, rule=0):
     n_tot = sum(wl.seq_lengths())
     L, H = wl.num_layers, wl.num_kv_heads
     rows = int(np.asarray(budgets).sum())
+    if stage in ("pool", "select") and blk > 1:
+        keys_div = H * blk                     # block problem: one score row per block
+    else:
+        keys_div = 1
     kv = kv_cache_bytes(L, H, d, n_tot)
     q = wl.num_requests * L * wl.num_q_heads * wl.window * d * 2
     keys = n_tot * L * H
@@ -329,11 +344,14 @@ def stage_roofline(stage, ms, wl, budgets, peaks, rule=0):
     elif stage == "rescore":
         nbytes = kv_pass + q + keys * 4        # ... plus one fp32 score per key
     elif stage == "pool":
-        nbytes = keys * 4 * 2                  # every score read and written once
+        nbytes = keys // keys_div * 4 * 2      # every score read and written once
     elif stage == "heads":
         nbytes = keys * 4 + units * (4 + 8) * 2   # scores read once; budgets, offsets
+    elif stage == "blocks":
+        nbytes = keys * 4 + keys * 4 // (H * blk)  # scores read once, block scores written
     elif stage == "select":
-        nbytes = keys * 4 + rows * 4 + 8 * (units + 1) * 2
+        nbytes = keys // keys_div * 4 + rows // (H * blk if blk > 1 else 1) * 4 + \
+            8 * (units // (H * blk if blk > 1 else 1) + 1) * 2
     else:
         nbytes = rows * (2 * d * 2) * 2 + rows * 4 + 8 * (units + 1)
     achieved = nbytes / (ms * 1e-3) / 1e9
@@ -405,11 +423,21 @@ def main(argv=None):
     rule = SCORE_RULES[args.score_rule]
     pool = args.pool
     heads = args.head_budgets
+    blk = args.block_layers
+    if blk and heads:
+        raise SystemExit("--block-layers and --head-budgets do not combine")
     prob = kv.Problem.for_workload(wl, device=dev, score_rule=rule, pool_kernel=pool,
                                    head_budgets=heads)
     bufs = kv.Buffers(prob, budgets)
     stream = torch.cuda.current_stream(dev)
     ranked = bufs.pooled if pool > 1 else bufs.scores
+    bb = None
+    if blk:
+        bb = kv.BlockBuffers(prob, blk, wl.budget_ratio, pool_kernel=pool)
+        ranked = bb.pooled if pool > 1 else bb.block_scores
+        # rows kept per unit: every unit keeps its block's budget
+        budgets = np.repeat(np.repeat(bb.block_budgets_host.reshape(wl.num_requests, -1), blk,
+                                      axis=1)[:, :, None], wl.num_kv_heads, axis=2)
     sel_b, sel_o = (bufs.head_budgets, bufs.head_offsets) if heads else (bufs.budgets,
                                                                          bufs.offsets)
 
@@ -422,22 +450,36 @@ def main(argv=None):
         kv.kv_score_rescore(prob, dw.q, dw.k, dw.v, bufs.scores, bufs.score_ws, stream)
         if ev is not None:
             ev[2].record(stream)
-        if pool > 1:
-            kv.kv_pool_scores(prob, pool, bufs.scores, bufs.pooled, stream)
+        if blk:
+            kv.kv_block_scores(prob, blk, bufs.scores, bb.block_scores, stream)
         if ev is not None:
             ev[3].record(stream)
+        if pool > 1 and blk:
+            kv.kv_pool_scores(bb.bprob, pool, bb.block_scores, bb.pooled, stream)
+        elif pool > 1:
+            kv.kv_pool_scores(prob, pool, bufs.scores, bufs.pooled, stream)
+        if ev is not None:
+            ev[4].record(stream)
         if heads:
             kv.kv_head_budgets(prob, ranked, bufs.budgets, bufs.offsets, bufs.head_budgets,
                                bufs.head_offsets, bufs.select_ws, stream)
         if ev is not None:
-            ev[4].record(stream)
-        kv.kv_select_topk(prob, ranked, sel_b, sel_o, bufs.sel, bufs.select_ws, stream)
-        if ev is not None:
             ev[5].record(stream)
-        kv.kv_compact(prob, dw.k, dw.v, bufs.sel, sel_o, bufs.total_rows, bufs.k_out,
-                      bufs.v_out, stream)
+        if blk:
+            kv.kv_select_topk(bb.bprob, ranked, bb.block_budgets, bb.block_offsets, bb.sel,
+                              bb.select_ws, stream)
+        else:
+            kv.kv_select_topk(prob, ranked, sel_b, sel_o, bufs.sel, bufs.select_ws, stream)
         if ev is not None:
             ev[6].record(stream)
+        if blk:
+            kv.kv_compact_blocks(prob, blk, dw.k, dw.v, bb.sel, bb.block_offsets,
+                                 bb.unit_offsets, bb.total_rows, bb.k_out, bb.v_out, stream)
+        else:
+            kv.kv_compact(prob, dw.k, dw.v, bufs.sel, sel_o, bufs.total_rows, bufs.k_out,
+                          bufs.v_out, stream)
+        if ev is not None:
+            ev[7].record(stream)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -465,7 +507,8 @@ def main(argv=None):
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, dist, dev)
-    st = (kv.kv_check_status(bufs.score_ws, stream), kv.kv_check_status(bufs.select_ws, stream))
+    st = (kv.kv_check_status(bufs.score_ws, stream),
+          kv.kv_check_status(bb.select_ws if blk else bufs.select_ws, stream))
     if st != (0, 0):
         raise SystemExit("device status after the timed region: %s" % (st,))
     stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
@@ -477,18 +520,20 @@ def main(argv=None):
     alg_bytes = algorithmic_bytes(wl, budgets)
     hbm_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
 
-    stages = [s for s in STAGES if (s != "pool" or pool > 1) and (s != "heads" or heads)]
+    stages = [s for s in STAGES if (s != "pool" or pool > 1) and (s != "heads" or heads)
+              and (s != "blocks" or blk)]
     for s in list(stage_ms):
         if s not in stages:
             stage_ms.pop(s)
     dominant = max(stages, key=lambda s: stage_ms[s])
-    roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule)
+    roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule, blk)
     kernel = stage_kernel(dominant, rule)
-    traffic = None if heads else TRAFFIC.get((wl.name, args.score_rule, pool), {}).get(kernel)
+    traffic = None if heads or blk else \
+        TRAFFIC.get((wl.name, args.score_rule, pool), {}).get(kernel)
     roof.update({"kernel": kernel, "peak_source": peak_src,
                  "traffic": traffic, "stage_ms": stage_ms[dominant],
                  "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
-                                                  rule)["frac"] for s in stages}})
+                                                  rule, blk)["frac"] for s in stages}})
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -514,7 +559,8 @@ def main(argv=None):
             "clocks": clocks}
 
     if not args.no_e2e:
-        line["e2e"] = e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens * world)
+        line["e2e"] = e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens * world,
+                                  bb)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         prof = synth.ripple_profile(wl) if wl.budget_policy == "ripple" else None
@@ -529,8 +575,9 @@ def main(argv=None):
                                           "thread each, fp64 score (%s)%s + select + gather%s"
                                           % (n_units, wl.num_units, args.score_rule,
                                              " + pool %d" % pool if pool > 1 else "",
-                                             " (per-head budgets not in the sample: they "
-                                             "need whole layers)" if heads else "")}
+                                             " (per-head budgets and block selection are not "
+                                             "in the sample: they need whole layers)"
+                                             if heads or blk else "")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -538,7 +585,7 @@ def main(argv=None):
     return 0
 
 
-def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens):
+def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=None):
     """Same metric through the public API with host buffers: pinned host Q/K/V
     copied in, the three calls, the kept indices and packed K/V copied out."""
     try:
@@ -548,8 +595,9 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens):
         qh.copy_(dw.q)
         kh.copy_(dw.k)
         vh.copy_(dw.v)
-        rows = bufs.total_rows
-        selh = torch.empty(rows, dtype=torch.int32, pin_memory=True)
+        rows = bb.total_rows if bb is not None else bufs.total_rows
+        selh = torch.empty(int(bb.block_offsets_host[-1]) if bb is not None else rows,
+                           dtype=torch.int32, pin_memory=True)
         koh = torch.empty((rows, wl.head_dim), dtype=torch.bfloat16, pin_memory=True)
         voh = torch.empty_like(koh, pin_memory=True)
     except RuntimeError as e:
@@ -559,7 +607,11 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens):
         dw.q.copy_(qh, non_blocking=True)
         dw.k.copy_(kh, non_blocking=True)
         dw.v.copy_(vh, non_blocking=True)
-        sel, ko, vo, _ = kv.evict(prob, dw.q, dw.k, dw.v, bufs, stream)
+        if bb is None:
+            sel, ko, vo, _ = kv.evict(prob, dw.q, dw.k, dw.v, bufs, stream)
+        else:
+            kv.kv_score(prob, dw.q, dw.k, dw.v, bufs.scores, bufs.score_ws, stream)
+            sel, ko, vo, _ = kv.evict_blocks(prob, bufs.scores, dw.k, dw.v, bb, stream)
         selh.copy_(sel, non_blocking=True)
         koh.copy_(ko, non_blocking=True)
         voh.copy_(vo, non_blocking=True)

@@ -8,6 +8,7 @@
  *                   SnapKV/PyramidKV attention sum)
  *   kv_pool_scores  optional 1-D max pooling of the scores before selection
  *   kv_head_budgets optional per-head budgets from the scores (AdaDropKV)
+ *   kv_block_scores, kv_compact_blocks  block eviction (BellowsKV)
  *   kv_select_topk  budgeted per-(request, layer, KV head) selection
  *   kv_compact      ragged gather of the kept K/V rows
  *
@@ -208,6 +209,39 @@ kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_
                           void *stream);
 
 /*
+ * Block eviction (BellowsKV blog, eviction operator): one eviction decision
+ * per block of `block_layers` consecutive layers, made from scores summed over
+ * all layers and heads of the block, then applied to every layer and head of
+ * the block.  The block view of a problem is the kv_problem with num_layers =
+ * L / block_layers, num_kv_heads = num_q_heads = 1 and the same requests,
+ * window and sinks; kv_pool_scores (13 in the blog), kv_budgets_fraction,
+ * kv_make_offsets and kv_select_topk run on it unchanged.
+ *
+ * kv_block_scores: block_scores[b][t] = sum over the block's layers l (in
+ * order) and heads h (in order) of scores[l][h][t], fp32, for every packed
+ * token t.  scores: device f32 [L][H][N_tot]; block_scores: device f32
+ * [L / block_layers][N_tot].  L must be a multiple of block_layers
+ * (KV_ERR_INVALID_ARG otherwise).
+ */
+kv_status kv_block_scores(const kv_problem *p, int32_t block_layers, const float *scores,
+                          float *block_scores, void *stream);
+
+/*
+ * Block form of kv_compact: unit u = (r, l, h) of p copies row i of its output
+ * (offsets_dev[u] + i) from token block_sel_idx[block_offsets_dev[ub] + i],
+ * ub = r * (L / block_layers) + l / block_layers, i.e. every layer and head of
+ * a block keeps the tokens its block selected.  block_sel_idx /
+ * block_offsets_dev: the selection and offsets of the block view;
+ * offsets_dev: exclusive scan over p's units of the budgets, each unit's
+ * budget being its block's.  Rows past the block's list, and out-of-range
+ * indices, are skipped and left untouched.
+ */
+kv_status kv_compact_blocks(const kv_problem *p, int32_t block_layers, const void *k,
+                            const void *v, const int32_t *block_sel_idx,
+                            const int64_t *block_offsets_dev, const int64_t *offsets_dev,
+                            int64_t total_rows, void *k_out, void *v_out, void *stream);
+
+/*
  * k_out[offsets[u] + i] = k[row of unit u, token sel_idx[offsets[u] + i]],
  * the same for v: a bit copy of the kept rows into one packed ragged cache.
  * total_rows = offsets[R*L*H] (the caller knows it from kv_make_offsets).
@@ -285,6 +319,14 @@ kv_status kv_budgets_pyramid(int32_t num_layers, int32_t mean_budget, double hi,
                              double curve, int32_t *budgets_out);
 kv_status kv_budgets_ripple(int32_t num_layers, int32_t mean_budget, const double *profile,
                             double beta, double gamma, int32_t *budgets_out);
+
+/*
+ * Host helper: budgets_host[u] = s + w + floor(q * (n_r - s - w)) for every
+ * unit of p: the sinks and window kept and the fraction q (in [0, 1]) of the
+ * rest (BellowsKV blog, eviction operator: the fraction q of the remaining
+ * positions survives).  budgets_host: host [R*L*H].
+ */
+kv_status kv_budgets_fraction(const kv_problem *p, double q, int32_t *budgets_host);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,8 @@ __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attentio
            "kv_score_rescore", "kv_make_offsets", "kv_select_topk", "kv_compact",
            "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
            "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores", "kv_head_budgets",
-           "EXPORTED_SYMBOLS",
+           "kv_block_scores", "kv_compact_blocks", "kv_budgets_fraction", "BlockBuffers",
+           "evict_blocks", "EXPORTED_SYMBOLS",
            "evict", "KV_SCORE_DROPKV", "KV_SCORE_DROPKV_SQUARED", "KV_SCORE_ATTN_SUM"]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
@@ -39,7 +40,8 @@ EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_select_topk", "kv_compact", "kv_check_status", "kv_status_string",
                     "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc",
                     "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores",
-                    "kv_head_budgets")
+                    "kv_head_budgets", "kv_block_scores", "kv_compact_blocks",
+                    "kv_budgets_fraction")
 
 
 class KvError(RuntimeError):
@@ -93,6 +95,9 @@ def load(path: Optional[str] = None):
         "kv_score_noalloc": [P, vp, vp, vp, vp, vp],
         "kv_pool_scores": [P, i32, vp, vp, vp],
         "kv_head_budgets": [P, vp, vp, vp, vp, vp, vp, sz, vp],
+        "kv_block_scores": [P, i32, vp, vp, vp],
+        "kv_compact_blocks": [P, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp],
+        "kv_budgets_fraction": [P, f64, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -175,6 +180,14 @@ class Problem:
     def total_tokens(self) -> int:
         return int(self.cu_host[-1])
 
+    def block_view(self, block_layers: int) -> "Problem":
+        """The problem whose units are (request, block of `block_layers` layers): one KV
+        head and one query head per block, same requests, window and sinks."""
+        if block_layers < 1 or self.num_layers % block_layers:
+            raise ValueError("num_layers must be a multiple of block_layers")
+        return Problem(list(self.lengths), self.num_layers // block_layers, 1, 1, self.head_dim,
+                       self.window, self.num_sinks, self.softmax_scale, self.cu_dev.device)
+
     @classmethod
     def for_workload(cls, wl, device="cuda", score_rule: int = KV_SCORE_DROPKV,
                      pool_kernel: int = 1, head_budgets: bool = False) -> "Problem":
@@ -233,6 +246,27 @@ def kv_head_budgets(prob, scores, budgets_dev, offsets_dev, budgets_out, offsets
                                   _ptr(budgets_out), _ptr(offsets_out), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "kv_head_budgets")
+
+
+def kv_block_scores(prob, block_layers: int, scores, block_scores, stream=None):
+    _check(load().kv_block_scores(prob.c, int(block_layers), _ptr(scores), _ptr(block_scores),
+                                  _stream(stream)), "kv_block_scores")
+
+
+def kv_compact_blocks(prob, block_layers: int, k, v, block_sel, block_offsets, offsets,
+                      total_rows: int, k_out, v_out, stream=None):
+    _check(load().kv_compact_blocks(prob.c, int(block_layers), _ptr(k), _ptr(v), _ptr(block_sel),
+                                    _ptr(block_offsets), _ptr(offsets), int(total_rows),
+                                    _ptr(k_out), _ptr(v_out), _stream(stream)),
+           "kv_compact_blocks")
+
+
+def kv_budgets_fraction(prob, q: float) -> np.ndarray:
+    out = np.zeros(prob.num_units, dtype=np.int32)
+    _check(load().kv_budgets_fraction(prob.c, float(q),
+                                      out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+           "kv_budgets_fraction")
+    return out
 
 
 def kv_make_offsets(prob, budgets_host: np.ndarray) -> np.ndarray:
@@ -344,3 +378,57 @@ def evict(prob: Problem, q, k, v, bufs: Buffers, stream=None):
     kv_compact(prob, k, v, bufs.sel, offsets, bufs.total_rows, bufs.k_out, bufs.v_out, stream)
     n = bufs.total_rows
     return bufs.sel[:n], bufs.k_out[:n], bufs.v_out[:n], offsets
+
+
+# ---------------------------------------------------------------------------
+# block eviction (BellowsKV): one decision per block of consecutive layers
+# ---------------------------------------------------------------------------
+class BlockBuffers:
+    """Buffers of block eviction for `prob`: blocks of `block_layers` layers, each keeping
+    its sinks, window and the fraction `q` of the rest, pooled with `pool_kernel`."""
+
+    def __init__(self, prob: Problem, block_layers: int, q: float, pool_kernel: int = 13):
+        import torch
+        dev = prob.cu_dev.device
+        self.block_layers = block_layers
+        self.pool_kernel = pool_kernel
+        self.bprob = prob.block_view(block_layers)
+        nblk = self.bprob.num_layers
+        N = prob.total_tokens
+        self.block_budgets_host = kv_budgets_fraction(self.bprob, q)
+        self.block_offsets_host = kv_make_offsets(self.bprob, self.block_budgets_host)
+        # every (layer, head) of a block keeps its block's tokens
+        per_unit = np.repeat(self.block_budgets_host.reshape(prob.num_requests, nblk),
+                             block_layers, axis=1)
+        per_unit = np.repeat(per_unit[:, :, None], prob.num_kv_heads, axis=2).reshape(-1)
+        self.unit_offsets_host = kv_make_offsets(prob, per_unit)
+        self.total_rows = int(self.unit_offsets_host[-1])
+        self.block_budgets = torch.from_numpy(self.block_budgets_host).to(dev)
+        self.block_offsets = torch.from_numpy(self.block_offsets_host).to(dev)
+        self.unit_offsets = torch.from_numpy(self.unit_offsets_host).to(dev)
+        self.block_scores = torch.empty((nblk, 1, N), dtype=torch.float32, device=dev)
+        self.pooled = torch.empty_like(self.block_scores) if pool_kernel > 1 else None
+        self.select_ws = torch.zeros(max(kv_select_workspace_size(self.bprob), 256),
+                                     dtype=torch.uint8, device=dev)
+        self.sel = torch.empty(max(int(self.block_offsets_host[-1]), 1), dtype=torch.int32,
+                               device=dev)
+        self.k_out = torch.empty((max(self.total_rows, 1), prob.head_dim), dtype=torch.bfloat16,
+                                 device=dev)
+        self.v_out = torch.empty_like(self.k_out)
+
+
+def evict_blocks(prob, scores, k, v, bb: BlockBuffers, stream=None):
+    """Block eviction from per-(layer, head) scores already computed by kv_score:
+    block sums, pooling, one selection per (request, block), and the compaction of every
+    layer and head with its block's tokens.  Returns (block_sel, k_out, v_out, offsets)."""
+    kv_block_scores(prob, bb.block_layers, scores, bb.block_scores, stream)
+    ranked = bb.block_scores
+    if bb.pool_kernel > 1:
+        kv_pool_scores(bb.bprob, bb.pool_kernel, bb.block_scores, bb.pooled, stream)
+        ranked = bb.pooled
+    kv_select_topk(bb.bprob, ranked, bb.block_budgets, bb.block_offsets, bb.sel, bb.select_ws,
+                   stream)
+    kv_compact_blocks(prob, bb.block_layers, k, v, bb.sel, bb.block_offsets, bb.unit_offsets,
+                      bb.total_rows, bb.k_out, bb.v_out, stream)
+    n = bb.total_rows
+    return bb.sel[:int(bb.block_offsets_host[-1])], bb.k_out[:n], bb.v_out[:n], bb.unit_offsets

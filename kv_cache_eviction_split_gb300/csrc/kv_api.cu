@@ -248,6 +248,40 @@ kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_
                                         (cudaStream_t)stream));
 }
 
+kv_status kv_block_scores(const kv_problem *p, int32_t block_layers, const float *scores,
+                          float *block_scores, void *stream) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK) return st;
+    if (block_layers < 1 || P.L % block_layers != 0) return KV_ERR_INVALID_ARG;
+    if (P.units == 0) return KV_OK;
+    if (!scores || !block_scores || !aligned16(scores) || !aligned16(block_scores))
+        return KV_ERR_INVALID_ARG;
+    return map_cuda(launch_block_sum(P, block_layers, scores, block_scores, (cudaStream_t)stream));
+}
+
+kv_status kv_compact_blocks(const kv_problem *p, int32_t block_layers, const void *k,
+                            const void *v, const int32_t *block_sel_idx,
+                            const int64_t *block_offsets_dev, const int64_t *offsets_dev,
+                            int64_t total_rows, void *k_out, void *v_out, void *stream) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK || P.units == 0) return st;
+    if (block_layers < 1 || P.L % block_layers != 0 || total_rows < 0) return KV_ERR_INVALID_ARG;
+    if (total_rows == 0) return KV_OK;
+    if (!k || !v || !block_sel_idx || !block_offsets_dev || !offsets_dev || !k_out || !v_out)
+        return KV_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(block_sel_idx) ||
+        !aligned16(block_offsets_dev) || !aligned16(offsets_dev) || !aligned16(k_out) ||
+        !aligned16(v_out))
+        return KV_ERR_INVALID_ARG;
+    return map_cuda(launch_compact_blocks(P, block_layers, (const __nv_bfloat16 *)k,
+                                          (const __nv_bfloat16 *)v, block_sel_idx,
+                                          block_offsets_dev, offsets_dev, total_rows,
+                                          (__nv_bfloat16 *)k_out, (__nv_bfloat16 *)v_out,
+                                          (cudaStream_t)stream));
+}
+
 kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const int32_t *sel_idx,
                      const int64_t *offsets_dev, int64_t total_rows, void *k_out, void *v_out,
                      void *stream) {
@@ -324,6 +358,21 @@ kv_status kv_budgets_pyramid(int32_t num_layers, int32_t mean_budget, double hi,
         for (int l = 0; l < L; ++l) m[l] = m[l] / mean;
     }
     return largest_remainder(L, mean_budget, m, budgets_out);
+}
+
+kv_status kv_budgets_fraction(const kv_problem *p, double q, int32_t *budgets_host) {
+    DevProblem P;
+    kv_status st = make_problem(p, &P);
+    if (st != KV_OK) return st;
+    if (!(q >= 0.0 && q <= 1.0)) return KV_ERR_INVALID_ARG;
+    if (P.units > 0 && !budgets_host) return KV_ERR_INVALID_ARG;
+    for (long long u = 0; u < P.units; ++u) {
+        const int r = (int)(u / ((long long)P.L * P.H));
+        const long long n = p->seq_offsets_host[r + 1] - p->seq_offsets_host[r];
+        const long long rest = n - P.sinks - P.w;
+        budgets_host[u] = (int32_t)(P.sinks + P.w + (long long)std::floor(q * (double)rest));
+    }
+    return KV_OK;
 }
 
 kv_status kv_budgets_ripple(int32_t num_layers, int32_t mean_budget, const double *profile,

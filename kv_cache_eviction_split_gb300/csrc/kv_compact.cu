@@ -7,6 +7,11 @@
 // the offsets table between the units of its first and last rows; a warp moves one
 // row pair (K and V) per step in 16-byte vectors, four rows in flight, with
 // read-only loads and streaming stores (the copy is touched once).
+//
+// Block form (BellowsKV blog, eviction operator: one decision per block of
+// consecutive layers): unit (r, l, h) takes its indices from the selection of
+// block unit (r, l / block_layers), row i of the unit reading index i of the
+// block's list.
 #include "kv_internal.cuh"
 
 namespace kvevict {
@@ -30,11 +35,20 @@ __device__ __forceinline__ void st_cs(uint4 *p, const uint4 &v) {
                  : "memory");
 }
 
+// Where a unit's indices come from in the block form.
+struct BlockSel {
+    const int32_t *sel;        // indices of the block units
+    const int64_t *offsets;    // [R * nblk + 1] offsets of the block units
+    int block_layers;          // 0: the plain form
+    int nblk;                  // L / block_layers
+};
+
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32)
 compact_kernel(DevProblem P, const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                const int32_t *__restrict__ sel, const int64_t *__restrict__ offsets,
-               long long total_rows, uint4 *__restrict__ kout, uint4 *__restrict__ vout) {
+               long long total_rows, uint4 *__restrict__ kout, uint4 *__restrict__ vout,
+               const BlockSel B) {
     constexpr int CPR = D / 8;                    // 16-byte chunks per row
     constexpr int LANES = 2 * CPR;                // K chunks then V chunks
     constexpr int ROWS_PER_PASS = 32 / LANES;     // rows one warp covers per step
@@ -76,7 +90,14 @@ compact_kernel(DevProblem P, const uint4 *__restrict__ k, const uint4 *__restric
             if (r < nrows) {
                 const UnitInfo U = unit_info(P, s_unit[r], P.cu);
                 const long long row = row0 + r;
-                const int tok = sel[row];
+                int tok = -1;
+                if (B.block_layers == 0) {
+                    tok = sel[row];
+                } else {
+                    const long long ub = (long long)U.r * B.nblk + U.l / B.block_layers;
+                    const long long i = row - offsets[s_unit[r]];
+                    if (i < B.offsets[ub + 1] - B.offsets[ub]) tok = B.sel[B.offsets[ub] + i];
+                }
                 if (tok >= 0 && tok < U.n) {
                     buf[q] = ld_nc(src_base + (U.kv_row0 + tok) * CPR + ch);
                     dst[q] = row * CPR + ch;
@@ -90,11 +111,11 @@ compact_kernel(DevProblem P, const uint4 *__restrict__ k, const uint4 *__restric
     }
 }
 
-}  // namespace
-
-cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
-                           const int32_t *sel, const int64_t *offsets, long long total_rows,
-                           __nv_bfloat16 *kout, __nv_bfloat16 *vout, cudaStream_t s) {
+cudaError_t launch_compact_any(const DevProblem &P, const __nv_bfloat16 *k,
+                               const __nv_bfloat16 *v, const int32_t *sel,
+                               const int64_t *offsets, long long total_rows,
+                               __nv_bfloat16 *kout, __nv_bfloat16 *vout, const BlockSel &B,
+                               cudaStream_t s) {
     const long long blocks = (total_rows + kRowsPerCta - 1) / kRowsPerCta;
     if (blocks <= 0) return cudaSuccess;
     auto kk = reinterpret_cast<const uint4 *>(k);
@@ -103,11 +124,30 @@ cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __
     auto vo = reinterpret_cast<uint4 *>(vout);
     if (P.d == 64)
         compact_kernel<64><<<(unsigned)blocks, kWarps * 32, 0, s>>>(P, kk, vv, sel, offsets,
-                                                                    total_rows, ko, vo);
+                                                                    total_rows, ko, vo, B);
     else
         compact_kernel<128><<<(unsigned)blocks, kWarps * 32, 0, s>>>(P, kk, vv, sel, offsets,
-                                                                     total_rows, ko, vo);
+                                                                     total_rows, ko, vo, B);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                           const int32_t *sel, const int64_t *offsets, long long total_rows,
+                           __nv_bfloat16 *kout, __nv_bfloat16 *vout, cudaStream_t s) {
+    return launch_compact_any(P, k, v, sel, offsets, total_rows, kout, vout,
+                              BlockSel{nullptr, nullptr, 0, 0}, s);
+}
+
+cudaError_t launch_compact_blocks(const DevProblem &P, int block_layers, const __nv_bfloat16 *k,
+                                  const __nv_bfloat16 *v, const int32_t *block_sel,
+                                  const int64_t *block_offsets, const int64_t *offsets,
+                                  long long total_rows, __nv_bfloat16 *kout,
+                                  __nv_bfloat16 *vout, cudaStream_t s) {
+    return launch_compact_any(P, k, v, nullptr, offsets, total_rows, kout, vout,
+                              BlockSel{block_sel, block_offsets, block_layers,
+                                       P.L / block_layers}, s);
 }
 
 }  // namespace kvevict

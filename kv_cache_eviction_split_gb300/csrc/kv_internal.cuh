@@ -96,6 +96,13 @@ cudaError_t launch_rescore(const DevProblem &P, const __nv_bfloat16 *q, const __
                            cudaStream_t s);
 cudaError_t launch_pool(const DevProblem &P, int kernel, const float *in, float *out,
                         cudaStream_t s);
+cudaError_t launch_block_sum(const DevProblem &P, int block_layers, const float *scores,
+                             float *out, cudaStream_t s);
+cudaError_t launch_compact_blocks(const DevProblem &P, int block_layers, const __nv_bfloat16 *k,
+                                  const __nv_bfloat16 *v, const int32_t *block_sel,
+                                  const int64_t *block_offsets, const int64_t *offsets,
+                                  long long total_rows, __nv_bfloat16 *kout,
+                                  __nv_bfloat16 *vout, cudaStream_t s);
 // Scratch bytes of the per-head budget select (after the status header).
 size_t head_budget_ws_bytes(const DevProblem &P);
 cudaError_t launch_head_budgets(const DevProblem &P, const float *scores, const int32_t *budgets,

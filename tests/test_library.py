@@ -136,3 +136,24 @@ def test_score_rule_and_pool_argument_checks(kv):
     assert lib.kv_pool_scores(p.c, 11, a + nbytes - 16, a, None) == kv.KV_ERR_INVALID_ARG
     empty = _prob(kv, lengths=[])
     assert lib.kv_pool_scores(empty.c, 11, None, None, None) == kv.KV_OK
+
+
+def test_block_helpers_host_side(kv):
+    lib = kv.load()
+    p = _prob(kv, num_layers=4)
+    bp = p.block_view(2)
+    assert (bp.num_layers, bp.num_kv_heads, bp.num_q_heads) == (2, 1, 1)
+    with pytest.raises(ValueError):
+        p.block_view(3)
+    b = kv.kv_budgets_fraction(bp, 0.1)
+    want = [oracle.block_budget(n, 32, 4, 0.1) for n in (1000, 2000) for _ in range(2)]
+    assert list(b) == want
+    with pytest.raises(kv.KvError):
+        kv.kv_budgets_fraction(bp, 1.5)
+    fake = 1 << 20
+    assert lib.kv_block_scores(p.c, 3, fake, fake, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_block_scores(p.c, 0, fake, fake, None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_compact_blocks(p.c, 3, fake, fake, fake, fake, fake, 10, fake, fake,
+                                 None) == kv.KV_ERR_INVALID_ARG
+    assert lib.kv_compact_blocks(p.c, 2, fake, fake, fake, fake, fake, -1, fake, fake,
+                                 None) == kv.KV_ERR_INVALID_ARG
