@@ -276,10 +276,10 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # (workload, score rule, pool kernel); None for any other combination.
 TRAFFIC = {
     (DEFAULT_WORKLOAD, "dropkv", 1): {
-        "attn_tc_kernel": 17206244864 + 400259840,
-        "rescore_tc_kernel": 17659765504 + 267694336,
-        "select_kernel": 668149504 + 8272640,
-        "compact_kernel": 1731538176 + 1657757952},
+        "attn_tc_kernel": 17203023360 + 396891136,
+        "rescore_tc_kernel": 17591976448 + 267728128,
+        "select_kernel": 668146432 + 8167424,
+        "compact_kernel": 1731917568 + 1657358336},
     (DEFAULT_WORKLOAD, "attn_sum", 11): {
         "attn_stats_kernel": 8607008000 + 4206336,
         "rescore_tc_kernel": 8636366848 + 266142208,
