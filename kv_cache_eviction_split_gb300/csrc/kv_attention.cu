@@ -37,7 +37,7 @@
 // Warp roles (320 threads): warp 0 TMA producer (the lanes' Q chunks per item;
 // K tiles through a 3-stage ring running ahead of V tiles in a 2-stage ring);
 // warp 1 TMEM owner and MMA issuer; warps 2-5 softmax of lane 0, 6-9 of lane 1.
-// Work items are (unit, 16384-key split, chunk pair), walked round-robin by a
+// Work items are (unit, 32768-key split, chunk pair), walked round-robin by a
 // persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
 #include <cfloat>
 

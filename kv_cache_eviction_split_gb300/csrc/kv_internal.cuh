@@ -15,7 +15,7 @@ namespace kvevict {
 // Largest R = G * w the kernels accept.
 constexpr int kMaxRows = 512;
 // Keys per split of the pass-1 attention (each split writes one partial).
-constexpr int kSplitKeys = 16384;
+constexpr int kSplitKeys = 32768;
 // Bytes reserved at the start of every workspace for the status word.
 constexpr size_t kHeaderBytes = 256;
 
