@@ -432,3 +432,156 @@ def evict_blocks(prob, scores, k, v, bb: BlockBuffers, stream=None):
                       bb.total_rows, bb.k_out, bb.v_out, stream)
     n = bb.total_rows
     return bb.sel[:int(bb.block_offsets_host[-1])], bb.k_out[:n], bb.v_out[:n], bb.unit_offsets
+
+
+# ---------------------------------------------------------------------------
+# eviction from host memory, layer groups pipelined against the copies
+# ---------------------------------------------------------------------------
+class HostPipeline:
+    """Eviction of a problem whose Q, K and V are in pinned host memory.
+
+    The layers are taken in groups of `group_layers`: while group g is scored,
+    selected and compacted on one stream, group g+1's inputs are copied in on a
+    second and group g-1's kept indices and rows are copied out on a third.  Device
+    memory holds two groups of inputs and outputs, not the whole problem.
+
+    Outputs are group-major: for each layer group, its units in the usual order
+    (request, then layer, then head); `offsets` indexes them.  With one request this
+    is the usual unit order.
+    """
+
+    def __init__(self, prob: Problem, budgets_host: np.ndarray, group_layers: int = 4):
+        import torch
+        dev = prob.cu_dev.device
+        self.prob = prob
+        R, L, H = prob.num_requests, prob.num_layers, prob.num_kv_heads
+        Hq, d, w = prob.num_q_heads, prob.head_dim, prob.window
+        N = prob.total_tokens
+        b = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(R, L, H)
+        self.groups = [(l0, min(L, l0 + group_layers)) for l0 in range(0, L, group_layers)]
+        self.subs, self.bufs_g, self.rows, self.row0 = [], [], [], []
+        offs, row = [0], 0
+        for (l0, l1) in self.groups:
+            sub = Problem(list(prob.lengths), l1 - l0, H, Hq, d, w, prob.num_sinks,
+                          prob.softmax_scale, dev, prob.score_rule, prob.pool_kernel,
+                          prob.head_budgets)
+            bg = np.ascontiguousarray(b[:, l0:l1])
+            og = kv_make_offsets(sub, bg)
+            self.subs.append(sub)
+            self.bufs_g.append((torch.from_numpy(bg.reshape(-1)).to(dev),
+                                torch.from_numpy(og).to(dev), og))
+            self.rows.append(int(og[-1]))
+            self.row0.append(row)
+            offs.extend((row + og[1:]).tolist())
+            row += int(og[-1])
+        self.offsets = np.asarray(offs, dtype=np.int64)
+        self.total_rows = row
+        Lg = max(l1 - l0 for (l0, l1) in self.groups)
+        big = self.subs[int(np.argmax([l1 - l0 for (l0, l1) in self.groups]))]
+        rows_max = max(self.rows)
+        self.slots = []
+        for _ in range(2):
+            self.slots.append(dict(
+                q=torch.empty(R * Lg * Hq * w * d, dtype=torch.bfloat16, device=dev),
+                k=torch.empty(Lg * H * N * d, dtype=torch.bfloat16, device=dev),
+                v=torch.empty(Lg * H * N * d, dtype=torch.bfloat16, device=dev),
+                scores=torch.empty(Lg * H * N, dtype=torch.float32, device=dev),
+                pooled=torch.empty(Lg * H * N, dtype=torch.float32, device=dev)
+                if prob.pool_kernel > 1 else None,
+                score_ws=torch.zeros(max(kv_score_workspace_size(big), 256), dtype=torch.uint8,
+                                     device=dev),
+                select_ws=torch.zeros(max(kv_select_workspace_size(big), 256), dtype=torch.uint8,
+                                      device=dev),
+                hb=torch.empty(R * Lg * H, dtype=torch.int32, device=dev),
+                ho=torch.empty(R * Lg * H + 1, dtype=torch.int64, device=dev),
+                sel=torch.empty(max(rows_max, 1), dtype=torch.int32, device=dev),
+                k_out=torch.empty((max(rows_max, 1), d), dtype=torch.bfloat16, device=dev),
+                v_out=torch.empty((max(rows_max, 1), d), dtype=torch.bfloat16, device=dev)))
+        self.sel_host = torch.empty(max(self.total_rows, 1), dtype=torch.int32, pin_memory=True)
+        self.k_out_host = torch.empty((max(self.total_rows, 1), d), dtype=torch.bfloat16,
+                                      pin_memory=True)
+        self.v_out_host = torch.empty_like(self.k_out_host, pin_memory=True)
+        # per-head budgets are computed on the device: their offsets come back per group
+        self.head_offsets_host = [torch.empty(R * (l1 - l0) * H + 1, dtype=torch.int64,
+                                              pin_memory=True) for (l0, l1) in self.groups] \
+            if prob.head_budgets else None
+        self.streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        cur = torch.cuda.current_stream(dev)
+        for e in self.ev_comp + self.ev_out:
+            e.record(cur)
+
+    @property
+    def h2d_bytes(self) -> int:
+        p = self.prob
+        q = p.num_requests * p.num_layers * p.num_q_heads * p.window * p.head_dim * 2
+        return q + 2 * p.num_layers * p.num_kv_heads * p.total_tokens * p.head_dim * 2
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.total_rows * (4 + 2 * self.prob.head_dim * 2)
+
+    def run(self, q_host, k_host, v_host):
+        """Copies in, evicts and copies out every layer group; returns when the host
+        outputs (sel_host, k_out_host, v_out_host) are complete.  Raises KvError if a
+        kernel posted a device status."""
+        import torch
+        p = self.prob
+        R, H, Hq, w, d, N = (p.num_requests, p.num_kv_heads, p.num_q_heads, p.window,
+                             p.head_dim, p.total_tokens)
+        s_in, s_comp, s_out = self.streams
+        for g, (l0, l1) in enumerate(self.groups):
+            slot, sub, Lg = self.slots[g & 1], self.subs[g], l1 - l0
+            b_dev, o_dev, _ = self.bufs_g[g]
+            q = slot["q"][:R * Lg * Hq * w * d].view(R, Lg, Hq, w, d)
+            k = slot["k"][:Lg * H * N * d].view(Lg, H, N, d)
+            v = slot["v"][:Lg * H * N * d].view(Lg, H, N, d)
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(self.ev_comp[g & 1])
+                for r in range(R):
+                    q[r].copy_(q_host[r, l0:l1], non_blocking=True)
+                k.copy_(k_host[l0:l1], non_blocking=True)
+                v.copy_(v_host[l0:l1], non_blocking=True)
+                self.ev_in[g & 1].record(s_in)
+            s_comp.wait_event(self.ev_in[g & 1])
+            s_comp.wait_event(self.ev_out[g & 1])
+            scores = slot["scores"][:Lg * H * N]
+            kv_score(sub, q, k, v, scores, slot["score_ws"], s_comp)
+            ranked = scores
+            if p.pool_kernel > 1:
+                ranked = slot["pooled"][:Lg * H * N]
+                kv_pool_scores(sub, p.pool_kernel, scores, ranked, s_comp)
+            if p.head_budgets:
+                hb, ho = slot["hb"][:R * Lg * H], slot["ho"][:R * Lg * H + 1]
+                kv_head_budgets(sub, ranked, b_dev, o_dev, hb, ho, slot["select_ws"], s_comp)
+                b_dev, o_dev = hb, ho
+            kv_select_topk(sub, ranked, b_dev, o_dev, slot["sel"], slot["select_ws"], s_comp)
+            kv_compact(sub, k, v, slot["sel"], o_dev, self.rows[g], slot["k_out"],
+                       slot["v_out"], s_comp)
+            self.ev_comp[g & 1].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(self.ev_comp[g & 1])
+                a, n = self.row0[g], self.rows[g]
+                self.sel_host[a:a + n].copy_(slot["sel"][:n], non_blocking=True)
+                self.k_out_host[a:a + n].copy_(slot["k_out"][:n], non_blocking=True)
+                self.v_out_host[a:a + n].copy_(slot["v_out"][:n], non_blocking=True)
+                if p.head_budgets:
+                    self.head_offsets_host[g].copy_(slot["ho"][:R * Lg * H + 1],
+                                                    non_blocking=True)
+                self.ev_out[g & 1].record(s_out)
+        for st in self.streams:
+            st.synchronize()
+        for slot in self.slots:
+            for ws in (slot["score_ws"], slot["select_ws"]):
+                code = kv_check_status(ws, s_comp)
+                if code != KV_OK:
+                    raise KvError(code, "HostPipeline.run")
+        if p.head_budgets:
+            offs = [0]
+            for g in range(len(self.groups)):
+                offs.extend((self.row0[g] + self.head_offsets_host[g].numpy()[1:]).tolist())
+            self.offsets = np.asarray(offs, dtype=np.int64)
+        n = self.total_rows
+        return self.sel_host[:n], self.k_out_host[:n], self.v_out_host[:n], self.offsets
