@@ -47,7 +47,7 @@ def product_budgets(kv, wl, profile=None) -> np.ndarray:
     return np.asarray(rows, dtype=np.int32)
 
 
-class GpuRun:
+class DeviceRun:
     """The three C-ABI calls on one workload, results kept on the device."""
 
     def __init__(self, kv, wl, budgets=None, dw=None, score_rule=0, pool_kernel=1,
@@ -115,7 +115,7 @@ def _check_scores(g, S, what):
     return max_rel
 
 
-def check_unit(run: GpuRun, r, l, h, oracle_out=None):
+def check_unit(run: DeviceRun, r, l, h, oracle_out=None):
     """Asserts parity of one unit; returns a small dict of error figures."""
     wl = run.wl
     n, g_scores, g_sel, kout, vout, b = run.unit_results(r, l, h)
@@ -154,7 +154,7 @@ def check_unit(run: GpuRun, r, l, h, oracle_out=None):
     return {"max_rel": max_rel, "swapped": len(diff) // 2}
 
 
-def check_units(run: GpuRun, units, threads=None):
+def check_units(run: DeviceRun, units, threads=None):
     """Oracle for several units in parallel threads (ctypes releases the GIL)."""
     wl = run.wl
     threads = threads or min(len(units), os.cpu_count() or 1)

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 def test_block_eviction_matches_oracle(cuda_lib, wl, block_layers, q, kernel):
     import torch
     kv = cuda_lib
-    run = parity.GpuRun(kv, wl, score_rule=oracle.RULE_ATTN_SUM)
+    run = parity.DeviceRun(kv, wl, score_rule=oracle.RULE_ATTN_SUM)
     assert run.status_score == 0
     bb = kv.BlockBuffers(run.prob, block_layers, q, pool_kernel=kernel)
     sel, k_out, v_out, offsets = kv.evict_blocks(run.prob, run.bufs.scores, run.dw.k, run.dw.v,

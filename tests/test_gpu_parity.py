@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(cuda_lib, wl, **kw):
-    run = parity.GpuRun(cuda_lib, wl, **kw)
+    run = parity.DeviceRun(cuda_lib, wl, **kw)
     assert run.status_score == 0 and run.status_select == 0
     return run
 
@@ -90,7 +90,7 @@ def test_equal_scores_break_ties_to_lower_index(cuda_lib):
     dw.k[0, 0, 100:900 - wl.window] = dw.k[0, 0, 100]
     dw.v[0, 0, 100:900 - wl.window] = dw.v[0, 0, 100]
     budgets = np.full((1, 1, 1), 200, dtype=np.int32)
-    run = parity.GpuRun(cuda_lib, wl, budgets=budgets, dw=dw)
+    run = parity.DeviceRun(cuda_lib, wl, budgets=budgets, dw=dw)
     n, scores, sel, _, _, b = run.unit_results(0, 0, 0)
     mine = oracle.select(scores.astype(np.float64), wl.window, wl.num_sinks, b)
     np.testing.assert_array_equal(sel, mine)

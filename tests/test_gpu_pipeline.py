@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 def test_host_pipeline_equals_device_path(cuda_lib, wl, group, rule, pool, heads):
     import torch
     kv = cuda_lib
-    run = parity.GpuRun(kv, wl, score_rule=rule, pool_kernel=pool, head_budgets=heads)
+    run = parity.DeviceRun(kv, wl, score_rule=rule, pool_kernel=pool, head_budgets=heads)
     assert run.status_score == 0 and run.status_select == 0
     dw = run.dw
     qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)

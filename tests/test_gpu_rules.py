@@ -26,7 +26,7 @@ SMALL = [
 
 
 def _run(kv, wl, **kw):
-    run = parity.GpuRun(kv, wl, **kw)
+    run = parity.DeviceRun(kv, wl, **kw)
     assert run.status_score == 0 and run.status_select == 0
     return run
 
