@@ -100,3 +100,28 @@ def test_block_scores_random_input(cuda_lib):
     torch.cuda.synchronize()
     ref = s.double().reshape(2, 2 * wl.num_kv_heads, -1).sum(dim=1)
     torch.testing.assert_close(out[:, 0].double(), ref, rtol=1e-6, atol=0)
+
+
+def test_block_eviction_head_dim_64(cuda_lib):
+    """The d = 64 instances (pass 1, rescoring, block compaction) on a two-layer block."""
+    import torch
+    kv = cuda_lib
+    wl = synth.TINY.scaled(name="tiny_2L_2kv_d64_n3000", num_layers=2, num_kv_heads=2,
+                           num_q_heads=8, lengths=(3000,))
+    run = parity.DeviceRun(kv, wl, score_rule=oracle.RULE_ATTN_SUM)
+    assert run.status_score == 0
+    bb = kv.BlockBuffers(run.prob, 2, 0.2, pool_kernel=13)
+    sel, k_out, v_out, _ = kv.evict_blocks(run.prob, run.bufs.scores, run.dw.k, run.dw.v, bb)
+    torch.cuda.synchronize()
+    assert kv.kv_check_status(bb.select_ws) == 0
+    sel = sel.cpu().numpy()
+    ko = k_out.cpu().view(torch.int16).numpy().view(np.uint16)
+    w, s, n = wl.window, wl.num_sinks, 3000
+    g_pool = bb.pooled.cpu().numpy()[0, 0].astype(np.float64)
+    np.testing.assert_array_equal(sel, oracle.select(g_pool, w, s, oracle.block_budget(n, w, s, 0.2)))
+    for l in range(2):
+        for h in range(2):
+            u = wl.unit_index(0, l, h)
+            a0, a1 = int(bb.unit_offsets_host[u]), int(bb.unit_offsets_host[u + 1])
+            _, k, _ = run.dw.unit_host(0, l, h)
+            np.testing.assert_array_equal(ko[a0:a1], k[sel])

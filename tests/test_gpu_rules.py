@@ -113,7 +113,9 @@ def _layer_heads(run, r, l, ranked):
 
 
 @pytest.mark.parametrize("rule,kernel", [(0, 1), (ATTN_SUM, 11)], ids=["dropkv", "attn_sum_k11"])
-@pytest.mark.parametrize("wl", SMALL[1:], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", SMALL[1:] + [synth.TINY.scaled(name="tiny_1L_4kv_d64_n2048",
+                                                              num_kv_heads=4, num_q_heads=16)],
+                         ids=lambda w: w.name)
 def test_head_budgets_small_workloads(cuda_lib, wl, rule, kernel):
     run = _run(cuda_lib, wl, score_rule=rule, pool_kernel=kernel, head_budgets=True)
     ranked = run.ranked_scores()
