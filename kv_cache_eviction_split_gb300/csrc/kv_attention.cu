@@ -20,8 +20,8 @@
 // softmax of one lane overlaps the MMAs of the other.  A softmax thread owns one
 // row of its lane over all 128 keys of a tile: no exchange between threads.  It
 // turns S into P' = 2^(s c - m + 13) and stores P' back over the S columns in
-// fp16 (two keys per column).  P V runs in fp16: the softmax warps convert each
-// V tile in shared memory from bf16 to fp16 in place first, which is exact for
+// fp16 (two keys per column).  P V runs in fp16: two converter warps turn each
+// V tile in shared memory from bf16 to fp16 in place as it lands, which is exact for
 // normal values below 65504 (larger ones post KV_ERR_UNSUPPORTED).  fp16 keeps
 // 11 bits of p where bf16 keeps 8; a single bf16 P would leave a with ~2^-9
 // relative error, which the rescoring expansion amplifies where a is close to
@@ -34,9 +34,11 @@
 // The attention-sum rule needs only m and l: attn_stats_kernel (below) computes
 // them from K alone.
 //
-// Warp roles (320 threads): warp 0 TMA producer (the lanes' Q chunks per item;
+// Warp roles (384 threads): warp 0 TMA producer (the lanes' Q chunks per item;
 // K tiles through a 3-stage ring running ahead of V tiles in a 2-stage ring);
-// warp 1 TMEM owner and MMA issuer; warps 2-5 softmax of lane 0, 6-9 of lane 1.
+// warp 1 TMEM owner and MMA issuer; warps 2-5 softmax of lane 0, 6-9 of lane 1;
+// warps 10-11 convert every V tile to fp16 as it lands (and compute ||v_j||^2),
+// so neither lane's softmax waits for V or for the other lane.
 // Work items are (unit, 32768-key split, chunk pair), walked round-robin by a
 // persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
 #include <cfloat>
@@ -55,7 +57,9 @@ constexpr int kChunkRows = 128;
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kSoftWarps = 8;       // 4 per lane
-constexpr int kThreads = (2 + kSoftWarps) * 32;
+constexpr int kConvWarps = 2;       // V tiles to fp16, ||v||^2
+constexpr int kThreads = (2 + kSoftWarps + kConvWarps) * 32;
+constexpr int kStatThreads = (2 + kSoftWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;     // O of lane L at column kOCol + 128 L
 constexpr int kBlockBytes = 128 * 128;   // [128 rows][64 bf16], 128 B swizzle
@@ -223,7 +227,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
     uint64_t *k_full = bars, *k_empty = bars + kKStages;
     uint64_t *v_full = bars + 2 * kKStages, *v_empty = v_full + kVStages;
-    uint64_t *v_conv = v_empty + kVStages;  // [stage]: V tile converted to fp16 (8 warp shares)
+    uint64_t *v_conv = v_empty + kVStages;  // [stage]: V tile converted to fp16 (2 warps)
     uint64_t *q_full = v_conv + kVStages, *q_empty = q_full + 1;
     uint64_t *s_full = q_empty + 1;        // [lane]: S of the lane's next tile is in TMEM
     uint64_t *p_full = s_full + 2;         // [lane]: P written (4 softmax warps)
@@ -243,7 +247,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
-            mbar_init(&v_conv[s], kSoftWarps);
+            mbar_init(&v_conv[s], kConvWarps);
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -445,7 +449,7 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             mma_commit(mma_done);
             mbar_drain(mma_done, 0, kDrainNs);
         }
-    } else if (run) {
+    } else if (run && warp < 2 + kSoftWarps) {
         // ------------------------------------------------------------ softmax
         const int L = (warp - 2) >> 2;                    // lane (row set) of this warp
         const int quarter = warp & 3;
@@ -455,50 +459,11 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
         const uint32_t o_base = tmem + lane_addr + kOCol + 128 * L;
         const float cs = P.scale_log2;
         long long sc = 0, oc = 0;
-        long long tbase = 0;   // tiles of this CTA's earlier items (V stage and parity)
         bool ok = true;
-        // This warp's share of converting the V tile of item tile ti to fp16, which
-        // also yields ||v_j||^2 of its keys (written for the rescoring pass): when
-        // both lanes use every tile the 8 softmax warps take 16 keys each, otherwise
-        // the 4 warps of the lane that uses the tile take 32 each (and arrive twice
-        // each at the 8-count barrier).  Two threads share a key row (lane, lane^16).
-        bool both = false;
-        int it_t0 = 0;
-        long long v2_row0 = 0;   // first key of the item's unit in ||v||^2
-        int unit_n = 0;
-        auto convert_v = [&](int ti) -> bool {
-            const long long vc = tbase + ti;
-            const int s = (int)(vc % kVStages);
-            const bool ok2 = __all_sync(0xffffffffu,
-                                        mbar_wait(&v_full[s], (uint32_t)((vc / kVStages) & 1),
-                                                  abort_flag, P.wait_ns));
-            if (!ok2) return false;
-            uint8_t *tile = smem + Ly::kV + s * Ly::kOp;
-            const int keys = both ? 16 : 32;
-            const int cw = both ? warp - 2 : (warp - 2) & 3;
-            bool bad = false;
-            for (int k0 = 0; k0 < keys; k0 += 16) {
-                const int row = cw * keys + k0 + (lane & 15);
-                float q = row_half_to_f16<D>(tile, row, lane >> 4, bad);
-                q += __shfl_xor_sync(0xffffffffu, q, 16);
-                const int j = (it_t0 + ti) * kTileKeys + row;   // key of the unit
-                if (lane < 16 && j < unit_n) A.v2[v2_row0 + j] = q;
-            }
-            if (bad) post_status(A.status, KV_ERR_UNSUPPORTED);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cnt(&v_conv[s], both ? 1u : 2u);
-            return true;
-        };
         for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
             const Item it = decode_item(item, A, P);
             const LaneWork w = lane_work(A, it, L);
             const UnitInfo U = unit_info(P, it.u, P.cu);
-            const long long item_tiles = it.t1 - it.t0;
-            both = A.parts == 1 && lane_work(A, it, 1).steps > 0;
-            v2_row0 = U.kv_row0;
-            unit_n = U.n;
-            it_t0 = it.t0;
             const int row = w.chunk * kChunkRows + rr;
             const bool row_valid = row < P.rows;
             const int slot = A.parts == 1 ? it.split : 2 * it.split + L;
@@ -507,11 +472,8 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             if (w.steps == 0) {
                 // no tile for this lane: an empty partial (l = 0) for the merge to skip
                 if (A.parts == 2 && row_valid) A.part_ml[prow_idx] = make_float2(-INFINITY, 0.f);
-                tbase += item_tiles;
                 continue;
             }
-            ok = convert_v(w.first);
-            if (!ok) break;
             const int pos = U.n - P.w + (row % P.w);      // last key this row sees
             const int pos_min = U.n - P.w;
             float m_used = -INFINITY, l = 0.f;
@@ -617,11 +579,6 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[L]);
-                // the lane's next tile: convert its V while S of that tile computes
-                if (j + 1 < w.steps) {
-                    ok = convert_v(ti + w.stride);
-                    if (!ok) break;
-                }
             }
             if (!ok) break;
             // item end: read O_L once the lane's last P V is done, write the partial
@@ -652,6 +609,44 @@ attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
             if (row_valid) A.part_ml[prow_idx] = make_float2(m_used, l * kUnscale);
             sc += w.steps;
             ++oc;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            post_status(A.status, KV_ERR_TIMEOUT);
+        }
+    } else if (run) {
+        // ------------------------------------------------------------ V conversion
+        // Every V tile of the item, in load order: warp cw converts rows 64 cw ..
+        // 64 cw + 63 to fp16 in place, two threads per row (lane, lane ^ 16), and
+        // writes ||v_j||^2 of those keys for the rescoring pass.
+        const int cw = warp - 2 - kSoftWarps;
+        long long tbase = 0;   // tiles of this CTA's earlier items (V stage and parity)
+        bool ok = true;
+        for (long long item = blockIdx.x; ok && item < A.total_items; item += gridDim.x) {
+            const Item it = decode_item(item, A, P);
+            const UnitInfo U = unit_info(P, it.u, P.cu);
+            const int item_tiles = it.t1 - it.t0;
+            for (int ti = 0; ok && ti < item_tiles; ++ti) {
+                const long long vc = tbase + ti;
+                const int s = (int)(vc % kVStages);
+                ok = __all_sync(0xffffffffu, mbar_wait(&v_full[s], (uint32_t)((vc / kVStages) & 1),
+                                                       abort_flag, P.wait_ns));
+                if (!ok) break;
+                uint8_t *tile = smem + Ly::kV + s * Ly::kOp;
+                bool bad = false;
+#pragma unroll 1
+                for (int k0 = 0; k0 < 64; k0 += 16) {
+                    const int row = cw * 64 + k0 + (lane & 15);
+                    float q = row_half_to_f16<D>(tile, row, lane >> 4, bad);
+                    q += __shfl_xor_sync(0xffffffffu, q, 16);
+                    const int j = (it.t0 + ti) * kTileKeys + row;   // key of the unit
+                    if (lane < 16 && j < U.n) A.v2[U.kv_row0 + j] = q;
+                }
+                if (bad) post_status(A.status, KV_ERR_UNSUPPORTED);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&v_conv[s]);
+            }
             tbase += item_tiles;
         }
         if (!ok) {
@@ -692,7 +687,7 @@ struct StatLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kStatThreads, 1)
 attn_stats_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const AttnArgs A) {
     using Ly = StatLayout<D>;
@@ -995,7 +990,8 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
         const int smem = StatLayout<D>::kTotal;
         cudaFuncSetAttribute(attn_stats_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
-        if (grid > 0) attn_stats_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, A);
+        if (grid > 0)
+            attn_stats_kernel<D><<<(unsigned)grid, kStatThreads, smem, st>>>(P, mq, mk, A);
         return cudaGetLastError();
     }
     const int smem = Layout<D>::kTotal;
