@@ -276,10 +276,10 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # (workload, score rule, pool kernel); None for any other combination.
 TRAFFIC = {
     (DEFAULT_WORKLOAD, "dropkv", 1): {
-        "attn_tc_kernel": 17200321280 + 257391104,
-        "rescore_tc_kernel": 17598075136 + 267709184,
-        "select_kernel": 668262656 + 8606720,
-        "compact_kernel": 1731428864 + 1657517824},
+        "attn_tc_kernel": 17206489088 + 259797248,
+        "rescore_tc_kernel": 17581460992 + 267090688,
+        "select_kernel": 668124160 + 8176640,
+        "compact_kernel": 1731427840 + 1657543168},
     (DEFAULT_WORKLOAD, "attn_sum", 11): {
         "attn_stats_kernel": 8607008000 + 4206336,
         "rescore_tc_kernel": 8636366848 + 266142208,
