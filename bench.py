@@ -61,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=0, help="oracle sample size (0: one per core)")
@@ -602,13 +602,12 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
         except RuntimeError as e:
             return {"value": None, "unit": UNIT, "error": "pinned host allocation failed: %s" % e}
         pipe.run(qh, kh, vh)
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            pipe.run(qh, kh, vh)
-        dt = (time.perf_counter() - t0) / args.e2e_steps
+        dt, spread = _timed_steps(args.e2e_steps, lambda: pipe.run(qh, kh, vh), torch)
         return {"value": unit_tokens / dt, "unit": UNIT, "ms_per_step": dt * 1e3,
+                "ms_per_step_min_max": spread,
                 "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
-                "steps": args.e2e_steps, "api": "kv.HostPipeline, groups of 4 layers"}
+                "steps": args.e2e_steps, "statistic": "median of per-step host wall times",
+                "api": "kv.HostPipeline, groups of 4 layers"}
     try:
         qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)
         kh = torch.empty(dw.k.shape, dtype=dw.k.dtype, pin_memory=True)
@@ -639,15 +638,29 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
 
     one()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        one()
-    torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / args.e2e_steps
+    dt, spread = _timed_steps(args.e2e_steps, one, torch)
     h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
     d2h = selh.numel() * 4 + (koh.numel() + voh.numel()) * 2
     return {"value": unit_tokens / dt, "unit": UNIT, "ms_per_step": dt * 1e3,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+            "ms_per_step_min_max": spread, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps, "statistic": "median of per-step host wall times"}
+
+
+def _timed_steps(steps, fn, torch):
+    """Host wall time of each of `steps` calls of fn (each ending in a device
+    synchronisation): the median in seconds and [min, max] in ms.  The host link
+    is shared with other work on the machine, so single steps can stall; the
+    median keeps one stall from setting the number."""
+    times = []
+    for _ in range(max(1, steps)):
+        t0 = time.perf_counter()
+        fn()
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+    times.sort()
+    n = len(times)
+    med = times[n // 2] if n % 2 else 0.5 * (times[n // 2 - 1] + times[n // 2])
+    return med, [round(times[0] * 1e3, 2), round(times[-1] * 1e3, 2)]
 
 
 if __name__ == "__main__":
