@@ -69,6 +69,9 @@ def parse_args(argv=None):
     ap.add_argument("--pool", type=int, default=1, help="max-pool kernel before selection (1: none)")
     ap.add_argument("--head-budgets", action="store_true",
                     help="per-head budgets from the scores before selection")
+    ap.add_argument("--fused", action="store_true",
+                    help="score, select and compaction as one cooperative launch "
+                         "(kv_evict_fused); no pooling, per-head budgets or blocks")
     ap.add_argument("--block-layers", type=int, default=0,
                     help="block eviction over blocks of this many layers (0: off)")
     return ap.parse_args(argv)
@@ -273,14 +276,14 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # DRAM bytes (read + write) per launch from single-pass ncu captures of the current
 # kernels (profiles/dram_traffic_long_32L_8kv_n131072.md and
 # profiles/launch_list_attn_sum_pool11_long_32L_8kv_n131072.md), keyed by
-# (workload, score rule, pool kernel); None for any other combination.
+# (workload, score rule, pool kernel, fused); None for any other combination.
 TRAFFIC = {
-    (DEFAULT_WORKLOAD, "dropkv", 1): {
+    (DEFAULT_WORKLOAD, "dropkv", 1, False): {
         "attn_tc_kernel": 17206489088 + 259797248,
         "rescore_tc_kernel": 17581460992 + 267090688,
         "select_kernel": 668124160 + 8176640,
         "compact_kernel": 1731427840 + 1657543168},
-    (DEFAULT_WORKLOAD, "attn_sum", 11): {
+    (DEFAULT_WORKLOAD, "attn_sum", 11, False): {
         "attn_stats_kernel": 8607008000 + 4206336,
         "rescore_tc_kernel": 8636366848 + 266142208,
         "pool_kernel": 134264320 + 84282624,
@@ -313,6 +316,8 @@ def product_budgets(kv, wl):
 
 def bench_config_tag(wl, args):
     tag = {"workload": wl.name}
+    if getattr(args, "fused", False):
+        tag["launch"] = "fused: one cooperative kernel per step"
     if args.score_rule != "dropkv" or args.pool > 1 or args.head_budgets or args.block_layers:
         tag.update(score_rule=args.score_rule, pool_kernel=args.pool,
                    head_budgets=bool(args.head_budgets))
@@ -326,6 +331,19 @@ def stage_roofline(stage, ms, wl, budgets, peaks, rule=0, blk=1):
     scoring passes, their algorithmic tensor flops: two d-long dot products per
     (window row, visible key) pair each, one for the attention sum, which needs
     only q.k).  The attention sum needs no V: its passes read K only."""
+    if stage == "fused":
+        # the fused kernel runs the phases of all four: their bytes and flops add up
+        parts = [stage_roofline(s, ms, wl, budgets, peaks, rule, blk)
+                 for s in ("attention", "rescore", "select", "compact")]
+        nbytes = sum(p["algorithmic_bytes"] for p in parts)
+        flops = sum(p["tensor"]["algorithmic_flops"] for p in parts if "tensor" in p)
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        tpeak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                "tensor": {"algorithmic_flops": flops,
+                           "achieved_tflops": flops / (ms * 1e-3) / 1e12, "peak_tflops": tpeak,
+                           "frac": flops / (ms * 1e-3) / 1e12 / tpeak}}
     d = wl.head_dim
     units = wl.num_units
     n_tot = sum(wl.seq_lengths())
@@ -426,6 +444,10 @@ def main(argv=None):
     blk = args.block_layers
     if blk and heads:
         raise SystemExit("--block-layers and --head-budgets do not combine")
+    fused = args.fused
+    if fused and (blk or heads or pool > 1):
+        raise SystemExit("--fused takes neither --pool, --head-budgets nor --block-layers")
+    stage_names = ["fused"] if fused else STAGES
     prob = kv.Problem.for_workload(wl, device=dev, score_rule=rule, pool_kernel=pool,
                                    head_budgets=heads)
     bufs = kv.Buffers(prob, budgets)
@@ -444,6 +466,13 @@ def main(argv=None):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
+        if fused:
+            kv.kv_evict_fused(prob, dw.q, dw.k, dw.v, bufs.budgets, bufs.offsets,
+                              bufs.total_rows, bufs.scores, bufs.sel, bufs.k_out, bufs.v_out,
+                              bufs.score_ws, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         kv.kv_score_attention(prob, dw.q, dw.k, dw.v, bufs.score_ws, stream)
         if ev is not None:
             ev[1].record(stream)
@@ -495,7 +524,7 @@ def main(argv=None):
     if args.steps <= 0:
         per = (time.perf_counter() - t_w0) / max(args.warmup, 1)
         args.steps = int(min(2000, max(20, math.ceil(2.0 / max(per, 1e-4)))))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
            for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -512,7 +541,7 @@ def main(argv=None):
     if st != (0, 0):
         raise SystemExit("device status after the timed region: %s" % (st,))
     stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
-                                   for i in range(args.steps)) for j, s in enumerate(STAGES)}
+                                   for i in range(args.steps)) for j, s in enumerate(stage_names)}
     ms_per_step = total_ms / args.steps
     n_tot = sum(wl.seq_lengths())
     unit_tokens = n_tot * wl.num_layers * wl.num_kv_heads
@@ -520,16 +549,17 @@ def main(argv=None):
     alg_bytes = algorithmic_bytes(wl, budgets)
     hbm_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
 
-    stages = [s for s in STAGES if (s != "pool" or pool > 1) and (s != "heads" or heads)
-              and (s != "blocks" or blk)]
+    stages = ["fused"] if fused else \
+        [s for s in STAGES if (s != "pool" or pool > 1) and (s != "heads" or heads)
+         and (s != "blocks" or blk)]
     for s in list(stage_ms):
         if s not in stages:
             stage_ms.pop(s)
     dominant = max(stages, key=lambda s: stage_ms[s])
     roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule, blk)
-    kernel = stage_kernel(dominant, rule)
+    kernel = "fused_kernel" if fused else stage_kernel(dominant, rule)
     traffic = None if heads or blk else \
-        TRAFFIC.get((wl.name, args.score_rule, pool), {}).get(kernel)
+        TRAFFIC.get((wl.name, args.score_rule, pool, fused), {}).get(kernel)
     roof.update({"kernel": kernel, "peak_source": peak_src,
                  "traffic": traffic, "stage_ms": stage_ms[dominant],
                  "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
@@ -554,7 +584,8 @@ def main(argv=None):
                     "peak_source": peak_src},
             "stages_ms": stage_ms,
             "roofline": roof,
-            "gpu_launches": args.steps * (sum(LAUNCHES_PER_STEP[s] for s in stages)
+            "gpu_launches": args.steps * (1 if fused else
+                                          sum(LAUNCHES_PER_STEP[s] for s in stages)
                                           + (1 if wl.rows > 128 else 0)),
             "clocks": clocks}
 
@@ -598,7 +629,8 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
             qh.copy_(dw.q)
             kh.copy_(dw.k)
             vh.copy_(dw.v)
-            pipe = kv.HostPipeline(prob, budgets, group_layers=4)
+            pipe = kv.HostPipeline(prob, budgets, group_layers=4,
+                                   fused=bool(getattr(args, "fused", False)))
         except RuntimeError as e:
             return {"value": None, "unit": UNIT, "error": "pinned host allocation failed: %s" % e}
         pipe.run(qh, kh, vh)
@@ -607,7 +639,8 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
                 "ms_per_step_min_max": spread,
                 "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
                 "steps": args.e2e_steps, "statistic": "median of per-step host wall times",
-                "api": "kv.HostPipeline, groups of 4 layers"}
+                "api": "kv.HostPipeline, groups of 4 layers%s"
+                       % (", fused launch per group" if pipe.fused else "")}
     try:
         qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)
         kh = torch.empty(dw.k.shape, dtype=dw.k.dtype, pin_memory=True)

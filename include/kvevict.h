@@ -253,6 +253,36 @@ kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const in
                      void *stream);
 
 /*
+ * kv_score, kv_select_topk and kv_compact in ONE launch: the whole eviction
+ * path (the score p/(1-p)*||a - v_j|| of DropKV, "Methodology in Plain English",
+ * or the rule p->score_rule selects; the budgeted top-k with sinks and window
+ * kept; the packed copy of the kept rows) as the phases of one persistent
+ * cooperative kernel, one CTA per SM, separated by grid-wide barriers.  The
+ * phases run the same device code as the three calls, so scores, sel_idx,
+ * k_out and v_out are bit-identical to theirs.
+ *
+ * Arguments: those of kv_score (q_win, k, v, scores, workspace and its size:
+ * the kv_score workspace), of kv_select_topk (budgets_dev, offsets_dev,
+ * sel_idx) and of kv_compact (total_rows, k_out, v_out; with total_rows = 0
+ * nothing is copied and k_out / v_out may be NULL).  Pooling and per-head
+ * budgets are not part of the fused path: run kv_score, kv_pool_scores,
+ * kv_head_budgets, kv_select_topk and kv_compact for those.
+ *
+ * Device-side errors go to the score workspace's status word
+ * (kv_check_status): KV_ERR_BUDGET from the selection (that unit's indices are
+ * not written), KV_ERR_UNSUPPORTED for V values fp16 cannot hold,
+ * KV_ERR_TIMEOUT when a pipeline wait or a grid barrier wait exceeds the limit
+ * of kv_set_wait_limit_ns (the kernel then skips its remaining phases and
+ * returns).  KV_ERR_CUDA if the device cannot run a cooperative launch of one
+ * CTA per SM.  Asynchronous on `stream` (an in-stream memset of the barrier
+ * words precedes the kernel).
+ */
+kv_status kv_evict_fused(const kv_problem *p, const void *q_win, const void *k, const void *v,
+                         const int32_t *budgets_dev, const int64_t *offsets_dev,
+                         int64_t total_rows, float *scores, int32_t *sel_idx, void *k_out,
+                         void *v_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of a
  * kv_score or kv_select_topk workspace.  *device_status receives the kv_status
  * a kernel posted (KV_OK if none).  Returns KV_ERR_CUDA if the stream itself

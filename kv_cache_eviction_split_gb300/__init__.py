@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc",
                     "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores",
                     "kv_head_budgets", "kv_block_scores", "kv_compact_blocks",
-                    "kv_budgets_fraction")
+                    "kv_budgets_fraction", "kv_evict_fused")
 
 
 class KvError(RuntimeError):
@@ -98,6 +98,7 @@ def load(path: Optional[str] = None):
         "kv_block_scores": [P, i32, vp, vp, vp],
         "kv_compact_blocks": [P, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp],
         "kv_budgets_fraction": [P, f64, ctypes.POINTER(i32)],
+        "kv_evict_fused": [P, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -285,6 +286,17 @@ def kv_select_topk(prob, scores, budgets_dev, offsets_dev, sel_idx, workspace, s
            "kv_select_topk")
 
 
+def kv_evict_fused(prob, q_win, k, v, budgets_dev, offsets_dev, total_rows: int, scores,
+                   sel_idx, k_out, v_out, workspace, stream=None):
+    """kv_score + kv_select_topk + kv_compact in one cooperative launch; device errors
+    (selection budgets included) go to the score workspace's status word."""
+    _check(load().kv_evict_fused(prob.c, _ptr(q_win), _ptr(k), _ptr(v), _ptr(budgets_dev),
+                                 _ptr(offsets_dev), int(total_rows), _ptr(scores),
+                                 _ptr(sel_idx), _ptr(k_out), _ptr(v_out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "kv_evict_fused")
+
+
 def kv_compact(prob, k, v, sel_idx, offsets_dev, total_rows: int, k_out, v_out, stream=None):
     _check(load().kv_compact(prob.c, _ptr(k), _ptr(v), _ptr(sel_idx), _ptr(offsets_dev),
                              int(total_rows), _ptr(k_out), _ptr(v_out), _stream(stream)),
@@ -361,9 +373,17 @@ class Buffers:
         self.head_offsets = torch.empty_like(self.offsets) if prob.head_budgets else None
 
 
-def evict(prob: Problem, q, k, v, bufs: Buffers, stream=None):
+def evict(prob: Problem, q, k, v, bufs: Buffers, stream=None, fused: bool = False):
     """Score (pool, if prob.pool_kernel > 1; per-head budgets, if prob.head_budgets),
-    select and compact on `stream`; returns (sel_idx, k_out, v_out, offsets)."""
+    select and compact on `stream`; returns (sel_idx, k_out, v_out, offsets).  With
+    fused=True (no pooling, no per-head budgets) the path runs as one launch."""
+    if fused:
+        if prob.pool_kernel > 1 or prob.head_budgets:
+            raise ValueError("the fused path takes neither pooling nor per-head budgets")
+        kv_evict_fused(prob, q, k, v, bufs.budgets, bufs.offsets, bufs.total_rows, bufs.scores,
+                       bufs.sel, bufs.k_out, bufs.v_out, bufs.score_ws, stream)
+        n = bufs.total_rows
+        return bufs.sel[:n], bufs.k_out[:n], bufs.v_out[:n], bufs.offsets
     kv_score(prob, q, k, v, bufs.scores, bufs.score_ws, stream)
     ranked = bufs.scores
     if prob.pool_kernel > 1:
@@ -450,7 +470,11 @@ class HostPipeline:
     is the usual unit order.
     """
 
-    def __init__(self, prob: Problem, budgets_host: np.ndarray, group_layers: int = 4):
+    def __init__(self, prob: Problem, budgets_host: np.ndarray, group_layers: int = 4,
+                 fused: bool = False):
+        if fused and (prob.pool_kernel > 1 or prob.head_budgets):
+            raise ValueError("the fused path takes neither pooling nor per-head budgets")
+        self.fused = fused
         import torch
         dev = prob.cu_dev.device
         self.prob = prob
@@ -523,6 +547,25 @@ class HostPipeline:
     def d2h_bytes(self) -> int:
         return self.total_rows * (4 + 2 * self.prob.head_dim * 2)
 
+    def _evict_group(self, sub, q, k, v, scores, slot, b_dev, o_dev, g, s_comp):
+        """The separate calls for layer group g: score, pool, per-head budgets, select,
+        compact."""
+        p = self.prob
+        R, H, N = p.num_requests, p.num_kv_heads, p.total_tokens
+        Lg = self.groups[g][1] - self.groups[g][0]
+        kv_score(sub, q, k, v, scores, slot["score_ws"], s_comp)
+        ranked = scores
+        if p.pool_kernel > 1:
+            ranked = slot["pooled"][:Lg * H * N]
+            kv_pool_scores(sub, p.pool_kernel, scores, ranked, s_comp)
+        if p.head_budgets:
+            hb, ho = slot["hb"][:R * Lg * H], slot["ho"][:R * Lg * H + 1]
+            kv_head_budgets(sub, ranked, b_dev, o_dev, hb, ho, slot["select_ws"], s_comp)
+            b_dev, o_dev = hb, ho
+        kv_select_topk(sub, ranked, b_dev, o_dev, slot["sel"], slot["select_ws"], s_comp)
+        kv_compact(sub, k, v, slot["sel"], o_dev, self.rows[g], slot["k_out"], slot["v_out"],
+                   s_comp)
+
     def run(self, q_host, k_host, v_host):
         """Copies in, evicts and copies out every layer group; returns when the host
         outputs (sel_host, k_out_host, v_out_host) are complete.  Raises KvError if a
@@ -548,18 +591,11 @@ class HostPipeline:
             s_comp.wait_event(self.ev_in[g & 1])
             s_comp.wait_event(self.ev_out[g & 1])
             scores = slot["scores"][:Lg * H * N]
-            kv_score(sub, q, k, v, scores, slot["score_ws"], s_comp)
-            ranked = scores
-            if p.pool_kernel > 1:
-                ranked = slot["pooled"][:Lg * H * N]
-                kv_pool_scores(sub, p.pool_kernel, scores, ranked, s_comp)
-            if p.head_budgets:
-                hb, ho = slot["hb"][:R * Lg * H], slot["ho"][:R * Lg * H + 1]
-                kv_head_budgets(sub, ranked, b_dev, o_dev, hb, ho, slot["select_ws"], s_comp)
-                b_dev, o_dev = hb, ho
-            kv_select_topk(sub, ranked, b_dev, o_dev, slot["sel"], slot["select_ws"], s_comp)
-            kv_compact(sub, k, v, slot["sel"], o_dev, self.rows[g], slot["k_out"],
-                       slot["v_out"], s_comp)
+            if self.fused:
+                kv_evict_fused(sub, q, k, v, b_dev, o_dev, self.rows[g], scores, slot["sel"],
+                               slot["k_out"], slot["v_out"], slot["score_ws"], s_comp)
+            else:
+                self._evict_group(sub, q, k, v, scores, slot, b_dev, o_dev, g, s_comp)
             self.ev_comp[g & 1].record(s_comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(self.ev_comp[g & 1])

@@ -92,6 +92,7 @@ ScoreWs score_ws_layout(const DevProblem &P, void *base) {
     ws.a_hi = reinterpret_cast<__nv_bfloat16 *>(take(U * AR * D * sizeof(__nv_bfloat16)));
     ws.a_lo = reinterpret_cast<__nv_bfloat16 *>(take(U * AR * D * sizeof(__nv_bfloat16)));
     ws.plan = reinterpret_cast<int32_t *>(take((U + 1) * sizeof(int32_t)));
+    ws.plan2 = reinterpret_cast<int32_t *>(take((U + 1) * sizeof(int32_t)));
     const size_t keys = (size_t)P.L * P.H * (size_t)P.N_tot;
     ws.part_scores = reinterpret_cast<float *>(
         take(ws.chunks > 1 ? (size_t)ws.chunks * keys * sizeof(float) : 0));
@@ -280,6 +281,26 @@ kv_status kv_compact_blocks(const kv_problem *p, int32_t block_layers, const voi
                                           block_offsets_dev, offsets_dev, total_rows,
                                           (__nv_bfloat16 *)k_out, (__nv_bfloat16 *)v_out,
                                           (cudaStream_t)stream));
+}
+
+kv_status kv_evict_fused(const kv_problem *p, const void *q_win, const void *k, const void *v,
+                         const int32_t *budgets_dev, const int64_t *offsets_dev,
+                         int64_t total_rows, float *scores, int32_t *sel_idx, void *k_out,
+                         void *v_out, void *workspace, size_t workspace_bytes, void *stream) {
+    DevProblem P;
+    kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
+    if (st != KV_OK || P.units == 0) return st;
+    if (total_rows < 0 || !scores || !budgets_dev || !offsets_dev || !sel_idx)
+        return KV_ERR_INVALID_ARG;
+    if (total_rows > 0 && (!k_out || !v_out)) return KV_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(budgets_dev) || !aligned16(offsets_dev) ||
+        !aligned16(sel_idx) || (total_rows > 0 && (!aligned16(k_out) || !aligned16(v_out))))
+        return KV_ERR_INVALID_ARG;
+    ScoreWs ws = score_ws_layout(P, workspace);
+    return map_cuda(launch_fused(P, (const __nv_bfloat16 *)q_win, (const __nv_bfloat16 *)k,
+                                 (const __nv_bfloat16 *)v, budgets_dev, offsets_dev, total_rows,
+                                 scores, sel_idx, (__nv_bfloat16 *)k_out, (__nv_bfloat16 *)v_out,
+                                 ws, (cudaStream_t)stream));
 }
 
 kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const int32_t *sel_idx,

@@ -16,8 +16,11 @@ namespace kvevict {
 constexpr int kMaxRows = 512;
 // Keys per split of the pass-1 attention (each split writes one partial).
 constexpr int kSplitKeys = 32768;
-// Bytes reserved at the start of every workspace for the status word.
+// Bytes reserved at the start of every workspace for the status word (offset
+// 0); the score workspace also keeps the fused kernel's grid-barrier counter and
+// abort word in it (offsets kGridBarOffset and kGridBarOffset + 64).
 constexpr size_t kHeaderBytes = 256;
+constexpr size_t kGridBarOffset = 64;
 
 // Problem description passed by value to every kernel.
 struct DevProblem {
@@ -66,7 +69,8 @@ struct ScoreWs {
     float *stat_a2;           // [units][rows]  ||a_hi + a_lo||^2
     __nv_bfloat16 *a_hi;      // [units][a_rows][d]  bf16(a)
     __nv_bfloat16 *a_lo;      // [units][a_rows][d]  bf16(a - a_hi); rows >= rows are zero
-    int32_t *plan;            // [units + 1] pass-2 work plan
+    int32_t *plan;            // [units + 1] work plan of the pass being launched
+    int32_t *plan2;           // [units + 1] pass-2 plan of the fused kernel (both live)
     float *part_scores;       // [chunks][L*H*N_tot] when chunks > 1
     float *v2;                // [L*H*N_tot] ||v_j||^2 of every key (written by pass 1)
     int a_rows;               // chunks * 128
@@ -114,6 +118,12 @@ cudaError_t launch_select(const DevProblem &P, const float *scores, const int32_
 cudaError_t launch_compact(const DevProblem &P, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                            const int32_t *sel, const int64_t *offsets, long long total_rows,
                            __nv_bfloat16 *kout, __nv_bfloat16 *vout, cudaStream_t s);
+// Score -> select -> compaction in one cooperative launch (kv_fused.cu); the
+// select's status goes to the score workspace's status word.
+cudaError_t launch_fused(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                         const __nv_bfloat16 *v, const int32_t *budgets, const int64_t *offsets,
+                         long long total_rows, float *scores, int32_t *sel, __nv_bfloat16 *kout,
+                         __nv_bfloat16 *vout, const ScoreWs &ws, cudaStream_t s);
 
 __device__ inline void post_status(int *status, int code) {
     atomicCAS(status, 0, code);

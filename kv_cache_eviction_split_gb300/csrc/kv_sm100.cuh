@@ -23,6 +23,11 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
 
+// Ends an mbarrier's life, so its shared memory can hold other data.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -150,6 +155,26 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Warp 1 allocates all 512 TMEM columns of the SM (one CTA per SM) and
+// publishes the base through `slot` in shared memory; every thread of the CTA
+// calls this and gets the base.
+__device__ __forceinline__ uint32_t tmem_acquire_all(uint32_t *slot) {
+    if ((threadIdx.x >> 5) == 1) {
+        tmem_alloc(slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return *slot;
+}
+
+// Frees what tmem_acquire_all took; every thread calls it after a CTA barrier
+// that follows the last TMEM access.
+__device__ __forceinline__ void tmem_release_all(uint32_t tmem) {
+    if ((threadIdx.x >> 5) == 1) tmem_dealloc(tmem, 512);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs here), one thread issues.
@@ -318,6 +343,12 @@ __device__ __forceinline__ void tmem_st_wait() {
 // proxy (the tensor core reading them as an MMA operand).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with later async-proxy
+// (TMA) accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -48,10 +48,11 @@ def product_budgets(kv, wl, profile=None) -> np.ndarray:
 
 
 class DeviceRun:
-    """The three C-ABI calls on one workload, results kept on the device."""
+    """The three C-ABI calls (or, with fused=True, kv_evict_fused) on one workload,
+    results kept on the device."""
 
     def __init__(self, kv, wl, budgets=None, dw=None, score_rule=0, pool_kernel=1,
-                 head_budgets=False):
+                 head_budgets=False, fused=False):
         import torch
         from synth.device import DeviceWorkload
         self.wl = wl
@@ -66,10 +67,11 @@ class DeviceRun:
             budgets = product_budgets(kv, wl, prof)
         self.budgets = budgets
         self.bufs = kv.Buffers(self.prob, budgets)
-        kv.evict(self.prob, self.dw.q, self.dw.k, self.dw.v, self.bufs)
+        kv.evict(self.prob, self.dw.q, self.dw.k, self.dw.v, self.bufs, fused=fused)
         torch.cuda.synchronize()
         self.status_score = kv.kv_check_status(self.bufs.score_ws)
-        self.status_select = kv.kv_check_status(self.bufs.select_ws)
+        # the fused launch posts the selection's errors to the score workspace
+        self.status_select = self.status_score if fused else kv.kv_check_status(self.bufs.select_ws)
         # budgets and offsets selection and compaction used (per-head ones if computed)
         if head_budgets:
             self.eff_budgets = self.bufs.head_budgets.cpu().numpy().reshape(-1)

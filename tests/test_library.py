@@ -84,6 +84,36 @@ def test_score_argument_checks_before_launch(kv):
     assert lib.kv_compact(empty.c, None, None, None, None, 0, None, None, None) == kv.KV_OK
 
 
+def test_fused_argument_checks_before_launch(kv):
+    """kv_evict_fused validates like kv_score, kv_select_topk and kv_compact together,
+    before anything is launched."""
+    lib = kv.load()
+    p = _prob(kv)
+    ws = kv.kv_score_workspace_size(p)
+    f = 1 << 20  # never dereferenced: the checks fail first
+    call = lib.kv_evict_fused
+    ok_args = [p.c, f, f, f, f, f, 64, f, f, f, f, f, ws, None]
+
+    def with_(i, value):
+        a = list(ok_args)
+        a[i] = value
+        return call(*a)
+
+    assert with_(1, None) == kv.KV_ERR_INVALID_ARG        # q_win
+    assert with_(1, f + 4) == kv.KV_ERR_INVALID_ARG       # misaligned q_win
+    assert with_(12, ws - 1) == kv.KV_ERR_WORKSPACE       # score workspace too small
+    assert with_(4, None) == kv.KV_ERR_INVALID_ARG        # budgets
+    assert with_(5, None) == kv.KV_ERR_INVALID_ARG        # offsets
+    assert with_(6, -1) == kv.KV_ERR_INVALID_ARG          # total_rows
+    assert with_(7, None) == kv.KV_ERR_INVALID_ARG        # scores
+    assert with_(8, None) == kv.KV_ERR_INVALID_ARG        # sel_idx
+    assert with_(9, None) == kv.KV_ERR_INVALID_ARG        # k_out with rows to copy
+    assert with_(10, f + 2) == kv.KV_ERR_INVALID_ARG      # misaligned v_out
+    empty = _prob(kv, lengths=[])
+    assert call(empty.c, None, None, None, None, None, 0, None, None, None, None, None, 0,
+                None) == kv.KV_OK
+
+
 def test_make_offsets(kv):
     p = _prob(kv)
     b = np.array([36, 40, 100, 1000, 36, 2000, 37, 50], np.int32)
