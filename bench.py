@@ -61,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=9)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=0, help="oracle sample size (0: one per core)")
@@ -276,19 +276,20 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # DRAM bytes (read + write) per launch from single-pass ncu captures of the current
 # kernels (profiles/dram_traffic_long_32L_8kv_n131072.md and
 # profiles/launch_list_attn_sum_pool11_long_32L_8kv_n131072.md), keyed by
-# (workload, score rule, pool kernel, fused); None for any other combination.
+# (workload, score rule, pool kernel, fused); None for any other combination and for
+# kernels changed since their capture.
 TRAFFIC = {
     (DEFAULT_WORKLOAD, "dropkv", 1, False): {
-        "attn_tc_kernel": 17206489088 + 259797248,
-        "rescore_tc_kernel": 17581460992 + 267090688,
-        "select_kernel": 668124160 + 8176640,
-        "compact_kernel": 1731427840 + 1657543168},
+        "attn_tc_kernel": 17203870464 + 259486464,
+        "rescore_tc_kernel": 17602009088 + 267612160,
+        "select_kernel": 134189568 + 5159168,
+        "compact_kernel": 1731433216 + 1657850112},
+    (DEFAULT_WORKLOAD, "dropkv", 1, True): {
+        "fused_kernel": 37089416448 + 2378666752},
     (DEFAULT_WORKLOAD, "attn_sum", 11, False): {
         "attn_stats_kernel": 8607008000 + 4206336,
         "rescore_tc_kernel": 8636366848 + 266142208,
-        "pool_kernel": 134264320 + 84282624,
-        "select_kernel": 668098816 + 8056320,
-        "compact_kernel": 1731947776 + 1657752576},
+        "pool_kernel": 134264320 + 84282624},
 }
 
 
