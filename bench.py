@@ -272,7 +272,7 @@ LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "blocks": 1, "pool": 1, "head
                      "select": 1, "compact": 1}
 STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
                  "blocks": "block_sum_kernel", "pool": "pool_kernel", "heads": "hb_hist_kernel",
-                 "select": "select_kernel", "compact": "compact_kernel"}
+                 "select": "select_kernel", "compact": "compact_range_kernel"}
 # DRAM bytes (read + write) per launch from single-pass ncu captures of the current
 # kernels (profiles/dram_traffic_long_32L_8kv_n131072.md and
 # profiles/launch_list_attn_sum_pool11_long_32L_8kv_n131072.md), keyed by
@@ -281,9 +281,7 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 TRAFFIC = {
     (DEFAULT_WORKLOAD, "dropkv", 1, False): {
         "attn_tc_kernel": 17203870464 + 259486464,
-        "rescore_tc_kernel": 17602009088 + 267612160,
-        "select_kernel": 134189568 + 5159168,
-        "compact_kernel": 1731433216 + 1657850112},
+        "rescore_tc_kernel": 17602009088 + 267612160},
     (DEFAULT_WORKLOAD, "dropkv", 1, True): {
         "fused_kernel": 37089416448 + 2378666752},
     (DEFAULT_WORKLOAD, "attn_sum", 11, False): {

@@ -1,5 +1,6 @@
-// kv_compact.cu -- the stand-alone compaction kernels (compact_block in
-// kv_compact.cuh): the plain form and the block-eviction form.
+// kv_compact.cu -- the stand-alone compaction kernels: the plain form
+// (compact_rows over 1024-row ranges, one range per CTA) and the block-eviction
+// form (compact_block, kv_compact.cuh).
 #include "kv_compact.cuh"
 
 namespace kvevict {
@@ -7,6 +8,18 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kUnroll = 4;
+constexpr long long kRangeRows = 1024;   // output rows per CTA in the plain form
+constexpr int kRangeUnroll = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+compact_range_kernel(DevProblem P, const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                     const int32_t *__restrict__ sel, const int64_t *__restrict__ offsets,
+                     long long total_rows, uint4 *__restrict__ kout, uint4 *__restrict__ vout) {
+    const long long r0 = (long long)blockIdx.x * kRangeRows;
+    compact_rows<D, kWarps, kRangeUnroll>(P, k, v, sel, offsets, r0,
+                                          min(total_rows, r0 + kRangeRows), kout, vout);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -31,6 +44,16 @@ cudaError_t launch_compact_any(const DevProblem &P, const __nv_bfloat16 *k,
     auto vv = reinterpret_cast<const uint4 *>(v);
     auto ko = reinterpret_cast<uint4 *>(kout);
     auto vo = reinterpret_cast<uint4 *>(vout);
+    if (B.block_layers == 0) {
+        const long long ranges = (total_rows + kRangeRows - 1) / kRangeRows;
+        if (P.d == 64)
+            compact_range_kernel<64><<<(unsigned)ranges, kWarps * 32, 0, s>>>(
+                P, kk, vv, sel, offsets, total_rows, ko, vo);
+        else
+            compact_range_kernel<128><<<(unsigned)ranges, kWarps * 32, 0, s>>>(
+                P, kk, vv, sel, offsets, total_rows, ko, vo);
+        return cudaGetLastError();
+    }
     if (P.d == 64)
         compact_kernel<64><<<(unsigned)blocks, kWarps * 32, 0, s>>>(P, kk, vv, sel, offsets,
                                                                     total_rows, ko, vo, B);

@@ -11,8 +11,8 @@ __global__ void __launch_bounds__(kSelThreads)
 select_kernel(DevProblem P, const float *__restrict__ scores, const int32_t *__restrict__ budgets,
               const int64_t *__restrict__ offsets, int32_t *__restrict__ sel, int *status) {
     __shared__ unsigned smem[sel_smem_bytes<kSelThreads>() / 4];
-    select_unit<kSelThreads, false>(P, scores, budgets, offsets, sel, status, blockIdx.x,
-                                    sel_smem<kSelThreads>(smem));
+    select_unit<kSelThreads, false, 16>(P, scores, budgets, offsets, sel, status, blockIdx.x,
+                                        sel_smem<kSelThreads>(smem));
 }
 
 }  // namespace
