@@ -291,9 +291,11 @@ TRAFFIC = {
 }
 
 
-def stage_kernel(stage, rule):
+def stage_kernel(stage, rule, blk=0):
     if stage == "attention" and rule == SCORE_RULES["attn_sum"]:
         return "attn_stats_kernel"
+    if stage == "compact" and blk:
+        return "compact_kernel"      # the block-eviction form
     return STAGE_KERNELS[stage]
 
 
@@ -556,7 +558,7 @@ def main(argv=None):
             stage_ms.pop(s)
     dominant = max(stages, key=lambda s: stage_ms[s])
     roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule, blk)
-    kernel = "fused_kernel" if fused else stage_kernel(dominant, rule)
+    kernel = "fused_kernel" if fused else stage_kernel(dominant, rule, blk)
     traffic = None if heads or blk else \
         TRAFFIC.get((wl.name, args.score_rule, pool, fused), {}).get(kernel)
     roof.update({"kernel": kernel, "peak_source": peak_src,
