@@ -281,7 +281,9 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 TRAFFIC = {
     (DEFAULT_WORKLOAD, "dropkv", 1, False): {
         "attn_tc_kernel": 17203870464 + 259486464,
-        "rescore_tc_kernel": 17602009088 + 267612160},
+        "rescore_tc_kernel": 17602009088 + 267612160,
+        "select_kernel": 134215680 + 5091328,
+        "compact_range_kernel": 1731630592 + 1657701376},
     (DEFAULT_WORKLOAD, "dropkv", 1, True): {
         "fused_kernel": 37089416448 + 2378666752},
     (DEFAULT_WORKLOAD, "attn_sum", 11, False): {
