@@ -51,6 +51,16 @@ def test_fused_matches_separate_calls_bitwise(cuda_lib, wl, rule):
     _compare(sep, fus)
 
 
+@pytest.mark.parametrize("wl", [w for w in __import__("tests.test_gpu_parity",
+                                                      fromlist=["ROW_EDGES"]).ROW_EDGES],
+                         ids=lambda w: w.name)
+def test_fused_matches_separate_calls_row_edges(cuda_lib, wl):
+    sep = parity.DeviceRun(cuda_lib, wl)
+    fus = parity.DeviceRun(cuda_lib, wl, dw=sep.dw, fused=True)
+    assert sep.status_score == 0 and fus.status_score == 0
+    _compare(sep, fus)
+
+
 @pytest.mark.parametrize("wl", SMALL[1:], ids=lambda w: w.name)
 def test_fused_against_oracle_all_units(cuda_lib, wl):
     run = parity.DeviceRun(cuda_lib, wl, fused=True)

@@ -60,6 +60,29 @@ def test_head_dim_64_many_splits(cuda_lib):
     parity.check_units(run, list(range(wl.num_units)))
 
 
+# window-row counts at the edges of the 128-row chunking: the largest G*w the kernels
+# take (512 = four full chunks) at both head dims, and 129 rows (the second chunk holds
+# one row, padded to the 32-row MMA width)
+ROW_EDGES = [
+    synth.LLAMA8B_32K.scaled(name="rows512_d128_g8_w64", num_layers=1, num_kv_heads=2,
+                             num_q_heads=16, window=64, lengths=(3000,), ragged_range=None,
+                             num_heavy=8, budget_ratio=0.1),
+    synth.TINY.scaled(name="rows512_d64_g16_w32", num_kv_heads=1, num_q_heads=16, window=32,
+                      lengths=(2600,), budget_tokens=400),
+    synth.LLAMA8B_32K.scaled(name="rows129_d128_g3_w43", num_layers=1, num_kv_heads=2,
+                             num_q_heads=6, window=43, lengths=(2500, 1700), ragged_range=None,
+                             num_heavy=8, budget_ratio=0.1),
+]
+
+
+@pytest.mark.parametrize("wl", ROW_EDGES, ids=lambda w: w.name)
+def test_window_row_edges_all_units(cuda_lib, wl):
+    assert wl.rows in (512, 129)
+    run = _run(cuda_lib, wl)
+    res = parity.check_units(run, list(range(wl.num_units)))
+    assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
+
+
 @pytest.mark.parametrize("b_kind", ["minimum", "everything"])
 def test_budget_extremes(cuda_lib, b_kind):
     wl = synth.small_variant(synth.LLAMA8B_32K, 700, layers=1)
