@@ -69,17 +69,19 @@ def test_fused_against_oracle_all_units(cuda_lib, wl):
     assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
 
 
-def test_fused_full_size_long_context(cuda_lib):
-    """32 layers x 8 KV heads at n = 131072 (the measured workload): the fused launch
-    equals the separate calls on every output, and sampled units match the oracle."""
+@pytest.mark.parametrize("wl,count", [(synth.LLAMA8B_32K, 1), (synth.LONG_128K, 2),
+                                      (synth.QWEN7B_128K, 1), (synth.RAGGED_MISTRAL, 1)],
+                         ids=lambda x: getattr(x, "name", str(x)))
+def test_fused_full_size(cuda_lib, wl, count):
+    """Every full-size configuration: the fused launch equals the separate calls on every
+    output (scores, indices, packed K and V), and sampled units match the oracle."""
     import torch
-    wl = synth.LONG_128K
     sep = parity.DeviceRun(cuda_lib, wl)
     fus = parity.DeviceRun(cuda_lib, wl, dw=sep.dw, fused=True)
     assert fus.status_score == 0
     _compare(sep, fus)
     del sep
-    parity.check_units(fus, parity.sample_units(wl, 2, seed=91))
+    parity.check_units(fus, parity.sample_units(wl, count, seed=91))
     del fus
     torch.cuda.empty_cache()
 
