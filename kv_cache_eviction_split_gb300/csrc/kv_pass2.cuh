@@ -59,7 +59,7 @@ using namespace sm100;
 constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
 constexpr int kTilesPerItem = 64;
-constexpr int kPrefetchTiles = 4;   // K/V tiles requested into L2 ahead of the smem loads
+constexpr int kPrefetchTiles = 2;   // K/V tiles requested into L2 ahead of the smem loads
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
