@@ -60,7 +60,26 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
         }
         P->N_tot = p->seq_offsets_host[P->R];
     }
-    P->max_splits = (P->max_n + kSplitKeys - 1) / kSplitKeys;
+    // Splits of kSplitKeys keys, halved (down to kMinSplitKeys) while the pass-1 work items
+    // -- splits over all units times the row-chunk pairs -- would leave fewer than
+    // kSplitItemsPerSm per SM: with one split per unit, the last round of a persistent
+    // grid runs part-empty.  The choice depends on the shapes only, so workspace sizes
+    // are known on the host.
+    const int chunks = (P->rows + 127) / 128;
+    const long long pairs = chunks == 1 ? 1 : (chunks + 1) / 2;
+    auto items = [&](long long split) {
+        long long per_layer_head = 0;
+        for (int r = 0; r < P->R; ++r) {
+            const long long n = p->seq_offsets_host[r + 1] - p->seq_offsets_host[r];
+            per_layer_head += (n + split - 1) / split;
+        }
+        return per_layer_head * P->L * P->H * pairs;
+    };
+    P->split_keys = kSplitKeys;
+    while (P->split_keys > kMinSplitKeys &&
+           items(P->split_keys) < (long long)kSplitItemsPerSm * kSplitSms)
+        P->split_keys /= 2;
+    P->max_splits = (int)((P->max_n + P->split_keys - 1) / P->split_keys);
     return KV_OK;
 }
 

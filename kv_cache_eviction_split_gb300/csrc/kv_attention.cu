@@ -41,7 +41,7 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     if (!make_tile_map(&mq, q, q_rows, D) || !make_tile_map(&mk, k, kv_rows, D) ||
         !make_tile_map(&mv, v, kv_rows, D))
         return cudaErrorInvalidValue;
-    launch_plan(P, kSplitKeys, ws.plan, st);
+    launch_plan(P, P.split_keys, ws.plan, st);
     AttnArgs A;
     A.plan = ws.plan;
     A.part_ml = ws.part_ml;
@@ -50,7 +50,7 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     A.chunks = ws.chunks;
     A.parts = ws.parts;
     A.pairs = ws.parts == 1 ? (ws.chunks + 1) / 2 : 1;
-    A.total_items = total_blocks(P, kSplitKeys) * A.pairs;
+    A.total_items = total_blocks(P, P.split_keys) * A.pairs;
     A.status = ws.status;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);

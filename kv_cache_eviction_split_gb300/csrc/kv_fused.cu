@@ -201,7 +201,7 @@ fused_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
 
     // 0. work plans
     if (cta == 0 && warp < 2)
-        plan_warp(P, warp == 0 ? kSplitKeys : pass2::kTileKeys * pass2::kTilesPerItem,
+        plan_warp(P, warp == 0 ? P.split_keys : pass2::kTileKeys * pass2::kTilesPerItem,
                   warp == 0 ? F.ws.plan : F.ws.plan2);
     bool ok = barrier();
     // 1. pass 1
@@ -276,7 +276,7 @@ cudaError_t fused_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bflo
     F.a1.chunks = ws.chunks;
     F.a1.parts = ws.parts;
     F.a1.pairs = ws.parts == 1 ? (ws.chunks + 1) / 2 : 1;
-    F.a1.total_items = total_blocks(P, kSplitKeys) * F.a1.pairs;
+    F.a1.total_items = total_blocks(P, P.split_keys) * F.a1.pairs;
     F.a1.status = ws.status;
     F.a2.plan = ws.plan2;
     F.a2.stat_ml = ws.stat_ml;

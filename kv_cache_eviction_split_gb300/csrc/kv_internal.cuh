@@ -14,8 +14,13 @@ namespace kvevict {
 
 // Largest R = G * w the kernels accept.
 constexpr int kMaxRows = 512;
-// Keys per split of the pass-1 attention (each split writes one partial).
+// Keys per split of the pass-1 attention (each split writes one partial): at most
+// kSplitKeys, chosen per problem (DevProblem::split_keys).
 constexpr int kSplitKeys = 32768;
+constexpr int kMinSplitKeys = 4096;
+// Work items per SM the split choice aims for, and the SM count it assumes (GB300).
+constexpr int kSplitItemsPerSm = 4;
+constexpr int kSplitSms = 152;
 // Bytes reserved at the start of every workspace for the status word (offset
 // 0); the score workspace also keeps the fused kernel's grid-barrier counter and
 // abort word in it (offsets kGridBarOffset and kGridBarOffset + 64).
@@ -28,7 +33,8 @@ struct DevProblem {
     int rule;                 // kv_score_rule
     int rows;                 // G * w
     int max_n;                // longest request
-    int max_splits;           // ceil(max_n / kSplitKeys)
+    int split_keys;           // keys per pass-1 split (a power of two, 4096..32768)
+    int max_splits;           // ceil(max_n / split_keys)
     long long N_tot;          // packed tokens
     long long units;          // R * L * H
     const long long *cu;      // device cu_seqlens [R + 1]

@@ -32,7 +32,7 @@ __device__ __forceinline__ void merge_row(const DevProblem &P, const ScoreWs &ws
     }
     if (!kO && row >= P.rows) return;
     const UnitInfo U = unit_info(P, u, P.cu);
-    const int nslots = (U.n + kSplitKeys - 1) / kSplitKeys * ws.parts;
+    const int nslots = (U.n + P.split_keys - 1) / P.split_keys * ws.parts;
     const size_t base = (size_t)u * P.max_splits * ws.parts * P.rows + row;
 
     // partials with l = 0 saw no key of this row (or no tile at all): skipped.

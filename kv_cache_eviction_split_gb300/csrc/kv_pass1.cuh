@@ -39,7 +39,7 @@
 // warp 1 TMEM owner and MMA issuer; warps 2-5 softmax of lane 0, 6-9 of lane 1;
 // warps 10-11 convert every V tile to fp16 as it lands (and compute ||v_j||^2),
 // so neither lane's softmax waits for V or for the other lane.
-// Work items are (unit, 32768-key split, chunk pair), walked round-robin by a
+// Work items are (unit, key split of up to 32768 keys, chunk pair), walked round-robin by a
 // persistent grid.  All waits are bounded (KV_ERR_TIMEOUT on expiry).
 //
 // The passes are written as device bodies (attn_tc_body, attn_stats_body) that
@@ -113,8 +113,8 @@ __device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, c
     const int r = (int)(lo / ((long long)P.L * P.H));
     const int n = (int)(P.cu[r + 1] - P.cu[r]);
     it.split = (int)(gs - A.plan[lo]);
-    const int k0 = it.split * kSplitKeys;
-    const int k1 = min(n, k0 + kSplitKeys);
+    const int k0 = it.split * P.split_keys;
+    const int k1 = min(n, k0 + P.split_keys);
     it.t0 = k0 / kTileKeys;
     it.t1 = (k1 + kTileKeys - 1) / kTileKeys;
     return it;
