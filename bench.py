@@ -280,12 +280,12 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # kernels changed since their capture.
 TRAFFIC = {
     (DEFAULT_WORKLOAD, "dropkv", 1, False): {
-        "attn_tc_kernel": 17203870464 + 259486464,
-        "rescore_tc_kernel": 17602009088 + 267612160,
-        "select_kernel": 134215680 + 5091328,
-        "compact_range_kernel": 1731630592 + 1657701376},
+        "attn_tc_kernel": 17204449792 + 259715328,
+        "rescore_tc_kernel": 17442629632 + 267109888,
+        "select_kernel": 134189824 + 5070080,
+        "compact_range_kernel": 1731816704 + 1657687552},
     (DEFAULT_WORKLOAD, "dropkv", 1, True): {
-        "fused_kernel": 37089416448 + 2378666752},
+        "fused_kernel": 36898065920 + 2378559744},
     (DEFAULT_WORKLOAD, "attn_sum", 11, False): {
         "attn_stats_kernel": 8607008000 + 4206336,
         "rescore_tc_kernel": 8636366848 + 266142208,
