@@ -62,3 +62,31 @@ def test_random_shapes(cuda_lib, seed):
     assert torch.equal(sep.bufs.sel[:n], fus.bufs.sel[:n])
     assert torch.equal(sep.bufs.k_out[:n].view(torch.int16), fus.bufs.k_out[:n].view(torch.int16))
     assert torch.equal(sep.bufs.v_out[:n].view(torch.int16), fus.bufs.v_out[:n].view(torch.int16))
+
+
+@pytest.mark.parametrize("seed", range(0, CASES, 2))
+def test_random_shapes_pooling_and_head_budgets(cuda_lib, seed):
+    """The same shapes with max pooling of a random odd width before the selection and, on
+    every other case, per-head budgets: pooled scores, the heads' budgets (against the
+    oracle's allocation over the GPU's ranked scores), selection and compaction."""
+    import oracle
+    wl, budgets, rule = _case(seed)
+    rng = np.random.default_rng(5000 + seed)
+    kernel = int(rng.choice([1, 3, 5, 11, 13, 31]))
+    heads = bool(seed % 4 == 0)
+    run = parity.DeviceRun(cuda_lib, wl, budgets=budgets, score_rule=rule, pool_kernel=kernel,
+                           head_budgets=heads)
+    assert run.status_score == 0 and run.status_select == 0, wl.name
+    if heads:
+        ranked = run.ranked_scores()
+        H, w, s = wl.num_kv_heads, wl.window, wl.num_sinks
+        inb = np.asarray(budgets).reshape(-1)
+        cu = run.dw.cu_host
+        for r in range(wl.num_requests):
+            for l in range(wl.num_layers):
+                u0 = wl.unit_index(r, l, 0)
+                S = ranked[l, :, int(cu[r]):int(cu[r + 1])].astype(np.float64)
+                want = oracle.head_budgets(S, w, s, inb[u0:u0 + H])
+                np.testing.assert_array_equal(run.eff_budgets[u0:u0 + H], want, err_msg=wl.name)
+        np.testing.assert_array_equal(run.eff_offsets, oracle.offsets(run.eff_budgets))
+    parity.check_units(run, list(range(wl.num_units)))
