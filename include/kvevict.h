@@ -121,7 +121,11 @@ kv_status kv_score_workspace_size(const kv_problem *p, size_t *bytes);
  * Full scoring step: kv_score_attention then kv_score_rescore on one stream.
  * scores receives one fp32 score per key of every unit under p->score_rule,
  * >= 0 (the two DropKV rules give +inf when a window row puts all of its
- * attention on one key; the attention sum is at most G * w).
+ * attention on one key; the attention sum is at most G * w).  Results are
+ * deterministic for a given problem.  The key-split size of the attention pass
+ * is chosen from the whole problem's shape (enough work items for every SM), so
+ * the same unit scored inside a problem of another shape may differ in the last
+ * bits (within the stated tolerance of the exact score).
  */
 kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const void *v,
                    float *scores, void *workspace, size_t workspace_bytes, void *stream);
