@@ -109,7 +109,8 @@ typedef struct kv_problem {
     int32_t window;                  /* w >= 1 */
     int32_t num_sinks;               /* s >= 0 (4 in the method) */
     int32_t score_rule;              /* kv_score_rule (0: the DropKV score) */
-    const int64_t *seq_offsets_host; /* [R+1] cu_seqlens, host memory; n_r >= s + w, n_r < 2^31 */
+    const int64_t *seq_offsets_host; /* [R+1] cu_seqlens, host memory; n_r >= s + w, n_r < 2^31;
+                                        L*H*N_tot and R*L*H_q*w below 2^31 (KV_ERR_UNSUPPORTED) */
     const int64_t *seq_offsets_dev;  /* the same [R+1] values, device memory */
     float softmax_scale;             /* logit scale, normally 1/sqrt(d); > 0 */
 } kv_problem;

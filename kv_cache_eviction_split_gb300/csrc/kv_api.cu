@@ -60,6 +60,13 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
         }
         P->N_tot = p->seq_offsets_host[P->R];
     }
+    // TMA tile coordinates are 32-bit: the packed K/V rows, the window query rows
+    // and pass 2's rows of a must each stay below 2^31.
+    const long long kRowLimit = 1LL << 31;
+    if ((long long)P->L * P->H * P->N_tot >= kRowLimit ||
+        (long long)P->R * P->L * P->Hq * P->w >= kRowLimit ||
+        P->units * (long long)((P->rows + 127) / 128 * 128) >= kRowLimit)
+        return KV_ERR_UNSUPPORTED;
     // Splits of kSplitKeys keys, halved (down to kMinSplitKeys) while the pass-1 work items
     // -- splits over all units times the row-chunk pairs -- would leave fewer than
     // kSplitItemsPerSm per SM: with one split per unit, the last round of a persistent

@@ -63,7 +63,10 @@ def test_workspace_size_and_shape_checks(kv):
                       (dict(num_q_heads=7), kv.KV_ERR_INVALID_ARG),
                       (dict(window=0), kv.KV_ERR_INVALID_ARG),
                       (dict(lengths=[20, 2000]), kv.KV_ERR_INVALID_ARG),
-                      (dict(num_q_heads=2 * 17, window=32), kv.KV_ERR_UNSUPPORTED)]:
+                      (dict(num_q_heads=2 * 17, window=32), kv.KV_ERR_UNSUPPORTED),
+                      # 2^31 packed K/V rows: beyond the 32-bit TMA row coordinates
+                      (dict(lengths=[1 << 30, 1 << 30], num_layers=1, num_kv_heads=1,
+                            num_q_heads=4), kv.KV_ERR_UNSUPPORTED)]:
         with pytest.raises(kv.KvError) as e:
             kv.kv_score_workspace_size(_prob(kv, **bad))
         assert e.value.code == code, bad
