@@ -54,3 +54,33 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.whole_job_rate(500.0, 1, 2.0) == 250000.0
+
+
+def test_roofline_accounting():
+    """The algorithmic bytes bench.py divides by: per-stage formulas from the workload's
+    shapes and budgets, and the fused launch as the sum of its four steps."""
+    import numpy as np
+    import bench
+    import synth
+    wl = synth.BY_NAME["long_32L_8kv_32q_d128_n131072_pyramid10"]
+    L, H, d, n = wl.num_layers, wl.num_kv_heads, wl.head_dim, wl.seq_lengths()[0]
+    budgets = np.full((1, L, H), 13107, dtype=np.int32)
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1700.0}
+    kv_bytes = L * H * n * d * 2 * 2
+    q_bytes = L * wl.num_q_heads * wl.window * d * 2
+    att = bench.stage_roofline("attention", 1.0, wl, budgets, peaks)
+    assert att["algorithmic_bytes"] == kv_bytes + q_bytes
+    res = bench.stage_roofline("rescore", 1.0, wl, budgets, peaks)
+    assert res["algorithmic_bytes"] == kv_bytes + q_bytes + L * H * n * 4
+    # achieved GB/s = bytes / time; frac against the given peak
+    assert abs(att["achieved"] - att["algorithmic_bytes"] / 1e-3 / 1e9) < 1e-6 * att["achieved"]
+    assert abs(att["frac"] - att["achieved"] / 6000.0) < 1e-12
+    fused = bench.stage_roofline("fused", 1.0, wl, budgets, peaks)
+    parts = [bench.stage_roofline(s, 1.0, wl, budgets, peaks)
+             for s in ("attention", "rescore", "select", "compact")]
+    assert fused["algorithmic_bytes"] == sum(p["algorithmic_bytes"] for p in parts)
+    assert fused["tensor"]["algorithmic_flops"] == \
+        att["tensor"]["algorithmic_flops"] + res["tensor"]["algorithmic_flops"]
+    # the attention sum reads K only
+    att2 = bench.stage_roofline("attention", 1.0, wl, budgets, peaks, rule=2)
+    assert att2["algorithmic_bytes"] == kv_bytes // 2 + q_bytes
