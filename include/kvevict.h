@@ -67,8 +67,15 @@
  * return KV_ERR_INVALID_ARG / KV_ERR_BUDGET / KV_ERR_WORKSPACE /
  * KV_ERR_UNSUPPORTED.  A failed launch returns KV_ERR_CUDA.  Conditions only
  * the device can see (a budget in device memory out of range, an offsets table
- * that disagrees with the budgets) are written to a status word in the
- * workspace; kv_check_status reads it.
+ * that disagrees with the budgets, a V value fp16 cannot carry, a bounded wait
+ * that expired) are written to a status word in the workspace header;
+ * kv_check_status reads it.  A workspace needs no initialisation: its first
+ * 256 bytes are a header whose first int32 is the status word, and each call
+ * that starts a sequence on the workspace zeroes that word (an in-stream memset
+ * before its first kernel): kv_score_attention (so kv_score), kv_evict_fused,
+ * kv_select_topk and kv_head_budgets.  kv_score_rescore adds to the word of the
+ * kv_score_attention it follows.  The word keeps the first code posted to it
+ * until the next such call or kv_check_status.
  *
  * Pointers: device pointers must be 16-byte aligned.  `stream` is a
  * cudaStream_t (NULL = legacy default stream).
@@ -134,16 +141,24 @@ kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const 
 /*
  * Pass 1: causal window attention of every unit with split-K over the keys and
  * a merge of the splits (row max, row sum and a = sum p v); leaves them in the
- * workspace for pass 2.  The product p v runs with p and v in fp16: V values
- * must be finite and below 65504 in magnitude (bf16 values in that range
- * convert exactly down to 6.1e-5; smaller magnitudes keep an absolute error
- * below 3e-8).  A larger value posts KV_ERR_UNSUPPORTED to the status word.
+ * workspace for pass 2.  Starts a new status sequence (zeroes status word 0).
+ * The product p v runs with p and v in fp16: V values must be finite and below
+ * 65504 in magnitude (bf16 values in that range convert exactly down to
+ * 2^-14 = 6.1e-5; smaller magnitudes keep an absolute error below 3e-8).  A
+ * larger value posts KV_ERR_UNSUPPORTED to the status word, and so does a block
+ * of 64 V rows as the kernel reads them (64-aligned within the unit; the block
+ * at a unit's end also holds the rows that follow it in memory) whose values
+ * are not all zero but all below 2^-14 in magnitude, where fp16 keeps too few
+ * bits for the score's tolerance (V scaled far below the usual range).  Rules
+ * that do not read V (KV_SCORE_ATTN_SUM) have neither limit.
  */
 kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void *k,
                              const void *v, void *workspace, size_t workspace_bytes,
                              void *stream);
 
-/* Pass 2: rescoring of every key from the pass-1 results in the workspace. */
+/* Pass 2: rescoring of every key from the pass-1 results in the workspace.  Its
+ * device status (a wait that expired) is added to the status word of the
+ * kv_score_attention it follows; the word is not zeroed here. */
 kv_status kv_score_rescore(const kv_problem *p, const void *q_win, const void *k,
                            const void *v, float *scores, void *workspace,
                            size_t workspace_bytes, void *stream);
@@ -182,7 +197,8 @@ kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes);
  * ordering compares the fp32 bit patterns, exact for values >= 0).
  * budgets_dev / offsets_dev: device copies of the tables above.  A budget
  * that is out of range, or disagrees with offsets, leaves its unit untouched
- * and posts KV_ERR_BUDGET to the workspace status word.
+ * and posts KV_ERR_BUDGET to the select workspace's status word (zeroed at the
+ * start of the call).
  */
 kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
                          const int64_t *offsets_dev, int32_t *sel_idx, void *workspace,
@@ -203,9 +219,12 @@ kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t
  * scores: as kv_score (or kv_pool_scores) writes them; budgets_dev, offsets_dev:
  * device [R*L*H] and [R*L*H + 1] as for kv_select_topk; outputs: device arrays
  * of the same sizes, distinct from the inputs.  workspace: at least
- * kv_select_workspace_size bytes (its status word is kv_select_topk's; the rest
- * is scratch).  A layer whose input budgets are out of range or
- * disagree with offsets_dev gets them copied through and posts KV_ERR_BUDGET.
+ * kv_select_workspace_size bytes (its status word is zeroed at the start of
+ * the call; after the header, scratch).  A layer whose input budgets are out of
+ * range or disagree with offsets_dev gets them copied through and posts
+ * KV_ERR_BUDGET; the kv_select_topk that takes these outputs then fails the same
+ * check on the same unit and posts KV_ERR_BUDGET again, so one kv_check_status
+ * after the selection sees the error.
  * H * max n_r must be below 2^32 (KV_ERR_UNSUPPORTED otherwise).
  */
 kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
@@ -309,14 +328,21 @@ kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status)
  *
  *  - Problems whose kv_score workspace (kv_score_workspace_size) exceeds
  *    64 MiB return KV_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture.
+ *  - The first call in each CUDA context (per device, and again after
+ *    cudaDeviceReset or when another context is made current) looks up the
+ *    array's device address with that context current, and later calls in
+ *    the same context reuse it (keyed on the context's unique ID); make the
+ *    first call of a context before any stream capture.
  *  - Every call shares the array and it keeps the last call's contents;
  *    calls that overlap on the GPU (other streams or host threads on the same
  *    device) race on it, so order them on one stream.
- *  - Device-side status (a bounded wait that expired) is written into the
- *    shared array and not reported; argument and launch errors are returned.
+ *  - Argument and launch errors are returned.  The device-side status that
+ *    kv_score posts to its workspace (kv_check_status) lands in the shared
+ *    array and is not reported here: a wait that expired (KV_ERR_TIMEOUT) and
+ *    V values outside what pass 1 carries in fp16 (KV_ERR_UNSUPPORTED: |v| of
+ *    65504 or more, or 64-row blocks of values all below 2^-14; see
+ *    kv_score_attention) then leave wrong scores without an error.  Callers
+ *    whose V may leave that range should use kv_score with a workspace.
  */
 kv_status kv_score_noalloc(const kv_problem *p, const void *q_win, const void *k,
                            const void *v, float *scores, void *stream);

@@ -170,6 +170,10 @@ kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void 
     kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
     if (st != KV_OK || P.units == 0) return st;
     ScoreWs ws = score_ws_layout(P, workspace);
+    // a new scoring sequence: its status word starts at zero (the workspace may be
+    // uninitialised memory)
+    if (cudaMemsetAsync(ws.status, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+        return KV_ERR_CUDA;
     return map_cuda(launch_attention(P, (const __nv_bfloat16 *)q_win, (const __nv_bfloat16 *)k,
                                      (const __nv_bfloat16 *)v, ws, (cudaStream_t)stream));
 }
@@ -248,8 +252,11 @@ kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t
         !aligned16(sel_idx) || !aligned16(workspace))
         return KV_ERR_INVALID_ARG;
     if (workspace_bytes < kHeaderBytes) return KV_ERR_WORKSPACE;
-    return map_cuda(launch_select(P, scores, budgets_dev, offsets_dev, sel_idx,
-                                  static_cast<int *>(workspace), (cudaStream_t)stream));
+    int *status = static_cast<int *>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+        return KV_ERR_CUDA;
+    return map_cuda(launch_select(P, scores, budgets_dev, offsets_dev, sel_idx, status,
+                                  (cudaStream_t)stream));
 }
 
 kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
@@ -269,8 +276,14 @@ kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_
     if (workspace_bytes < kHeaderBytes + head_budget_ws_bytes(P)) return KV_ERR_WORKSPACE;
     // the layer-wide counts are 32-bit
     if ((long long)P.H * P.max_n >= (1LL << 32)) return KV_ERR_UNSUPPORTED;
+    // a layer whose budgets fail the check is copied through unchanged, so the
+    // kv_select_topk that takes these outputs (and zeroes the word again) fails the
+    // same check on the same unit and posts KV_ERR_BUDGET once more
+    int *status = static_cast<int *>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+        return KV_ERR_CUDA;
     return map_cuda(launch_head_budgets(P, scores, budgets_dev, offsets_dev, budgets_out_dev,
-                                        offsets_out_dev, static_cast<int *>(workspace),
+                                        offsets_out_dev, status,
                                         static_cast<char *>(workspace) + kHeaderBytes,
                                         (cudaStream_t)stream));
 }

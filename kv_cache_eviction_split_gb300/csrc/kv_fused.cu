@@ -300,7 +300,8 @@ cudaError_t fused_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bflo
     F.vout = reinterpret_cast<uint4 *>(vout);
     F.total_rows = total_rows;
     F.bar = reinterpret_cast<unsigned *>(reinterpret_cast<char *>(ws.status) + kGridBarOffset);
-    cudaError_t e = cudaMemsetAsync(F.bar, 0, 2 * 64, st);
+    // the whole header: the status word (a new sequence) and the barrier words
+    cudaError_t e = cudaMemsetAsync(ws.status, 0, kHeaderBytes, st);
     if (e != cudaSuccess) return e;
 
     auto kern = fused_kernel<D, RULE>;

@@ -21,9 +21,13 @@ constexpr int kMinSplitKeys = 4096;
 // Work items per SM the split choice aims for, and the SM count it assumes (GB300).
 constexpr int kSplitItemsPerSm = 4;
 constexpr int kSplitSms = 152;
-// Bytes reserved at the start of every workspace for the status word (offset
-// 0); the score workspace also keeps the fused kernel's grid-barrier counter and
-// abort word in it (offsets kGridBarOffset and kGridBarOffset + 64).
+// Bytes reserved at the start of every workspace for the status word (int32 at
+// offset 0); the score workspace also keeps the fused kernel's grid-barrier
+// counter and abort word in it (offsets kGridBarOffset and kGridBarOffset + 64).
+// The calls that start a sequence on a workspace zero the status word in-stream
+// before their first kernel (kv_score_attention, kv_evict_fused,
+// kv_select_topk, kv_head_budgets); kv_score_rescore keeps adding to the word of
+// the kv_score_attention it follows.
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kGridBarOffset = 64;
 

@@ -194,9 +194,13 @@ __device__ __forceinline__ void sq_acc_bf16x2(float &acc, uint32_t w) {
 // Converts half of one key row of a swizzled [128][D] bf16 tile (`row`, 16-byte
 // chunks [half * D/16, (half + 1) * D/16) across the 64-column blocks) to fp16 in
 // place, and returns the sum of the squares of its bf16 values; `bad` is set if
-// a value overflowed fp16.
+// a value overflowed fp16.  `nz` collects the magnitude bits of the bf16 inputs
+// and `nrm` the exponent bits of the fp16 outputs, so that the caller can tell
+// a block of rows whose values are nonzero but all below fp16's normal range
+// (2^-14), where fp16 keeps only a few of their bits.
 template <int D>
-__device__ __forceinline__ float row_half_to_f16(uint8_t *tile, int row, int half, bool &bad) {
+__device__ __forceinline__ float row_half_to_f16(uint8_t *tile, int row, int half, bool &bad,
+                                                 uint32_t &nz, uint32_t &nrm) {
     constexpr int kChunks = D / 16;            // 16-byte chunks per half row
     float acc[2] = {0.f, 0.f};
     uint32_t over = 0;
@@ -213,6 +217,8 @@ __device__ __forceinline__ float row_half_to_f16(uint8_t *tile, int row, int hal
             sq_acc_bf16x2(acc[k & 1], in[k]);
             o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xFFFF0000u));
             over |= ((o[k] & 0x7C00u) == 0x7C00u) | ((o[k] & 0x7C000000u) == 0x7C000000u);
+            nz |= in[k] & 0x7FFF7FFFu;
+            nrm |= o[k] & 0x7C007C00u;
         }
         *g = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -634,15 +640,20 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                 if (!ok) break;
                 uint8_t *tile = smem + Ly::kV + s * Ly::kOp;
                 bool bad = false;
+                uint32_t nz = 0, nrm = 0;
 #pragma unroll 1
                 for (int k0 = 0; k0 < 64; k0 += 16) {
                     const int row = cw * 64 + k0 + (lane & 15);
-                    float q = row_half_to_f16<D>(tile, row, lane >> 4, bad);
+                    float q = row_half_to_f16<D>(tile, row, lane >> 4, bad, nz, nrm);
                     q += __shfl_xor_sync(0xffffffffu, q, 16);
                     const int j = (it.t0 + ti) * kTileKeys + row;   // key of the unit
                     if (lane < 16 && j < U.n) A.v2[U.kv_row0 + j] = q;
                 }
-                if (bad) post_status(A.status, KV_ERR_UNSUPPORTED);
+                // refused: a value fp16 cannot hold, or 64 rows of nonzero values that
+                // all fall below 2^-14 (fp16 subnormals keep too few of their bits)
+                const bool tiny = __any_sync(0xffffffffu, nz != 0) &&
+                                  !__any_sync(0xffffffffu, nrm != 0);
+                if (bad || (tiny && lane == 0)) post_status(A.status, KV_ERR_UNSUPPORTED);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&v_conv[s]);
