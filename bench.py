@@ -61,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=9)
+    ap.add_argument("--e2e-steps", type=int, default=21)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=0, help="oracle sample size (0: one per core)")
@@ -273,24 +273,36 @@ LAUNCHES_PER_STEP = {"attention": 3, "rescore": 2, "blocks": 1, "pool": 1, "head
 STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
                  "blocks": "block_sum_kernel", "pool": "pool_kernel", "heads": "hb_hist_kernel",
                  "select": "select_kernel", "compact": "compact_range_kernel"}
-# DRAM bytes (read + write) per launch from single-pass ncu captures of the current
-# kernels (profiles/dram_traffic_long_32L_8kv_n131072.md and
-# profiles/launch_list_attn_sum_pool11_long_32L_8kv_n131072.md), keyed by
-# (workload, score rule, pool kernel, fused); None for any other combination and for
-# kernels changed since their capture.
-TRAFFIC = {
-    (DEFAULT_WORKLOAD, "dropkv", 1, False): {
-        "attn_tc_kernel": 17204449792 + 259715328,
-        "rescore_tc_kernel": 17442629632 + 267109888,
-        "select_kernel": 134189824 + 5070080,
-        "compact_range_kernel": 1731816704 + 1657687552},
-    (DEFAULT_WORKLOAD, "dropkv", 1, True): {
-        "fused_kernel": 36898065920 + 2378559744},
-    (DEFAULT_WORKLOAD, "attn_sum", 11, False): {
-        "attn_stats_kernel": 8607008000 + 4206336,
-        "rescore_tc_kernel": 8636366848 + 266142208,
-        "pool_kernel": 134264320 + 84282624},
-}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a stage's
+# kernel at full size, keyed by (workload, score rule, pool kernel, fused).  Each
+# entry records the kernel sources it was measured on ("src": kernel_source_hash()
+# at capture time), the ncu case it came from and the factor that scales that
+# case to the full workload; bench reports traffic as null once the sources differ.
+TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    """sha256 (first 16 hex digits) of the CUDA sources of the library."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_cache_eviction_split_gb300", "csrc")
+    for path in sorted(glob.glob(os.path.join(csrc, "*.cu")) +
+                       glob.glob(os.path.join(csrc, "*.cuh"))):
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(key, kernel):
+    """(bytes per launch, provenance) of `kernel`, or (None, reason)."""
+    entry = TRAFFIC.get(key)
+    if entry is None or kernel not in entry["bytes"]:
+        return None, "no ncu capture for this workload and kernel"
+    if entry["src"] != kernel_source_hash():
+        return None, "kernel sources changed since the ncu capture (%s)" % entry["src"]
+    return entry["bytes"][kernel], "ncu, %s, x%g" % (entry["case"], entry["scale"])
 
 
 def stage_kernel(stage, rule, blk=0):
@@ -335,15 +347,19 @@ def stage_roofline(stage, ms, wl, budgets, peaks, rule=0, blk=1):
     (window row, visible key) pair each, one for the attention sum, which needs
     only q.k).  The attention sum needs no V: its passes read K only."""
     if stage == "fused":
-        # the fused kernel runs the phases of all four: their bytes and flops add up
+        # the fused kernel is the whole path: its roofline counts every byte once
+        # (K+V, the window queries, the kept rows and indices, the offsets), the
+        # headline basis; the sum of its phases' own bytes (K+V twice, the scores
+        # written and read) is kept beside it as phase_bytes
         parts = [stage_roofline(s, ms, wl, budgets, peaks, rule, blk)
                  for s in ("attention", "rescore", "select", "compact")]
-        nbytes = sum(p["algorithmic_bytes"] for p in parts)
+        nbytes = algorithmic_bytes(wl, budgets)
         flops = sum(p["tensor"]["algorithmic_flops"] for p in parts if "tensor" in p)
         achieved = nbytes / (ms * 1e-3) / 1e9
         tpeak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                "phase_bytes": sum(p["algorithmic_bytes"] for p in parts),
                 "tensor": {"algorithmic_flops": flops,
                            "achieved_tflops": flops / (ms * 1e-3) / 1e12, "peak_tflops": tpeak,
                            "frac": flops / (ms * 1e-3) / 1e12 / tpeak}}
@@ -561,10 +577,13 @@ def main(argv=None):
     dominant = max(stages, key=lambda s: stage_ms[s])
     roof = stage_roofline(dominant, stage_ms[dominant], wl, budgets, peaks, rule, blk)
     kernel = "fused_kernel" if fused else stage_kernel(dominant, rule, blk)
-    traffic = None if heads or blk else \
-        TRAFFIC.get((wl.name, args.score_rule, pool, fused), {}).get(kernel)
+    if heads or blk:
+        traffic, traffic_src = None, "no ncu capture for per-head budgets or block eviction"
+    else:
+        traffic, traffic_src = measured_traffic((wl.name, args.score_rule, pool, fused), kernel)
     roof.update({"kernel": kernel, "peak_source": peak_src,
-                 "traffic": traffic, "stage_ms": stage_ms[dominant],
+                 "traffic": traffic, "traffic_source": traffic_src,
+                 "kernel_source_hash": kernel_source_hash(), "stage_ms": stage_ms[dominant],
                  "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
                                                   rule, blk)["frac"] for s in stages}})
 
@@ -622,7 +641,8 @@ def main(argv=None):
 def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=None, budgets=None):
     """Same metric through the public API with host buffers: pinned host Q/K/V
     copied in, scored, selected and compacted, the kept indices and packed K/V
-    copied out.  kv.HostPipeline overlaps the copies of one layer group with the
+    copied out.  The C entry point kv_evict_host (through kv.HostPipeline, which
+    only allocates its buffers) overlaps the copies of one layer group with the
     work on another; block eviction copies everything in, then runs."""
     if bb is None:
         try:
@@ -642,7 +662,7 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
                 "ms_per_step_min_max": spread,
                 "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
                 "steps": args.e2e_steps, "statistic": "median of per-step host wall times",
-                "api": "kv.HostPipeline, groups of 4 layers%s"
+                "api": "kv_evict_host (C ABI), groups of 4 layers%s"
                        % (", fused launch per group" if pipe.fused else "")}
     try:
         qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)

@@ -307,10 +307,55 @@ kv_status kv_evict_fused(const kv_problem *p, const void *q_win, const void *k, 
                          void *v_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The whole path for inputs and outputs in HOST memory (the end-to-end form of
+ * kv_score + [kv_pool_scores] + [kv_head_budgets] + kv_select_topk +
+ * kv_compact, or kv_evict_fused): the layers are processed in groups of
+ * plan->group_layers; group g's window queries, K and V are copied to the
+ * device on one internal stream while group g-1 is scored, selected and
+ * compacted on `stream` and group g-2's kept indices and rows are copied back
+ * on another, each copy one cudaMemcpyAsync.  The copies overlap the kernels
+ * only when the host buffers are pinned (cudaHostAlloc / cudaHostRegister);
+ * pageable buffers work, with the copies serialised.  Synchronous: returns
+ * when the host outputs are complete.  The pages have no such entry point;
+ * it exists so that a C caller can evict a cache that is not on the device.
+ *
+ * Inputs (host): q_win_host, k_host, v_host in the device layouts above;
+ * budgets_host [R*L*H].  Outputs (host): offsets_host [R*L*H + 1] (the scan of
+ * the budgets, or of the per-head budgets when plan->head_budgets is set),
+ * sel_idx_host [offsets_host[R*L*H]], k_out_host / v_out_host
+ * [offsets_host[R*L*H]][d] bf16 -- the standard unit order, bit-identical to
+ * the device path on the same problem split into the same layer groups (each
+ * group is scored as a problem of its own, so its pass-1 split size, chosen
+ * from the group's shape, can differ from the whole problem's; scores then
+ * differ in the last bits, within the score tolerance).
+ * workspace: device memory of kv_evict_host_workspace_size bytes (two groups
+ * of inputs, scores, workspaces and outputs, plus small tables), 16-byte
+ * aligned.  Errors: as the calls it makes (KV_ERR_BUDGET from the host check of
+ * the budgets before anything is copied); the device status of every group is
+ * kept and the first nonzero code is returned in *device_status (KV_OK if
+ * none).  Internal streams and events are created and destroyed per call.
+ */
+typedef struct kv_host_plan {
+    int32_t group_layers;   /* layers per group, 1..L */
+    int32_t pool_kernel;    /* 1 (no pooling) or an odd width up to 255 (kv_pool_scores) */
+    int32_t head_budgets;   /* nonzero: per-head budgets (kv_head_budgets) within each layer */
+    int32_t fused;          /* nonzero: kv_evict_fused per group (no pooling, no head budgets) */
+} kv_host_plan;
+
+kv_status kv_evict_host_workspace_size(const kv_problem *p, const kv_host_plan *plan,
+                                       const int32_t *budgets_host, size_t *bytes);
+kv_status kv_evict_host(const kv_problem *p, const kv_host_plan *plan, const void *q_win_host,
+                        const void *k_host, const void *v_host, const int32_t *budgets_host,
+                        int64_t *offsets_host, int32_t *sel_idx_host, void *k_out_host,
+                        void *v_out_host, void *workspace, size_t workspace_bytes, void *stream,
+                        int32_t *device_status);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of a
- * kv_score or kv_select_topk workspace.  *device_status receives the kv_status
- * a kernel posted (KV_OK if none).  Returns KV_ERR_CUDA if the stream itself
- * reports an error.
+ * score or select workspace.  *device_status receives the kv_status a kernel
+ * posted (KV_OK if none).  Returns KV_ERR_CUDA if the stream itself reports an
+ * error.  It takes the workspace because the library keeps no state between
+ * calls: the word lives in the caller's workspace.
  */
 kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status);
 

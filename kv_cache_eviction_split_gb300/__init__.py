@@ -27,7 +27,8 @@ __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attentio
            "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
            "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores", "kv_head_budgets",
            "kv_block_scores", "kv_compact_blocks", "kv_budgets_fraction", "BlockBuffers",
-           "evict_blocks", "EXPORTED_SYMBOLS",
+           "evict_blocks", "EXPORTED_SYMBOLS", "HostPipeline", "kv_evict_host",
+           "kv_evict_host_workspace_size",
            "evict", "KV_SCORE_DROPKV", "KV_SCORE_DROPKV_SQUARED", "KV_SCORE_ATTN_SUM"]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_BUDGET, KV_ERR_WORKSPACE, KV_ERR_CUDA, KV_ERR_TIMEOUT, \
@@ -41,7 +42,8 @@ EXPORTED_SYMBOLS = ("kv_score_workspace_size", "kv_score", "kv_score_attention",
                     "kv_budgets_pyramid", "kv_budgets_ripple", "kv_score_noalloc",
                     "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores",
                     "kv_head_budgets", "kv_block_scores", "kv_compact_blocks",
-                    "kv_budgets_fraction", "kv_evict_fused")
+                    "kv_budgets_fraction", "kv_evict_fused", "kv_evict_host_workspace_size",
+                    "kv_evict_host")
 
 
 class KvError(RuntimeError):
@@ -59,11 +61,33 @@ class _KvProblem(ctypes.Structure):
                 ("seq_offsets_dev", ctypes.c_void_p), ("softmax_scale", ctypes.c_float)]
 
 
+class _KvHostPlan(ctypes.Structure):
+    _fields_ = [("group_layers", ctypes.c_int32), ("pool_kernel", ctypes.c_int32),
+                ("head_budgets", ctypes.c_int32), ("fused", ctypes.c_int32)]
+
+
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    return _build.build(force=force)
+def build(force: bool = False, debug: bool = False) -> str:
+    """Build libkvevict.so (debug=True: the bounds-checked libkvevict_debug.so)."""
+    return _build.build(force=force, debug=debug)
+
+
+_debug_lib = None
+
+
+def load_debug():
+    """The bounds-checked build (libkvevict_debug.so), bound like load()'s library:
+    the same C ABI, with every TMA coordinate, workspace offset and gather index
+    checked on the device (KV_ERR_INVALID_ARG in the status word on a failed
+    check).  Its functions are called on the returned handle directly."""
+    global _debug_lib
+    if _debug_lib is None:
+        if not os.path.exists(_build.LIB_PATH_DEBUG):
+            raise RuntimeError("libkvevict_debug.so not found: run build(debug=True)")
+        _debug_lib = _bind(ctypes.CDLL(_build.LIB_PATH_DEBUG))
+    return _debug_lib
 
 
 def load(path: Optional[str] = None):
@@ -75,7 +99,12 @@ def load(path: Optional[str] = None):
     if not os.path.exists(path):
         raise RuntimeError("libkvevict.so not found at %s: run "
                            "kv_cache_eviction_split_gb300.build() (needs nvcc)" % path)
-    lib = ctypes.CDLL(path)
+    _lib = _bind(ctypes.CDLL(path))
+    return _lib
+
+
+def _bind(lib):
+    """Sets the argument and result types of every exported function of `lib`."""
     P = ctypes.POINTER(_KvProblem)
     vp, sz, i32, i64, f64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64, \
         ctypes.c_double
@@ -99,6 +128,10 @@ def load(path: Optional[str] = None):
         "kv_compact_blocks": [P, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp],
         "kv_budgets_fraction": [P, f64, ctypes.POINTER(i32)],
         "kv_evict_fused": [P, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp],
+        "kv_evict_host_workspace_size": [P, ctypes.POINTER(_KvHostPlan), ctypes.POINTER(i32),
+                                         szp],
+        "kv_evict_host": [P, ctypes.POINTER(_KvHostPlan), vp, vp, vp, ctypes.POINTER(i32),
+                          ctypes.POINTER(i64), vp, vp, vp, vp, sz, vp, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -110,7 +143,6 @@ def load(path: Optional[str] = None):
     lib.kv_set_wait_limit_ns.restype = None
     lib.kv_get_wait_limit_ns.argtypes = []
     lib.kv_get_wait_limit_ns.restype = ctypes.c_uint64
-    _lib = lib
     return lib
 
 
@@ -457,85 +489,65 @@ def evict_blocks(prob, scores, k, v, bb: BlockBuffers, stream=None):
 # ---------------------------------------------------------------------------
 # eviction from host memory, layer groups pipelined against the copies
 # ---------------------------------------------------------------------------
+def kv_evict_host_workspace_size(prob: Problem, plan, budgets_host: np.ndarray) -> int:
+    b = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(-1)
+    n = ctypes.c_size_t()
+    _check(load().kv_evict_host_workspace_size(
+        prob.c, ctypes.byref(plan), b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        ctypes.byref(n)), "kv_evict_host_workspace_size")
+    return n.value
+
+
+def kv_evict_host(prob: Problem, plan, q_host, k_host, v_host, budgets_host: np.ndarray,
+                  offsets_host: np.ndarray, sel_host, k_out_host, v_out_host, workspace,
+                  stream=None) -> int:
+    """The C entry point: host inputs in, host outputs out; returns the device status."""
+    b = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(-1)
+    assert offsets_host.dtype == np.int64 and offsets_host.flags.c_contiguous
+    st = ctypes.c_int32()
+    _check(load().kv_evict_host(
+        prob.c, ctypes.byref(plan), _ptr(q_host), _ptr(k_host), _ptr(v_host),
+        b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        offsets_host.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _ptr(sel_host),
+        _ptr(k_out_host), _ptr(v_out_host), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(st)),
+        "kv_evict_host")
+    return st.value
+
+
 class HostPipeline:
-    """Eviction of a problem whose Q, K and V are in pinned host memory.
+    """Eviction of a problem whose Q, K and V are in host memory, through kv_evict_host.
 
     The layers are taken in groups of `group_layers`: while group g is scored,
-    selected and compacted on one stream, group g+1's inputs are copied in on a
-    second and group g-1's kept indices and rows are copied out on a third.  Device
-    memory holds two groups of inputs and outputs, not the whole problem.
-
-    Outputs are group-major: for each layer group, its units in the usual order
-    (request, then layer, then head); `offsets` indexes them.  With one request this
-    is the usual unit order.
+    selected and compacted, group g+1's inputs are copied in and group g-1's kept
+    indices and rows are copied out (the copies overlap the kernels when the host
+    buffers are pinned).  Device memory holds two groups, not the whole problem.
+    This class allocates the device workspace and pinned host outputs once;
+    run() is one C call.  Outputs are in the standard unit order.
     """
 
     def __init__(self, prob: Problem, budgets_host: np.ndarray, group_layers: int = 4,
                  fused: bool = False):
+        import torch
         if fused and (prob.pool_kernel > 1 or prob.head_budgets):
             raise ValueError("the fused path takes neither pooling nor per-head budgets")
-        self.fused = fused
-        import torch
         dev = prob.cu_dev.device
         self.prob = prob
-        R, L, H = prob.num_requests, prob.num_layers, prob.num_kv_heads
-        Hq, d, w = prob.num_q_heads, prob.head_dim, prob.window
-        N = prob.total_tokens
-        b = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(R, L, H)
+        self.fused = fused
+        self.group_layers = group_layers
+        L = prob.num_layers
         self.groups = [(l0, min(L, l0 + group_layers)) for l0 in range(0, L, group_layers)]
-        self.subs, self.bufs_g, self.rows, self.row0 = [], [], [], []
-        offs, row = [0], 0
-        for (l0, l1) in self.groups:
-            sub = Problem(list(prob.lengths), l1 - l0, H, Hq, d, w, prob.num_sinks,
-                          prob.softmax_scale, dev, prob.score_rule, prob.pool_kernel,
-                          prob.head_budgets)
-            bg = np.ascontiguousarray(b[:, l0:l1])
-            og = kv_make_offsets(sub, bg)
-            self.subs.append(sub)
-            self.bufs_g.append((torch.from_numpy(bg.reshape(-1)).to(dev),
-                                torch.from_numpy(og).to(dev), og))
-            self.rows.append(int(og[-1]))
-            self.row0.append(row)
-            offs.extend((row + og[1:]).tolist())
-            row += int(og[-1])
-        self.offsets = np.asarray(offs, dtype=np.int64)
-        self.total_rows = row
-        Lg = max(l1 - l0 for (l0, l1) in self.groups)
-        big = self.subs[int(np.argmax([l1 - l0 for (l0, l1) in self.groups]))]
-        rows_max = max(self.rows)
-        self.slots = []
-        for _ in range(2):
-            self.slots.append(dict(
-                q=torch.empty(R * Lg * Hq * w * d, dtype=torch.bfloat16, device=dev),
-                k=torch.empty(Lg * H * N * d, dtype=torch.bfloat16, device=dev),
-                v=torch.empty(Lg * H * N * d, dtype=torch.bfloat16, device=dev),
-                scores=torch.empty(Lg * H * N, dtype=torch.float32, device=dev),
-                pooled=torch.empty(Lg * H * N, dtype=torch.float32, device=dev)
-                if prob.pool_kernel > 1 else None,
-                score_ws=torch.zeros(max(kv_score_workspace_size(big), 256), dtype=torch.uint8,
-                                     device=dev),
-                select_ws=torch.zeros(max(kv_select_workspace_size(big), 256), dtype=torch.uint8,
-                                      device=dev),
-                hb=torch.empty(R * Lg * H, dtype=torch.int32, device=dev),
-                ho=torch.empty(R * Lg * H + 1, dtype=torch.int64, device=dev),
-                sel=torch.empty(max(rows_max, 1), dtype=torch.int32, device=dev),
-                k_out=torch.empty((max(rows_max, 1), d), dtype=torch.bfloat16, device=dev),
-                v_out=torch.empty((max(rows_max, 1), d), dtype=torch.bfloat16, device=dev)))
-        self.sel_host = torch.empty(max(self.total_rows, 1), dtype=torch.int32, pin_memory=True)
-        self.k_out_host = torch.empty((max(self.total_rows, 1), d), dtype=torch.bfloat16,
-                                      pin_memory=True)
+        self.plan = _KvHostPlan(int(group_layers), int(prob.pool_kernel), int(prob.head_budgets),
+                                int(fused))
+        self.budgets_host = np.ascontiguousarray(budgets_host, dtype=np.int32).reshape(-1)
+        self.offsets = kv_make_offsets(prob, self.budgets_host)
+        self.total_rows = int(self.offsets[-1])
+        nbytes = kv_evict_host_workspace_size(prob, self.plan, self.budgets_host)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        rows, d = max(self.total_rows, 1), prob.head_dim
+        self.sel_host = torch.empty(rows, dtype=torch.int32, pin_memory=True)
+        self.k_out_host = torch.empty((rows, d), dtype=torch.bfloat16, pin_memory=True)
         self.v_out_host = torch.empty_like(self.k_out_host, pin_memory=True)
-        # per-head budgets are computed on the device: their offsets come back per group
-        self.head_offsets_host = [torch.empty(R * (l1 - l0) * H + 1, dtype=torch.int64,
-                                              pin_memory=True) for (l0, l1) in self.groups] \
-            if prob.head_budgets else None
-        self.streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
-        self.ev_in = [torch.cuda.Event() for _ in range(2)]
-        self.ev_comp = [torch.cuda.Event() for _ in range(2)]
-        self.ev_out = [torch.cuda.Event() for _ in range(2)]
-        cur = torch.cuda.current_stream(dev)
-        for e in self.ev_comp + self.ev_out:
-            e.record(cur)
 
     @property
     def h2d_bytes(self) -> int:
@@ -547,77 +559,15 @@ class HostPipeline:
     def d2h_bytes(self) -> int:
         return self.total_rows * (4 + 2 * self.prob.head_dim * 2)
 
-    def _evict_group(self, sub, q, k, v, scores, slot, b_dev, o_dev, g, s_comp):
-        """The separate calls for layer group g: score, pool, per-head budgets, select,
-        compact."""
-        p = self.prob
-        R, H, N = p.num_requests, p.num_kv_heads, p.total_tokens
-        Lg = self.groups[g][1] - self.groups[g][0]
-        kv_score(sub, q, k, v, scores, slot["score_ws"], s_comp)
-        ranked = scores
-        if p.pool_kernel > 1:
-            ranked = slot["pooled"][:Lg * H * N]
-            kv_pool_scores(sub, p.pool_kernel, scores, ranked, s_comp)
-        if p.head_budgets:
-            hb, ho = slot["hb"][:R * Lg * H], slot["ho"][:R * Lg * H + 1]
-            kv_head_budgets(sub, ranked, b_dev, o_dev, hb, ho, slot["select_ws"], s_comp)
-            b_dev, o_dev = hb, ho
-        kv_select_topk(sub, ranked, b_dev, o_dev, slot["sel"], slot["select_ws"], s_comp)
-        kv_compact(sub, k, v, slot["sel"], o_dev, self.rows[g], slot["k_out"], slot["v_out"],
-                   s_comp)
-
-    def run(self, q_host, k_host, v_host):
-        """Copies in, evicts and copies out every layer group; returns when the host
-        outputs (sel_host, k_out_host, v_out_host) are complete.  Raises KvError if a
-        kernel posted a device status."""
-        import torch
-        p = self.prob
-        R, H, Hq, w, d, N = (p.num_requests, p.num_kv_heads, p.num_q_heads, p.window,
-                             p.head_dim, p.total_tokens)
-        s_in, s_comp, s_out = self.streams
-        for g, (l0, l1) in enumerate(self.groups):
-            slot, sub, Lg = self.slots[g & 1], self.subs[g], l1 - l0
-            b_dev, o_dev, _ = self.bufs_g[g]
-            q = slot["q"][:R * Lg * Hq * w * d].view(R, Lg, Hq, w, d)
-            k = slot["k"][:Lg * H * N * d].view(Lg, H, N, d)
-            v = slot["v"][:Lg * H * N * d].view(Lg, H, N, d)
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(self.ev_comp[g & 1])
-                for r in range(R):
-                    q[r].copy_(q_host[r, l0:l1], non_blocking=True)
-                k.copy_(k_host[l0:l1], non_blocking=True)
-                v.copy_(v_host[l0:l1], non_blocking=True)
-                self.ev_in[g & 1].record(s_in)
-            s_comp.wait_event(self.ev_in[g & 1])
-            s_comp.wait_event(self.ev_out[g & 1])
-            scores = slot["scores"][:Lg * H * N]
-            if self.fused:
-                kv_evict_fused(sub, q, k, v, b_dev, o_dev, self.rows[g], scores, slot["sel"],
-                               slot["k_out"], slot["v_out"], slot["score_ws"], s_comp)
-            else:
-                self._evict_group(sub, q, k, v, scores, slot, b_dev, o_dev, g, s_comp)
-            self.ev_comp[g & 1].record(s_comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(self.ev_comp[g & 1])
-                a, n = self.row0[g], self.rows[g]
-                self.sel_host[a:a + n].copy_(slot["sel"][:n], non_blocking=True)
-                self.k_out_host[a:a + n].copy_(slot["k_out"][:n], non_blocking=True)
-                self.v_out_host[a:a + n].copy_(slot["v_out"][:n], non_blocking=True)
-                if p.head_budgets:
-                    self.head_offsets_host[g].copy_(slot["ho"][:R * Lg * H + 1],
-                                                    non_blocking=True)
-                self.ev_out[g & 1].record(s_out)
-        for st in self.streams:
-            st.synchronize()
-        for slot in self.slots:
-            for ws in (slot["score_ws"], slot["select_ws"]):
-                code = kv_check_status(ws, s_comp)
-                if code != KV_OK:
-                    raise KvError(code, "HostPipeline.run")
-        if p.head_budgets:
-            offs = [0]
-            for g in range(len(self.groups)):
-                offs.extend((self.row0[g] + self.head_offsets_host[g].numpy()[1:]).tolist())
-            self.offsets = np.asarray(offs, dtype=np.int64)
+    def run(self, q_host, k_host, v_host, stream=None):
+        """One kv_evict_host call; returns (sel, k_out, v_out, offsets) in host memory.
+        Raises KvError if a kernel posted a device status."""
+        offsets = np.zeros(self.prob.num_units + 1, dtype=np.int64)
+        code = kv_evict_host(self.prob, self.plan, q_host, k_host, v_host, self.budgets_host,
+                             offsets, self.sel_host, self.k_out_host, self.v_out_host,
+                             self.workspace, stream)
+        if code != KV_OK:
+            raise KvError(code, "kv_evict_host (device status)")
+        self.offsets = offsets
         n = self.total_rows
         return self.sel_host[:n], self.k_out_host[:n], self.v_out_host[:n], self.offsets

@@ -18,12 +18,17 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libkvevict.so")
+# The bounds-checked variant (-DKV_DEBUG_BOUNDS): every TMA coordinate, workspace
+# offset and gather index checked against its tensor's extent; a failed check posts
+# KV_ERR_INVALID_ARG instead of touching memory.  Same sources, same ABI.
+BUILD_DIR_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_PATH_DEBUG = os.path.join(PKG, "libkvevict_debug.so")
 HEADER = os.path.join(ROOT, "include", "kvevict.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-ffp-contract=off", "-Xptxas", "-O3"]
-_lock = threading.Lock()
+_locks = {False: threading.Lock(), True: threading.Lock()}   # per variant
 
 
 def nvcc() -> str:
@@ -48,17 +53,23 @@ def up_to_date(lib_path: str = LIB_PATH) -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link; returns the library path.  Rebuilds only when sources changed."""
-    with _lock:
-        if not force and up_to_date():
-            return LIB_PATH
-        os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None,
+          debug: bool = False) -> str:
+    """Compile and link; returns the library path.  Rebuilds only when sources changed.
+    debug=True builds the bounds-checked variant libkvevict_debug.so."""
+    lib_path = LIB_PATH_DEBUG if debug else LIB_PATH
+    build_dir = BUILD_DIR_DEBUG if debug else BUILD_DIR
+    with _locks[debug]:
+        if not force and up_to_date(lib_path):
+            return lib_path
+        os.makedirs(build_dir, exist_ok=True)
         cc = nvcc()
         flags = NVCC_FLAGS + ARCH + ["-I", os.path.join(ROOT, "include")] + list(extra_flags or [])
+        if debug:
+            flags.append("-DKV_DEBUG_BOUNDS")
 
         def compile_one(src):
-            obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+            obj = os.path.join(build_dir, os.path.basename(src) + ".o")
             cmd = [cc, "-c", src, "-o", obj] + flags
             res = subprocess.run(cmd, capture_output=True, text=True)
             if res.returncode != 0:
@@ -69,10 +80,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
         with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
             objs = list(ex.map(compile_one, _sources()))
-        tmp = LIB_PATH + ".%d.tmp" % os.getpid()
+        tmp = lib_path + ".%d.tmp" % os.getpid()
         cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("nvcc link failed:\n%s%s" % (res.stdout, res.stderr))
-        os.replace(tmp, LIB_PATH)
-        return LIB_PATH
+        os.replace(tmp, lib_path)
+        return lib_path

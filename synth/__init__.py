@@ -83,7 +83,13 @@ def uniform01(key: int, start: int, count: int) -> np.ndarray:
 
 
 def _normals_chunk(key: int, start: int, count: int) -> np.ndarray:
-    e = np.arange(start, start + count, dtype=np.uint64)
+    return _normals_at(key, np.arange(start, start + count, dtype=np.uint64))
+
+
+def _normals_at(key: int, e: np.ndarray) -> np.ndarray:
+    """Irwin-Hall(12) deviates of the elements with indices ``e`` (any order), float32."""
+    e = np.asarray(e, dtype=np.uint64)
+    count = e.size
     base = e * np.uint64(3) + np.uint64(1)
     m = np.uint64(0x0000FFFF0000FFFF)
     acc = np.zeros(count, dtype=np.uint64)   # two 32-bit lanes of partial 16-bit sums
@@ -361,6 +367,34 @@ def kv_unit(wl: Workload, r: int, l: int, h: int, *, outl=None, heavy_pos=None,
         if heavy_vec is None:
             heavy_vec = heavy_rows(wl, q_window(wl))
         k[heavy_pos[r, l, h]] = heavy_vec[r, l, h]
+    return k, v
+
+
+def kv_rows(wl: Workload, r: int, l: int, h: int, rows, *, outl=None, heavy_pos=None,
+            heavy_vec=None) -> tuple[np.ndarray, np.ndarray]:
+    """Host regeneration of chosen K and V rows of one unit: ``rows`` are token indices
+    within request r; returns two uint16 arrays [len(rows)][d], bit-identical to
+    ``kv_unit(wl, r, l, h)[i][rows]`` without generating the whole unit."""
+    d = wl.head_dim
+    cu = wl.cu_seqlens()
+    N_tot = int(cu[-1])
+    row0 = (l * wl.num_kv_heads + h) * N_tot + int(cu[r])
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    if outl is None:
+        outl = outlier_channels(wl)
+    sc = _channel_scale(wl, l, h, outl)
+    e = ((row0 + rows)[:, None] * d + np.arange(d, dtype=np.int64)[None, :]).reshape(-1)
+    out = []
+    for sid in (S_K, S_V):
+        z = _normals_at(stream_key(wl.seed, sid), e.astype(np.uint64)).reshape(rows.size, d)
+        out.append(f32_to_bf16_bits(z * sc[None, :]))
+    k, v = out
+    if wl.num_heavy:
+        if heavy_pos is None:
+            heavy_pos = heavy_positions(wl)
+        if heavy_vec is None:
+            heavy_vec = heavy_rows(wl, q_window(wl))
+        k[np.isin(rows, heavy_pos[r, l, h])] = heavy_vec[r, l, h]
     return k, v
 
 

@@ -179,3 +179,91 @@ def sample_units(wl, count, seed=1234):
         if len(picks) == count:
             break
     return picks
+
+
+def check_every_unit_select_compact(run: DeviceRun, host_rows=64, threads=None, seed=4321):
+    """Selection and compaction of EVERY unit, at any size, without oracle scoring:
+
+    * selection: equal to the oracle's selection rule (oracle.select) applied to the
+      GPU's own (ranked) scores of the unit;
+    * compaction: every kept row equals the row of the device K/V at the kept index
+      (a torch gather, bit for bit), and `host_rows` kept rows of every unit (its
+      first and last four and a seeded sample of the rest) equal the host
+      regeneration of those rows from the seed (synth.kv_rows), which ties the
+      device K/V to the generator.
+    Returns the number of units checked."""
+    import torch
+    wl, b = run.wl, run.bufs
+    cu = run.dw.cu_host
+    L, H = wl.num_layers, wl.num_kv_heads
+    units = wl.num_units
+    offs = np.asarray(run.eff_offsets, dtype=np.int64)
+    bud = np.asarray(run.eff_budgets, dtype=np.int64)
+    total = int(offs[-1])
+    ranked = (b.pooled if b.pooled is not None else b.scores)
+    scores = ranked.cpu().numpy()
+    sel = b.sel[:total].cpu().numpy()
+
+    def one_select(u):
+        r, l, h = wl.unit_coords(u)
+        g = scores[l, h, int(cu[r]):int(cu[r + 1])].astype(np.float64)
+        mine = oracle.select(g, wl.window, wl.num_sinks, int(bud[u]))
+        got = sel[offs[u]:offs[u + 1]]
+        if not np.array_equal(got, mine):
+            raise AssertionError("unit %d (%d,%d,%d): selection differs from the oracle's "
+                                 "rule on the GPU's scores" % (u, r, l, h))
+        return True
+
+    threads = threads or min(32, os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        assert all(ex.map(one_select, range(units)))
+
+    # every kept row against the device K/V, gathered by torch on the device
+    dev = b.sel.device
+    N_tot = int(cu[-1])
+    r_of = np.repeat(np.arange(wl.num_requests), L * H)
+    lh = np.tile(np.arange(L * H), wl.num_requests)
+    row0 = lh * N_tot + cu[r_of]                       # first K/V row of each unit
+    counts = torch.from_numpy(offs[1:] - offs[:-1]).to(dev)
+    base = torch.repeat_interleave(torch.from_numpy(row0).to(dev), counts)
+    idx = base + b.sel[:total].long()
+    d = wl.head_dim
+    kf = run.dw.k.reshape(-1, d)
+    vf = run.dw.v.reshape(-1, d)
+    as16 = lambda t: t.view(torch.int16)
+    assert torch.equal(as16(kf[idx]), as16(b.k_out[:total])), "compacted K differs from K[sel]"
+    assert torch.equal(as16(vf[idx]), as16(b.v_out[:total])), "compacted V differs from V[sel]"
+
+    # a sample of kept rows of every unit against the host generator
+    outl = synth.outlier_channels(wl)
+    hp = synth.heavy_positions(wl)
+    hv = synth.heavy_rows(wl, synth.q_window(wl)) if wl.num_heavy else None
+    picks = []
+    for u in range(units):
+        n_u = int(bud[u])
+        if n_u <= host_rows:
+            pos = np.arange(n_u)
+        else:
+            rng = synth.uniform01(synth.stream_key(seed, u), 0, host_rows)
+            mid = 4 + np.floor(rng * (n_u - 8)).astype(np.int64)
+            pos = np.unique(np.concatenate([np.arange(4), np.arange(n_u - 4, n_u),
+                                            mid[:host_rows - 8]]))
+        picks.append(pos)
+    flat = torch.from_numpy(np.concatenate([offs[u] + picks[u] for u in range(units)])).to(dev)
+    k_s = as16(b.k_out[flat]).cpu().numpy().view(np.uint16)
+    v_s = as16(b.v_out[flat]).cpu().numpy().view(np.uint16)
+    starts = np.concatenate([[0], np.cumsum([len(p) for p in picks])])
+
+    def one_rows(u):
+        r, l, h = wl.unit_coords(u)
+        toks = sel[offs[u] + picks[u]]
+        kr, vr = synth.kv_rows(wl, r, l, h, toks, outl=outl, heavy_pos=hp, heavy_vec=hv)
+        a, z = starts[u], starts[u + 1]
+        if not (np.array_equal(k_s[a:z], kr) and np.array_equal(v_s[a:z], vr)):
+            raise AssertionError("unit %d (%d,%d,%d): compacted rows differ from the host "
+                                 "generator" % (u, r, l, h))
+        return True
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        assert all(ex.map(one_rows, range(units)))
+    return units

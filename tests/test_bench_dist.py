@@ -58,7 +58,8 @@ def test_single_process_helpers():
 
 def test_roofline_accounting():
     """The algorithmic bytes bench.py divides by: per-stage formulas from the workload's
-    shapes and budgets, and the fused launch as the sum of its four steps."""
+    shapes and budgets; the fused launch (the whole path) on the each-byte-once basis
+    of the headline HBM fraction, with the sum of its four steps kept as phase_bytes."""
     import numpy as np
     import bench
     import synth
@@ -78,7 +79,10 @@ def test_roofline_accounting():
     fused = bench.stage_roofline("fused", 1.0, wl, budgets, peaks)
     parts = [bench.stage_roofline(s, 1.0, wl, budgets, peaks)
              for s in ("attention", "rescore", "select", "compact")]
-    assert fused["algorithmic_bytes"] == sum(p["algorithmic_bytes"] for p in parts)
+    rows = int(budgets.sum())
+    once = kv_bytes + q_bytes + rows * (2 * d * 2 + 4) + 8 * (L * H + 1)
+    assert fused["algorithmic_bytes"] == once == bench.algorithmic_bytes(wl, budgets)
+    assert fused["phase_bytes"] == sum(p["algorithmic_bytes"] for p in parts)
     assert fused["tensor"]["algorithmic_flops"] == \
         att["tensor"]["algorithmic_flops"] + res["tensor"]["algorithmic_flops"]
     # the attention sum reads K only

@@ -137,16 +137,19 @@ def test_bad_device_budget_posts_status(cuda_lib):
     assert kv.kv_check_status(bufs.select_ws) == 0   # cleared
 
 
-@pytest.mark.parametrize("wl,count", [(synth.LLAMA8B_32K, 3), (synth.LONG_128K, 2),
-                                      (synth.QWEN7B_128K, 2), (synth.RAGGED_MISTRAL, 3)],
-                         ids=lambda x: getattr(x, "name", str(x)))
-def test_full_size_sampled_units(cuda_lib, wl, count):
+@pytest.mark.parametrize("wl", [synth.LLAMA8B_32K, synth.LONG_128K, synth.QWEN7B_128K,
+                                synth.RAGGED_MISTRAL], ids=lambda w: w.name)
+def test_full_size_every_unit(cuda_lib, wl):
+    """The full-size configurations in the launch configuration the benchmark times:
+    selection and compaction of every unit (all 2048 segments of the ragged batch)
+    against the oracle's rule and the generator, oracle scores on 16 seeded units
+    (computed in parallel on the host cores), and properties of every score."""
     import torch
     run = _run(cuda_lib, wl)
-    parity.check_units(run, parity.sample_units(wl, count))
-    # properties that hold on every unit at any size
+    assert parity.check_every_unit_select_compact(run) == wl.num_units
+    res = parity.check_units(run, parity.sample_units(wl, 16))
+    assert len(res) == 16
     b = run.bufs
-    sel = b.sel[: b.total_rows]
     seg_len = torch.diff(b.offsets)
     assert int(seg_len.min()) >= wl.num_sinks + wl.window
     assert bool(torch.isfinite(b.scores).all()) and float(b.scores.min()) >= 0.0

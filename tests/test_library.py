@@ -190,3 +190,44 @@ def test_block_helpers_host_side(kv):
                                  None) == kv.KV_ERR_INVALID_ARG
     assert lib.kv_compact_blocks(p.c, 2, fake, fake, fake, fake, fake, -1, fake, fake,
                                  None) == kv.KV_ERR_INVALID_ARG
+
+
+def test_host_pipeline_plan_checks(kv):
+    """kv_evict_host_workspace_size / kv_evict_host argument checks (host only)."""
+    prob = _prob(kv, lengths=[1000, 2000], num_layers=5)
+    budgets = np.full(prob.num_units, 200, dtype=np.int32)
+    good = kv._KvHostPlan(2, 1, 0, 0)
+    one = kv.kv_evict_host_workspace_size(prob, good, budgets)
+    # the workspace holds two slots of a 2-layer group: more than one layer's K and V
+    N, d, H = prob.total_tokens, prob.head_dim, prob.num_kv_heads
+    assert one > 2 * 2 * (2 * H * N * d * 2)
+    for bad in (kv._KvHostPlan(0, 1, 0, 0), kv._KvHostPlan(6, 1, 0, 0),
+                kv._KvHostPlan(2, 4, 0, 0), kv._KvHostPlan(2, 11, 0, 1),
+                kv._KvHostPlan(2, 1, 1, 1)):
+        with pytest.raises(kv.KvError) as e:
+            kv.kv_evict_host_workspace_size(prob, bad, budgets)
+        assert e.value.code == kv.KV_ERR_INVALID_ARG
+    # a budget below sinks + window is refused on the host before anything is copied
+    bad_b = budgets.copy()
+    bad_b[3] = 10
+    offs = np.zeros(prob.num_units + 1, dtype=np.int64)
+    st = ctypes.c_int32()
+    rc = kv.load().kv_evict_host(prob.c, ctypes.byref(good), 16, 16, 16,
+                                 bad_b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                 offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), 16, 16, 16,
+                                 256, one, None, ctypes.byref(st))
+    assert rc == kv.KV_ERR_BUDGET
+
+
+def test_host_pipeline_workspace_covers_every_group_shape(kv):
+    """A smaller last group can choose smaller pass-1 splits (more partials per unit)
+    than the full groups: the workspace must cover the largest need of any group."""
+    prob = _prob(kv, lengths=[131072], num_layers=5, num_kv_heads=1, num_q_heads=4)
+    budgets = np.full(prob.num_units, 2000, dtype=np.int32)
+    plan = kv._KvHostPlan(4, 1, 0, 0)
+    total = kv.kv_evict_host_workspace_size(prob, plan, budgets)
+    sub4 = _prob(kv, lengths=[131072], num_layers=4, num_kv_heads=1, num_q_heads=4)
+    sub1 = _prob(kv, lengths=[131072], num_layers=1, num_kv_heads=1, num_q_heads=4)
+    s4, s1 = kv.kv_score_workspace_size(sub4), kv.kv_score_workspace_size(sub1)
+    assert s1 > s4 / 4          # the one-layer group needs more than a quarter of four layers
+    assert total >= 2 * max(s4, s1)

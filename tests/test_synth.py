@@ -55,3 +55,16 @@ def test_heavy_and_outliers():
     big = set(oc[1, 1])
     for c in range(wl.head_dim):
         assert (rms[c] > 4.0) == (c in big)
+
+
+def test_kv_rows_equal_whole_unit_rows():
+    """The row-level host regenerator gives the same bits as the whole-unit one,
+    heavy rows and outlier channels included."""
+    wl = synth.small_variant(synth.RAGGED_MISTRAL, 0, requests=[900, 1300], layers=2)
+    for (r, l, h) in [(0, 0, 0), (1, 1, 1), (1, 0, 1)]:
+        k, v = synth.kv_unit(wl, r, l, h)
+        n = k.shape[0]
+        rows = np.array([0, 3, 17, n // 2, n - 1] + list(synth.heavy_positions(wl)[r, l, h][:3]))
+        kr, vr = synth.kv_rows(wl, r, l, h, rows)
+        np.testing.assert_array_equal(kr, k[rows])
+        np.testing.assert_array_equal(vr, v[rows])
