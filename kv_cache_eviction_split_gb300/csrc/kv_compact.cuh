@@ -103,7 +103,8 @@ __device__ __forceinline__ void compact_block(const DevProblem &P, const uint4 *
                     const long long i = row - offsets[s_unit[r]];
                     if (i < B.offsets[ub + 1] - B.offsets[ub]) tok = B.sel[B.offsets[ub] + i];
                 }
-                if (tok >= 0 && tok < U.n) {
+                if (tok >= 0 && tok < U.n &&
+                    in_range(U.kv_row0 + tok, kv_rows_total(P), nullptr)) {
                     buf[q] = ld_nc(src_base + (U.kv_row0 + tok) * CPR + ch);
                     dst[q] = row * CPR + ch;
                     ok[q] = true;
@@ -173,7 +174,8 @@ __device__ __forceinline__ void compact_rows(const DevProblem &P, const uint4 *_
                     U = unit_info(P, u, P.cu);
                 }
                 const int tok = row < u_end ? toks[q] : -1;
-                if (tok >= 0 && tok < U.n) {
+                if (tok >= 0 && tok < U.n &&
+                    in_range(U.kv_row0 + tok, kv_rows_total(P), nullptr)) {
                     buf[q] = ld_nc(src_base + (U.kv_row0 + tok) * CPR + ch);
                     dst[q] = row * CPR + ch;
                     ok[q] = true;

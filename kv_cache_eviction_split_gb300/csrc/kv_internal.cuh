@@ -139,4 +139,34 @@ __device__ inline void post_status(int *status, int code) {
     atomicCAS(status, 0, code);
 }
 
+// Bounds checks of the debug build (-DKV_DEBUG_BOUNDS, libkvevict_debug.so): every
+// TMA tile coordinate, workspace offset and gather index is tested against the
+// extent of its tensor before use.  in_range(i, n, status) is true when
+// 0 <= i < n; otherwise it posts KV_ERR_INVALID_ARG and the caller skips the
+// access (a pipeline producer instead stops issuing and aborts its CTA's pipeline,
+// whose other roles drain out as after an expired wait).  Nothing traps.  Calls
+// without a status word (kv_compact has no workspace) pass nullptr and only skip.
+// In the release build it is the constant true and costs nothing.
+#ifdef KV_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+__device__ __forceinline__ bool in_range(long long i, long long n, int *status) {
+    if constexpr (!kDebugBounds) {
+        return true;
+    } else {
+        const bool ok = i >= 0 && i < n;
+        if (!ok && status) post_status(status, KV_ERR_INVALID_ARG);
+        return ok;
+    }
+}
+// Rows of the packed K/V (and scores, ||v||^2) tensors, and of the window queries.
+__host__ __device__ inline long long kv_rows_total(const DevProblem &P) {
+    return (long long)P.L * P.H * P.N_tot;
+}
+__host__ __device__ inline long long q_rows_total(const DevProblem &P) {
+    return (long long)P.R * P.L * P.Hq * P.w;
+}
+
 }  // namespace kvevict

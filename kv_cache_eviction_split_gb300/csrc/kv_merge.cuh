@@ -22,6 +22,7 @@ namespace kvevict {
 template <int D, bool kO>
 __device__ __forceinline__ void merge_row(const DevProblem &P, const ScoreWs &ws, long long u,
                                           int row, int lane) {
+    if (!in_range((long long)u * ws.a_rows + row, P.units * ws.a_rows, ws.status)) return;
     if (kO && row >= P.rows) {   // padding rows of the last 128-row chunk read as zeros
         const size_t arow = (size_t)u * ws.a_rows + row;
         for (int c = lane; c < D; c += 32) {
@@ -34,6 +35,12 @@ __device__ __forceinline__ void merge_row(const DevProblem &P, const ScoreWs &ws
     const UnitInfo U = unit_info(P, u, P.cu);
     const int nslots = (U.n + P.split_keys - 1) / P.split_keys * ws.parts;
     const size_t base = (size_t)u * P.max_splits * ws.parts * P.rows + row;
+    // the unit's partial slots and its merged rows lie inside their arrays
+    if (!in_range((long long)(base + (size_t)(nslots > 0 ? nslots - 1 : 0) * P.rows),
+                  P.units * P.max_splits * ws.parts * P.rows, ws.status) ||
+        !in_range((long long)u * P.rows + row, P.units * P.rows, ws.status) ||
+        nslots > P.max_splits * ws.parts)
+        return;
 
     // partials with l = 0 saw no key of this row (or no tile at all): skipped.
     // Lane j holds the (m, l) of slots j, j + 32, ...: loaded together.

@@ -297,6 +297,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                 mbar_arrive_expect_tx(q_full, (two_q ? 2 : 1) * Ly::kOp);
                 for (int L = 0; L < (two_q ? 2 : 1); ++L) {
                     const int qy = (int)(U.q_row0 + (L ? w1.chunk : w0.chunk) * kChunkRows);
+                    if (!in_range(qy, q_rows_total(P), A.status)) ok = false;
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
                         tma_load_2d(smem + Ly::kQ + L * Ly::kOp + kb * kBlockBytes, tm_q,
@@ -312,7 +313,9 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                         const long long kc = tcount + i;
                         const int s = (int)(kc % kKStages);
                         const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
-                        ok = mbar_wait(&k_empty[s], (uint32_t)((kc / kKStages) & 1) ^ 1u,
+                        ok = ok && in_range((it.t0 + i) * kTileKeys, U.n, A.status) &&
+                             in_range(ky, kv_rows_total(P), A.status) &&
+                             mbar_wait(&k_empty[s], (uint32_t)((kc / kKStages) & 1) ^ 1u,
                                        abort_flag, P.wait_ns);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
@@ -327,7 +330,9 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                         const long long vc = tcount + iv;
                         const int s = (int)(vc % kVStages);
                         const int vy = (int)(U.kv_row0 + (long long)(it.t0 + iv) * kTileKeys);
-                        ok = mbar_wait(&v_empty[s], (uint32_t)((vc / kVStages) & 1) ^ 1u,
+                        ok = in_range((it.t0 + iv) * kTileKeys, U.n, A.status) &&
+                             in_range(vy, kv_rows_total(P), A.status) &&
+                             mbar_wait(&v_empty[s], (uint32_t)((vc / kVStages) & 1) ^ 1u,
                                        abort_flag, P.wait_ns);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
@@ -471,10 +476,12 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
             const LaneWork w = lane_work(A, it, L);
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const int row = w.chunk * kChunkRows + rr;
-            const bool row_valid = row < P.rows;
             const int slot = A.parts == 1 ? it.split : 2 * it.split + L;
             const size_t prow_idx =
                 ((size_t)it.u * P.max_splits * A.parts + slot) * P.rows + row;
+            const bool row_valid =
+                row < P.rows &&
+                in_range((long long)prow_idx, P.units * P.max_splits * A.parts * P.rows, A.status);
             if (w.steps == 0) {
                 // no tile for this lane: an empty partial (l = 0) for the merge to skip
                 if (A.parts == 2 && row_valid) A.part_ml[prow_idx] = make_float2(-INFINITY, 0.f);
@@ -647,7 +654,9 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                     float q = row_half_to_f16<D>(tile, row, lane >> 4, bad, nz, nrm);
                     q += __shfl_xor_sync(0xffffffffu, q, 16);
                     const int j = (it.t0 + ti) * kTileKeys + row;   // key of the unit
-                    if (lane < 16 && j < U.n) A.v2[U.kv_row0 + j] = q;
+                    if (lane < 16 && j < U.n &&
+                        in_range(U.kv_row0 + j, kv_rows_total(P), A.status))
+                        A.v2[U.kv_row0 + j] = q;
                 }
                 // refused: a value fp16 cannot hold, or 64 rows of nonzero values that
                 // all fall below 2^-14 (fp16 subnormals keep too few of their bits)
@@ -756,6 +765,7 @@ __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtens
                 mbar_arrive_expect_tx(q_full, (two_q ? 2 : 1) * Ly::kOp);
                 for (int L = 0; L < (two_q ? 2 : 1); ++L) {
                     const int qy = (int)(U.q_row0 + (L ? w1.chunk : w0.chunk) * kChunkRows);
+                    if (!in_range(qy, q_rows_total(P), A.status)) ok = false;
 #pragma unroll
                     for (int kb = 0; kb < D / 64; ++kb)
                         tma_load_2d(smem + Ly::kQ + L * Ly::kOp + kb * kBlockBytes, tm_q,
@@ -767,7 +777,9 @@ __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtens
                     const long long kc = tcount + i;
                     const int s = (int)(kc % kStatKSt);
                     const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
-                    ok = mbar_wait(&k_empty[s], (uint32_t)((kc / kStatKSt) & 1) ^ 1u, abort_flag,
+                    ok = in_range((it.t0 + i) * kTileKeys, U.n, A.status) &&
+                         in_range(ky, kv_rows_total(P), A.status) &&
+                         mbar_wait(&k_empty[s], (uint32_t)((kc / kStatKSt) & 1) ^ 1u, abort_flag,
                                    P.wait_ns);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
@@ -864,10 +876,12 @@ __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtens
             const LaneWork w = lane_work(A, it, L);
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const int row = w.chunk * kChunkRows + rr;
-            const bool row_valid = row < P.rows;
             const int slot = A.parts == 1 ? it.split : 2 * it.split + L;
             const size_t prow_idx =
                 ((size_t)it.u * P.max_splits * A.parts + slot) * P.rows + row;
+            const bool row_valid =
+                row < P.rows &&
+                in_range((long long)prow_idx, P.units * P.max_splits * A.parts * P.rows, A.status);
             if (w.steps == 0) {
                 if (A.parts == 2 && row_valid) A.part_ml[prow_idx] = make_float2(-INFINITY, 0.f);
                 continue;

@@ -305,6 +305,10 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
             auto pf_step = [&]() {
                 if (pf_item >= A.total_items) return;
                 const int ky = (int)(pf_row0 + (long long)pf_t * kTileKeys);
+                if (!in_range(ky, kv_rows_total(P), A.status)) {
+                    pf_item = A.total_items;   // no further prefetches
+                    return;
+                }
 #pragma unroll
                 for (int kb = 0; kb < D / 64; ++kb) {
                     tma_prefetch_2d(tm_k, kb * 64, ky);
@@ -325,6 +329,9 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
                 mbar_arrive_expect_tx(qa_full, (kX ? 3 : 1) * Ly::kOp);
                 const int qy = (int)(U.q_row0 + it.c * kChunkRows);
                 const int ay = (int)(it.u * A.a_rows + it.c * kChunkRows);
+                if (!in_range(qy, q_rows_total(P), A.status) ||
+                    !in_range(ay, P.units * A.a_rows, A.status))
+                    ok = false;
 #pragma unroll
                 for (int kb = 0; kb < D / 64; ++kb) {
                     tma_load_2d(smem + Ly::kQ + kb * kBlockBytes, tm_q, qa_full, kb * 64, qy);
@@ -341,7 +348,9 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
                     const uint32_t par = (uint32_t)((tcount / kKSt) & 1) ^ 1u;
                     const int ky = (int)(U.kv_row0 + (long long)t * kTileKeys);
                     pf_step();
-                    ok = mbar_wait(&k_empty[s], par, abort_flag, P.wait_ns);
+                    ok = in_range((long long)t * kTileKeys, U.n, A.status) &&
+                         in_range(ky, kv_rows_total(P), A.status) &&
+                         mbar_wait(&k_empty[s], par, abort_flag, P.wait_ns);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
 #pragma unroll
@@ -485,10 +494,15 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
             const int pos0 = U.n - P.w;
             const float *u_v2 = A.v2 + U.kv_row0;
             float vq[2] = {0.f, 0.f};
+            // the unit's rows of the score (or chunk partial) and ||v||^2 arrays
+            const bool rows_ok =
+                in_range(U.kv_row0, kv_rows_total(P), A.status) &&
+                in_range(U.kv_row0 + U.n - 1, kv_rows_total(P), A.status) &&
+                in_range(it.c, A.chunks, A.status);
             if constexpr (kX) {
                 const int jf = it.t_begin * kTileKeys + key0;
-                vq[0] = jf < U.n ? ld_v2<kCoherent>(u_v2 + jf) : 0.f;
-                vq[1] = jf + 8 < U.n ? ld_v2<kCoherent>(u_v2 + jf + 8) : 0.f;
+                vq[0] = jf < U.n && rows_ok ? ld_v2<kCoherent>(u_v2 + jf) : 0.f;
+                vq[1] = jf + 8 < U.n && rows_ok ? ld_v2<kCoherent>(u_v2 + jf + 8) : 0.f;
             }
             for (int t = it.t_begin; ok && t < it.t_end; ++t, ++tcount) {
                 const int b = (int)(tcount % kBufs);          // TMEM buffer of this tile
@@ -496,8 +510,8 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
                 const float q0 = vq[0], q1 = vq[1];
                 if (kX && t + 1 < it.t_end) {
                     const int jn = (t + 1) * kTileKeys + key0;
-                    vq[0] = jn < U.n ? ld_v2<kCoherent>(u_v2 + jn) : 0.f;
-                    vq[1] = jn + 8 < U.n ? ld_v2<kCoherent>(u_v2 + jn + 8) : 0.f;
+                    vq[0] = jn < U.n && rows_ok ? ld_v2<kCoherent>(u_v2 + jn) : 0.f;
+                    vq[1] = jn + 8 < U.n && rows_ok ? ld_v2<kCoherent>(u_v2 + jn + 8) : 0.f;
                 }
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&tm_full[b], (uint32_t)((tcount / kBufs) & 1), abort_flag,
@@ -544,8 +558,8 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
                 s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
                 s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
                 s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-                if (part == 0 && j0 < U.n) out[j0] = s0;
-                if (part == 1 && j0 + 8 < U.n) out[j0 + 8] = s1;
+                if (part == 0 && j0 < U.n && rows_ok) out[j0] = s0;
+                if (part == 1 && j0 + 8 < U.n && rows_ok) out[j0 + 8] = s1;
             }
         }
         if (!ok) {

@@ -98,6 +98,10 @@ __device__ __forceinline__ void select_unit(const DevProblem &P, const float *sc
         if (tid == 0) post_status(status, KV_ERR_BUDGET);
         return;
     }
+    // the unit's output range and its scores lie inside their arrays
+    if (!in_range(off, offsets[P.units], status) || !in_range(off + b - 1, offsets[P.units], status) ||
+        !in_range(U.kv_row0 + n - 1, kv_rows_total(P), status))
+        return;
     int32_t *out = sel + off;
     for (int j = tid; j < P.sinks; j += kT) out[j] = j;
     for (int t = tid; t < P.w; t += kT) out[b - P.w + t] = n - P.w + t;
@@ -192,7 +196,11 @@ __device__ __forceinline__ void select_unit(const DevProblem &P, const float *sc
         unsigned dst = base_sel + sel_block_scan<kT>(n_keep, sm.warp_sums, &keep_total);
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
-            if (keep_bits & (1u << it)) out[P.sinks + dst++] = c0 + tid * kItems + it;
+            if (keep_bits & (1u << it)) {
+                if (in_range(P.sinks + dst, b - P.w, status))
+                    out[P.sinks + dst] = c0 + tid * kItems + it;
+                ++dst;
+            }
         }
         base_sel += keep_total;
         eq_seen += eq_total;
