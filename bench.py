@@ -534,35 +534,53 @@ def main(argv=None):
         if dist is not None:
             dist.barrier()
 
+    # Inputs smaller than a few L2s (the tiny configuration) would stay in L2 from one
+    # step to the next: then L2 is flushed (a 512 MB buffer written) before every
+    # step, outside its events, and each step is timed alone.
+    n_tot = sum(wl.seq_lengths())
+    kv_in = kv_cache_bytes(wl.num_layers, wl.num_kv_heads, wl.head_dim, n_tot)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if kv_in < 4 * l2_bytes \
+        else None
     sampler = ClockSampler(gpu_uuid(torch, dev))
     sampler.start()
     t_w0 = time.perf_counter()
     for _ in range(max(args.warmup, 0)):
+        if flush is not None:
+            flush.zero_()
         step()
     barrier()
     if args.steps <= 0:
         per = (time.perf_counter() - t_w0) / max(args.warmup, 1)
-        args.steps = int(min(2000, max(20, math.ceil(2.0 / max(per, 1e-4)))))
+        args.steps = int(min(20000 if flush is not None else 2000,
+                             max(20, math.ceil(2.0 / max(per, 1e-4)))))
+    # per-stage events on every step when each step is timed alone, else on the
+    # first 200 timed steps (the step time itself spans all of them)
+    staged = args.steps if flush is not None else min(args.steps, 200)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
-           for _ in range(args.steps)]
+           for _ in range(staged)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        if flush is not None:
+            flush.zero_()
+        step(evs[i] if i < staged else None)
     t_end.record(stream)
     barrier()
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        total_ms = sum(evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps))
+    else:
+        total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, dist, dev)
     st = (kv.kv_check_status(bufs.score_ws, stream),
           kv.kv_check_status(bb.select_ws if blk else bufs.select_ws, stream))
     if st != (0, 0):
         raise SystemExit("device status after the timed region: %s" % (st,))
     stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
-                                   for i in range(args.steps)) for j, s in enumerate(stage_names)}
+                                   for i in range(staged)) for j, s in enumerate(stage_names)}
     ms_per_step = total_ms / args.steps
-    n_tot = sum(wl.seq_lengths())
     unit_tokens = n_tot * wl.num_layers * wl.num_kv_heads
     value = whole_job_rate(unit_tokens, world, ms_per_step)
     alg_bytes = algorithmic_bytes(wl, budgets)
@@ -587,6 +605,8 @@ def main(argv=None):
                  "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
                                                   rule, blk)["frac"] for s in stages}})
 
+    launches = (1 if fused else sum(LAUNCHES_PER_STEP[s] for s in stages)
+                + (1 if wl.rows > 128 else 0))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -597,18 +617,19 @@ def main(argv=None):
                        "budget": "%s, mean %s tokens/head" % (wl.budget_policy,
                                                               wl.mean_budgets()),
                        "units": wl.num_units, "parallelism": "replicas x%d" % world,
-                       "l2": "no flush: the K+V inputs (%.1f GB) exceed L2 every step"
-                             % (kv_cache_bytes(wl.num_layers, wl.num_kv_heads, wl.head_dim,
-                                               n_tot) / 1e9)},
+                       "l2": ("flushed before every step (512 MB written outside the step's "
+                              "events; each step timed alone): the K+V inputs (%.2f MB) fit "
+                              "in L2" % (kv_in / 1e6)) if flush is not None else
+                             "no flush: the K+V inputs (%.1f GB) exceed L2 every step"
+                             % (kv_in / 1e9)},
             "seq_tokens_per_s": n_tot * world / (ms_per_step * 1e-3),
             "hbm": {"alg_bytes_per_step": alg_bytes, "achieved_gbs": hbm_gbs,
                     "peak_gbs": peaks["hbm_gbs"], "frac": hbm_gbs / peaks["hbm_gbs"],
                     "peak_source": peak_src},
             "stages_ms": stage_ms,
             "roofline": roof,
-            "gpu_launches": args.steps * (1 if fused else
-                                          sum(LAUNCHES_PER_STEP[s] for s in stages)
-                                          + (1 if wl.rows > 128 else 0)),
+            "gpu_launches": args.steps * launches,
+            "us_per_launch": ms_per_step * 1e3 / launches,
             "clocks": clocks}
 
     if not args.no_e2e:
@@ -645,25 +666,41 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
     only allocates its buffers) overlaps the copies of one layer group with the
     work on another; block eviction copies everything in, then runs."""
     if bb is None:
+        # inputs page-locked at their exact size, unless that would lock more than
+        # 60% of the host's memory (then pageable: the copies no longer overlap)
+        in_bytes = sum(t.numel() * t.element_size() for t in (dw.q, dw.k, dw.v))
+        out_bytes = bufs.total_rows * (4 + 2 * wl.head_dim * 2)
+        host_ram = host_memory_bytes()
+        pin_inputs = in_bytes + out_bytes <= 0.6 * host_ram
+        held = []
         try:
-            qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)
-            kh = torch.empty(dw.k.shape, dtype=dw.k.dtype, pin_memory=True)
-            vh = torch.empty(dw.v.shape, dtype=dw.v.dtype, pin_memory=True)
+            if pin_inputs:
+                held = [kv.PinnedTensor(t.shape, t.dtype) for t in (dw.q, dw.k, dw.v)]
+                qh, kh, vh = (p.t for p in held)
+            else:
+                qh, kh, vh = (torch.empty(t.shape, dtype=t.dtype) for t in (dw.q, dw.k, dw.v))
             qh.copy_(dw.q)
             kh.copy_(dw.k)
             vh.copy_(dw.v)
             pipe = kv.HostPipeline(prob, budgets, group_layers=4,
                                    fused=bool(getattr(args, "fused", False)))
         except RuntimeError as e:
-            return {"value": None, "unit": UNIT, "error": "pinned host allocation failed: %s" % e}
+            return {"value": None, "unit": UNIT, "error": "host allocation failed: %s" % e}
         pipe.run(qh, kh, vh)
         dt, spread = _timed_steps(args.e2e_steps, lambda: pipe.run(qh, kh, vh), torch)
-        return {"value": unit_tokens / dt, "unit": UNIT, "ms_per_step": dt * 1e3,
-                "ms_per_step_min_max": spread,
-                "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
-                "steps": args.e2e_steps, "statistic": "median of per-step host wall times",
-                "api": "kv_evict_host (C ABI), groups of 4 layers%s"
-                       % (", fused launch per group" if pipe.fused else "")}
+        out = {"value": unit_tokens / dt, "unit": UNIT, "ms_per_step": dt * 1e3,
+               "ms_per_step_min_max": spread,
+               "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
+               "steps": args.e2e_steps, "statistic": "median of per-step host wall times",
+               "api": "kv_evict_host (C ABI), groups of 4 layers%s"
+                      % (", fused launch per group" if pipe.fused else ""),
+               "host_inputs": "pinned (cudaHostRegister, exact size)" if pin_inputs else
+                              "pageable: pinning %.0f GB would lock over 60%% of the %.0f GB "
+                              "of host memory available" % ((in_bytes + out_bytes) / 1e9,
+                                                            host_ram / 1e9)}
+        for p in held:
+            p.close()
+        return out
     try:
         qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)
         kh = torch.empty(dw.k.shape, dtype=dw.k.dtype, pin_memory=True)
@@ -700,6 +737,28 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
     return {"value": unit_tokens / dt, "unit": UNIT, "ms_per_step": dt * 1e3,
             "ms_per_step_min_max": spread, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": args.e2e_steps, "statistic": "median of per-step host wall times"}
+
+
+def host_memory_bytes() -> int:
+    """Host memory this process may use: the smallest of MemAvailable, the cgroup
+    limit (a container's can be far below the machine's RAM) and physical RAM."""
+    cands = [os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")]
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    cands.append(int(ln.split()[1]) * 1024)
+    except OSError:
+        pass
+    for path in ("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory/memory.limit_in_bytes"):
+        try:
+            with open(path) as f:
+                v = f.read().strip()
+            if v.isdigit():
+                cands.append(int(v))
+        except OSError:
+            pass
+    return min(cands)
 
 
 def _timed_steps(steps, fn, torch):

@@ -27,7 +27,7 @@ __all__ = ["KvError", "Problem", "load", "build", "kv_score", "kv_score_attentio
            "kv_check_status", "kv_score_noalloc", "kv_budgets_pyramid", "kv_budgets_ripple", "kv_budgets_uniform",
            "kv_set_wait_limit_ns", "kv_get_wait_limit_ns", "kv_pool_scores", "kv_head_budgets",
            "kv_block_scores", "kv_compact_blocks", "kv_budgets_fraction", "BlockBuffers",
-           "evict_blocks", "EXPORTED_SYMBOLS", "HostPipeline", "kv_evict_host",
+           "evict_blocks", "EXPORTED_SYMBOLS", "HostPipeline", "PinnedTensor", "kv_evict_host",
            "kv_evict_host_workspace_size",
            "evict", "KV_SCORE_DROPKV", "KV_SCORE_DROPKV_SQUARED", "KV_SCORE_ATTN_SUM"]
 
@@ -515,6 +515,37 @@ def kv_evict_host(prob: Problem, plan, q_host, k_host, v_host, budgets_host: np.
     return st.value
 
 
+class PinnedTensor:
+    """A host tensor page-locked at its exact size (cudaHostRegister on a plain CPU
+    allocation; torch's own pinned allocator rounds every block up to a power of
+    two, which at tens of GB doubles the locked host memory).  `.t` is the tensor;
+    close() (or garbage collection) unregisters it."""
+
+    def __init__(self, shape, dtype):
+        import torch
+        self.t = torch.empty(shape, dtype=dtype)
+        self._ptr = self.t.data_ptr()
+        nbytes = self.t.numel() * self.t.element_size()
+        self._registered = False
+        if nbytes:
+            err = torch._C._cudart.cudaHostRegister(self._ptr, nbytes, 0)
+            if int(err) != 0:
+                raise RuntimeError("cudaHostRegister of %d bytes failed (%s)" % (nbytes, err))
+            self._registered = True
+
+    def close(self):
+        if self._registered:
+            import torch
+            torch._C._cudart.cudaHostUnregister(self._ptr)
+            self._registered = False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class HostPipeline:
     """Eviction of a problem whose Q, K and V are in host memory, through kv_evict_host.
 
@@ -545,9 +576,9 @@ class HostPipeline:
         nbytes = kv_evict_host_workspace_size(prob, self.plan, self.budgets_host)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         rows, d = max(self.total_rows, 1), prob.head_dim
-        self.sel_host = torch.empty(rows, dtype=torch.int32, pin_memory=True)
-        self.k_out_host = torch.empty((rows, d), dtype=torch.bfloat16, pin_memory=True)
-        self.v_out_host = torch.empty_like(self.k_out_host, pin_memory=True)
+        self._pinned = [PinnedTensor(rows, torch.int32), PinnedTensor((rows, d), torch.bfloat16),
+                        PinnedTensor((rows, d), torch.bfloat16)]
+        self.sel_host, self.k_out_host, self.v_out_host = (b.t for b in self._pinned)
 
     @property
     def h2d_bytes(self) -> int:
