@@ -141,16 +141,18 @@ kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const 
 /*
  * Pass 1: causal window attention of every unit with split-K over the keys and
  * a merge of the splits (row max, row sum and a = sum p v); leaves them in the
- * workspace for pass 2.  Starts a new status sequence (zeroes status word 0).
- * The product p v runs with p and v in fp16: V values must be finite and below
- * 65504 in magnitude (bf16 values in that range convert exactly down to
- * 2^-14 = 6.1e-5; smaller magnitudes keep an absolute error below 3e-8).  A
- * larger value posts KV_ERR_UNSUPPORTED to the status word, and so does a block
- * of 64 V rows as the kernel reads them (64-aligned within the unit; the block
- * at a unit's end also holds the rows that follow it in memory) whose values
- * are not all zero but all below 2^-14 in magnitude, where fp16 keeps too few
- * bits for the score's tolerance (V scaled far below the usual range).  Rules
- * that do not read V (KV_SCORE_ATTN_SUM) have neither limit.
+ * workspace for pass 2.  Starts a new status sequence (zeroes the status word).
+ * When the G*w window rows fit one 128-row chunk, p v multiplies bf16 v by p as
+ * a bf16 hi/lo pair: V may take any finite bf16 value.  With more window rows it
+ * runs with p and v in fp16: V values must then be below 65504 in magnitude
+ * (bf16 values in that range convert exactly down to 2^-14 = 6.1e-5; smaller
+ * magnitudes keep an absolute error below 3e-8).  A larger value posts
+ * KV_ERR_UNSUPPORTED to the status word, and so does a block of 64 V rows as the
+ * kernel reads them (64-aligned within the unit; the block at a unit's end also
+ * holds the rows that follow it in memory) whose values are not all zero but all
+ * below 2^-14 in magnitude, where fp16 keeps too few bits for the score's
+ * tolerance (V scaled far below the usual range).  Rules that do not read V
+ * (KV_SCORE_ATTN_SUM) have neither limit.
  */
 kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void *k,
                              const void *v, void *workspace, size_t workspace_bytes,
@@ -383,11 +385,12 @@ kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status)
  *    device) race on it, so order them on one stream.
  *  - Argument and launch errors are returned.  The device-side status that
  *    kv_score posts to its workspace (kv_check_status) lands in the shared
- *    array and is not reported here: a wait that expired (KV_ERR_TIMEOUT) and
- *    V values outside what pass 1 carries in fp16 (KV_ERR_UNSUPPORTED: |v| of
- *    65504 or more, or 64-row blocks of values all below 2^-14; see
- *    kv_score_attention) then leave wrong scores without an error.  Callers
- *    whose V may leave that range should use kv_score with a workspace.
+ *    array and is not reported here: a wait that expired (KV_ERR_TIMEOUT) and,
+ *    with more than 128 window rows, V values outside what pass 1 carries in
+ *    fp16 (KV_ERR_UNSUPPORTED: |v| of 65504 or more, or 64-row blocks of values
+ *    all below 2^-14; see kv_score_attention) then leave wrong scores without
+ *    an error.  Callers whose V may leave that range should use kv_score with a
+ *    workspace.
  */
 kv_status kv_score_noalloc(const kv_problem *p, const void *q_win, const void *k,
                            const void *v, float *scores, void *stream);

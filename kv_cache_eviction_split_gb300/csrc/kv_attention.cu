@@ -10,14 +10,15 @@ namespace {
 using namespace sm100;
 using namespace pass1;
 
-template <int D>
+template <int D, bool kOneQ>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const AttnArgs A) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const uint32_t tmem = tmem_acquire_all(reinterpret_cast<uint32_t *>(smem + Layout<D>::kMisc));
-    attn_tc_body<D>(P, &tm_q, &tm_k, &tm_v, A, smem, tmem, blockIdx.x, gridDim.x);
+    const uint32_t tmem =
+        tmem_acquire_all(reinterpret_cast<uint32_t *>(smem + Layout<D, kOneQ>::kMisc));
+    attn_tc_body<D, kOneQ>(P, &tm_q, &tm_k, &tm_v, A, smem, tmem, blockIdx.x, gridDim.x);
     tmem_release_all(tmem);
 }
 
@@ -64,9 +65,20 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
             attn_stats_kernel<D><<<(unsigned)grid, kStatThreads, smem, st>>>(P, mq, mk, A);
         return cudaGetLastError();
     }
-    const int smem = Layout<D>::kTotal;
-    cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (grid > 0) attn_tc_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
+    // one row chunk (lanes on alternate tiles): one Q slot and a third V stage
+    if (A.parts == 2) {
+        const int smem = Layout<D, true>::kTotal;
+        cudaFuncSetAttribute(attn_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+        if (grid > 0)
+            attn_tc_kernel<D, true><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
+    } else {
+        const int smem = Layout<D, false>::kTotal;
+        cudaFuncSetAttribute(attn_tc_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (grid > 0)
+            attn_tc_kernel<D, false><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
+    }
     return cudaGetLastError();
 }
 

@@ -61,8 +61,10 @@ __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 template <int D, int RULE>
 struct FusedSmem {
-    static constexpr int kP1 = RULE == KV_SCORE_ATTN_SUM ? pass1::StatLayout<D>::kTotal
-                                                          : pass1::Layout<D>::kTotal;
+    static constexpr int kP1 = RULE == KV_SCORE_ATTN_SUM
+                                   ? pass1::StatLayout<D>::kTotal
+                                   : cmax(pass1::Layout<D, false>::kTotal,
+                                          pass1::Layout<D, true>::kTotal);
     static constexpr int kP2 = pass2::Layout<D, RULE>::kTotal;
     static constexpr int kSel = sel_smem_bytes<kFusedThreads, kFusedSelItems>();
     static constexpr int kSlot = (cmax(cmax(kP1, kP2), kSel) + 15) / 16 * 16;
@@ -208,8 +210,10 @@ fused_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
         if constexpr (RULE == KV_SCORE_ATTN_SUM)
             pass1::attn_stats_body<D>(P, &tm_q, &tm_k, F.a1, smem, tmem, cta, ncta);
+        else if (F.a1.parts == 2)   // one row chunk: one Q slot, a third V stage
+            pass1::attn_tc_body<D, true>(P, &tm_q, &tm_k, &tm_v, F.a1, smem, tmem, cta, ncta);
         else
-            pass1::attn_tc_body<D>(P, &tm_q, &tm_k, &tm_v, F.a1, smem, tmem, cta, ncta);
+            pass1::attn_tc_body<D, false>(P, &tm_q, &tm_k, &tm_v, F.a1, smem, tmem, cta, ncta);
     }
     ok = barrier() && ok;
     // 2. merge: one warp per (unit, row)

@@ -34,8 +34,9 @@
 // The attention-sum rule needs only m and l: attn_stats_kernel (below) computes
 // them from K alone.
 //
-// Warp roles (384 threads): warp 0 TMA producer (the lanes' Q chunks per item;
-// K tiles through a 3-stage ring running ahead of V tiles in a 2-stage ring);
+// Warp roles (384 threads): warp 0 TMA producers (lane 0: the lanes' Q chunks per
+// item and K tiles through a 3-stage ring; lane 1: V tiles through a 2- or
+// 3-stage ring, each lane running as far ahead as its ring allows);
 // warp 1 TMEM owner and MMA issuer; warps 2-5 softmax of lane 0, 6-9 of lane 1;
 // warps 10-11 convert every V tile to fp16 as it lands (and compute ||v_j||^2),
 // so neither lane's softmax waits for V or for the other lane.
@@ -59,8 +60,6 @@ using namespace sm100;
 
 constexpr int kTileKeys = 128;
 constexpr int kChunkRows = 128;
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
 constexpr int kSoftWarps = 8;       // 4 per lane
 constexpr int kConvWarps = 2;       // V tiles to fp16, ||v||^2
 constexpr int kThreads = (2 + kSoftWarps + kConvWarps) * 32;
@@ -71,14 +70,21 @@ constexpr int kBlockBytes = 128 * 128;   // [128 rows][64 bf16], 128 B swizzle
 constexpr float kRescaleLog2 = 2.f;
 constexpr float kPScaleLog2 = 13.f;    // P' = p 2^13 in fp16
 
-template <int D>
+// Shared memory of attn_tc_body.  With two row chunks per item (chunk pairs) the
+// CTA keeps both chunks' Q tiles, a 3-stage K ring and a 2-stage V ring.  With a
+// single chunk (the lanes on alternate tiles; kOneQ) one Q tile serves both lanes
+// and the second Q slot holds a third V stage.
+template <int D, bool kOneQ = false>
 struct Layout {
     static constexpr int kOp = (D / 64) * kBlockBytes;   // [128][D] bf16
+    static constexpr int kQSlots = kOneQ ? 1 : 2;
+    static constexpr int kKSt = 3;
+    static constexpr int kVSt = kOneQ ? 3 : 2;
     static constexpr int kQ = 0;                          // Q of lane 0, then lane 1
-    static constexpr int kK = kQ + 2 * kOp;
-    static constexpr int kV = kK + kKStages * kOp;
-    static constexpr int kBars = kV + kVStages * kOp;
-    static constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 2 + 4 * 2 + 1;
+    static constexpr int kK = kQ + kQSlots * kOp;
+    static constexpr int kV = kK + kKSt * kOp;
+    static constexpr int kBars = kV + kVSt * kOp;
+    static constexpr int kNumBars = 2 * kKSt + 3 * kVSt + 2 + 4 * 2 + 1;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kTotal = kMisc + 16;
 };
@@ -161,6 +167,19 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Two fp32 values as bf16x2 (round to nearest), the first in the low half.
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// P' of two keys as a bf16 pair: hi = bf16(p), lo = bf16(p - hi); hi + lo keeps 16
+// bits of p (bf16 alone keeps 8, fp16 11).
+__device__ __forceinline__ void split_bf162(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf162(p0, p1);
+    lo = pack_bf162(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+
 // Masked form for tiles that reach the observation window: P' for 16 keys, zero
 // for keys after `lim` (tile-local); adds P' to the row sum and stores the 8
 // fp16x2 columns at `col`.
@@ -180,6 +199,27 @@ __device__ __forceinline__ void soft16_masked(const float *v, int j0, int lim, f
         w[h] = pack_half2(p.x, p.y);
     }
     tmem_st8u(col, w);
+}
+
+// As soft16_masked with P' as a bf16 hi/lo pair: the 8 hi columns at `col`, the 8
+// lo columns at `col` + 8 (the single-chunk layout of P in TMEM: per 16-key group
+// q, hi at columns 16q .. 16q+7 and lo at 16q+8 .. 16q+15 of the S buffer).
+__device__ __forceinline__ void soft16_masked_split(const float *v, int j0, int lim, float cs,
+                                                    float negm, float2 &lsum, uint32_t col) {
+    const float2 cs2 = make_float2(cs, cs);
+    const float2 nm2 = make_float2(negm, negm);
+    uint32_t w[16];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+        const int j = 2 * h;
+        const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), cs2, nm2);
+        float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        if (j0 + j > lim) p.x = 0.f;
+        if (j0 + j + 1 > lim) p.y = 0.f;
+        lsum = __fadd2_rn(lsum, p);
+        split_bf162(p.x, p.y, w[h], w[8 + h]);
+    }
+    tmem_st16u(col, w);
 }
 
 // Adds the squares of the two bf16 halves of `w` to `acc` (fp32 products of bf16
@@ -226,14 +266,43 @@ __device__ __forceinline__ float row_half_to_f16(uint8_t *tile, int row, int hal
     return acc[0] + acc[1];
 }
 
-// The kernel body, for CTA `cta` of `ncta` (all threads of the CTA call it;
-// `tmem` is the base of 512 TMEM columns the caller allocated).
+// Sum of the squares of the bf16 values of half of one key row of a swizzled
+// [128][D] tile (as row_half_to_f16, without converting).
 template <int D>
+__device__ __forceinline__ float row_half_sq(const uint8_t *tile, int row, int half) {
+    constexpr int kChunks = D / 16;
+    float acc[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        const int c = half * kChunks + i;
+        const uint4 w = *reinterpret_cast<const uint4 *>(tile + (c >> 3) * kBlockBytes + row * 128 +
+                                                         (((c & 7) ^ (row & 7)) << 4));
+        sq_acc_bf16x2(acc[0], w.x);
+        sq_acc_bf16x2(acc[1], w.y);
+        sq_acc_bf16x2(acc[0], w.z);
+        sq_acc_bf16x2(acc[1], w.w);
+    }
+    return acc[0] + acc[1];
+}
+
+// The kernel body, for CTA `cta` of `ncta` (all threads of the CTA call it;
+// `tmem` is the base of 512 TMEM columns the caller allocated).  kOneQ selects the
+// single-chunk form, for problems whose window rows fit one 128-row chunk
+// (A.parts == 2; other problems post KV_ERR_UNSUPPORTED to it).  There the two
+// lanes take alternate tiles and the tensor pipe has room to spare, while
+// converting every V tile to fp16 would keep the two converter warps busy for
+// most of a tile period (measured ~3600 of ~4000 clocks).  So V stays bf16 as it
+// lands, P is written as a bf16 hi/lo pair (16 bits of p instead of fp16's 11)
+// and P V runs as two MMA groups, P_hi V and P_lo V; the converter warps only
+// compute ||v_j||^2.  V then has the whole bf16 range.
+template <int D, bool kOneQ = false>
 __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorMap *tm_q,
                                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                              const AttnArgs A, uint8_t *smem, uint32_t tmem,
                                              long long cta, long long ncta) {
-    using Ly = Layout<D>;
+    using Ly = Layout<D, kOneQ>;
+    constexpr int kKStages = Ly::kKSt;
+    constexpr int kVStages = Ly::kVSt;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly::kBars);
@@ -249,7 +318,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Ly::kMisc + 4);
 
     if (threadIdx.x == 0) {
-        *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
+        *abort_flag = ((smem_u32(smem) & 1023u) || (kOneQ && A.parts != 2)) ? 1 : 0;
         if (*abort_flag) post_status(A.status, KV_ERR_UNSUPPORTED);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -257,7 +326,10 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            // the last P V reading the stage frees it; in the single-chunk form the
+            // converter warps, which then read the bf16 tile for ||v||^2 alongside
+            // the MMAs, arrive too
+            mbar_init(&v_empty[s], kOneQ ? 1 + kConvWarps : 1);
             mbar_init(&v_conv[s], kConvWarps);
         }
         mbar_init(q_full, 1);
@@ -282,10 +354,14 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
     const bool run = *abort_flag == 0;
 
     if (run && warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producers
+        // Lane 0 loads each item's Q and the K tiles, lane 1 the V tiles, each as
+        // far ahead as its own ring allows: a V tile is requested as soon as its
+        // stage frees, not after the K tiles before it (its HBM latency then hides
+        // behind the tiles in flight).
         if (lane == 0) {
-            long long tcount = 0, icount = 0;   // tiles loaded (both rings), items
-            long long qcount = 0, kiss = 0, viss = 0;   // Q, K and V loads issued
+            long long tcount = 0, icount = 0;   // K tiles loaded, items
+            long long qcount = 0, kiss = 0;     // Q and K loads issued
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
                 const Item it = decode_item(item, A, P);
@@ -304,44 +380,22 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                                     q_full, kb * 64, qy);
                 }
                 ++qcount;
-                // K tiles run `lead` tiles ahead of V tiles: the MMA thread needs
-                // K of the next tile of each lane before V of the current one
                 const int ntiles = it.t1 - it.t0;
-                const int lead = A.parts == 1 ? 1 : 2;
-                for (int i = 0; ok && i < ntiles + lead; ++i) {
-                    if (i < ntiles) {
-                        const long long kc = tcount + i;
-                        const int s = (int)(kc % kKStages);
-                        const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
-                        ok = ok && in_range((it.t0 + i) * kTileKeys, U.n, A.status) &&
-                             in_range(ky, kv_rows_total(P), A.status) &&
-                             mbar_wait(&k_empty[s], (uint32_t)((kc / kKStages) & 1) ^ 1u,
-                                       abort_flag, P.wait_ns);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const long long kc = tcount + i;
+                    const int s = (int)(kc % kKStages);
+                    const int ky = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
+                    ok = in_range((it.t0 + i) * kTileKeys, U.n, A.status) &&
+                         in_range(ky, kv_rows_total(P), A.status) &&
+                         mbar_wait(&k_empty[s], (uint32_t)((kc / kKStages) & 1) ^ 1u, abort_flag,
+                                   P.wait_ns);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[s], Ly::kOp);
 #pragma unroll
-                        for (int kb = 0; kb < D / 64; ++kb)
-                            tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, tm_k,
-                                        &k_full[s], kb * 64, ky);
-                        ++kiss;
-                    }
-                    const int iv = i - lead;
-                    if (iv >= 0 && iv < ntiles) {
-                        const long long vc = tcount + iv;
-                        const int s = (int)(vc % kVStages);
-                        const int vy = (int)(U.kv_row0 + (long long)(it.t0 + iv) * kTileKeys);
-                        ok = in_range((it.t0 + iv) * kTileKeys, U.n, A.status) &&
-                             in_range(vy, kv_rows_total(P), A.status) &&
-                             mbar_wait(&v_empty[s], (uint32_t)((vc / kVStages) & 1) ^ 1u,
-                                       abort_flag, P.wait_ns);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
-#pragma unroll
-                        for (int kb = 0; kb < D / 64; ++kb)
-                            tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, tm_v,
-                                        &v_full[s], kb * 64, vy);
-                        ++viss;
-                    }
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kK + s * Ly::kOp + kb * kBlockBytes, tm_k,
+                                    &k_full[s], kb * 64, ky);
+                    ++kiss;
                 }
                 tcount += ntiles;
                 ++icount;
@@ -357,6 +411,35 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                 const long long uses = kiss / kKStages + ((kiss % kKStages) > s ? 1 : 0);
                 if (uses > 0) mbar_drain(&k_full[s], (uint32_t)((uses - 1) & 1), kDrainNs);
             }
+        } else if (lane == 1) {
+            long long tcount = 0, viss = 0;     // V tiles loaded (= issued)
+            bool ok = true;
+            for (long long item = cta; ok && item < A.total_items; item += ncta) {
+                const Item it = decode_item(item, A, P);
+                const UnitInfo U = unit_info(P, it.u, P.cu);
+                const int ntiles = it.t1 - it.t0;
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const long long vc = tcount + i;
+                    const int s = (int)(vc % kVStages);
+                    const int vy = (int)(U.kv_row0 + (long long)(it.t0 + i) * kTileKeys);
+                    ok = in_range((it.t0 + i) * kTileKeys, U.n, A.status) &&
+                         in_range(vy, kv_rows_total(P), A.status) &&
+                         mbar_wait(&v_empty[s], (uint32_t)((vc / kVStages) & 1) ^ 1u, abort_flag,
+                                   P.wait_ns);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&v_full[s], Ly::kOp);
+#pragma unroll
+                    for (int kb = 0; kb < D / 64; ++kb)
+                        tma_load_2d(smem + Ly::kV + s * Ly::kOp + kb * kBlockBytes, tm_v,
+                                    &v_full[s], kb * 64, vy);
+                    ++viss;
+                }
+                tcount += ntiles;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                post_status(A.status, KV_ERR_TIMEOUT);
+            }
             for (int s = 0; s < kVStages; ++s) {
                 const long long uses = viss / kVStages + ((viss % kVStages) > s ? 1 : 0);
                 if (uses > 0) mbar_drain(&v_full[s], (uint32_t)((uses - 1) & 1), kDrainNs);
@@ -367,6 +450,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(128, kTileKeys);
             const uint32_t idesc_pv = idesc_f16_f32_bmn(128, D);
+            const uint32_t idesc_pv_bf = idesc_bf16_f32_bmn(128, D);
             long long tcount = 0, icount = 0;
             long long sc[2] = {0, 0};   // steps issued per lane
             long long oc[2] = {0, 0};   // items in which the lane took part
@@ -414,8 +498,10 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                                              P.wait_ns);
                     ok = ok && mbar_wait(&p_full[L], (uint32_t)((sc[L] + j) & 1), abort_flag,
                                          P.wait_ns);
-                    ok = ok && mbar_wait(&v_conv[s], (uint32_t)((vc / kVStages) & 1), abort_flag,
-                                         P.wait_ns);
+                    // the single-chunk form multiplies the bf16 tile as it landed; the
+                    // other waits for its conversion to fp16
+                    ok = ok && mbar_wait(kOneQ ? &v_full[s] : &v_conv[s],
+                                         (uint32_t)((vc / kVStages) & 1), abort_flag, P.wait_ns);
                     if (!ok) return;
                     tc_fence_after();
                     const uint64_t vb =
@@ -424,13 +510,24 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                     const uint32_t d_o = tmem + kOCol + 128 * L;
 #pragma unroll
                     for (int q = 0; q < kTileKeys / 16; ++q) {
-                        // keys 16q..16q+15: fp16x2 columns 8q..8q+7
-                        const uint32_t a = pcol + q * 8;
                         const uint64_t bd = sdesc_add(vb, q * 16 * 128);
-                        if (j == 0 && q == 0)
-                            mma_ts_c<false>(d_o, a, bd, idesc_pv);
-                        else
-                            mma_ts_c<true>(d_o, a, bd, idesc_pv);
+                        if constexpr (kOneQ) {
+                            // keys 16q..16q+15: P_hi in bf16x2 columns 16q..16q+7, P_lo in
+                            // 16q+8..16q+15
+                            const uint32_t a = pcol + q * 16;
+                            if (j == 0 && q == 0)
+                                mma_ts_c<false>(d_o, a, bd, idesc_pv_bf);
+                            else
+                                mma_ts_c<true>(d_o, a, bd, idesc_pv_bf);
+                            mma_ts_c<true>(d_o, a + 8, bd, idesc_pv_bf);
+                        } else {
+                            // keys 16q..16q+15: fp16x2 columns 8q..8q+7
+                            const uint32_t a = pcol + q * 8;
+                            if (j == 0 && q == 0)
+                                mma_ts_c<false>(d_o, a, bd, idesc_pv);
+                            else
+                                mma_ts_c<true>(d_o, a, bd, idesc_pv);
+                        }
                     }
                     if (frees(L)) mma_commit(&v_empty[s]);
                 };
@@ -561,9 +658,10 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                         tmem_ld_wait();
                         reg_fence(cur);
                         if (c < 3) tmem_ld32(s_base + 32 * (c + 1), nxt);
-                        // keys 32c..32c+31 -> fp16x2 columns 16c..16c+15: only columns of
-                        // keys already read are overwritten
-                        uint32_t pw[16];
+                        // keys 32c..32c+31 -> fp16x2 columns 16c..16c+15, or in the
+                        // single-chunk form bf16x2 hi/lo columns 32c..32c+31: only
+                        // columns of keys already read are overwritten
+                        uint32_t pw[kOneQ ? 32 : 16];
                         float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                         make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -571,9 +669,16 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                             const float2 t = __ffma2_rn(make_float2(cur[i], cur[i + 1]), cs2, nm2);
                             const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
                             ps[(i / 2) & 3] = __fadd2_rn(ps[(i / 2) & 3], make_float2(p0, p1));
-                            pw[i / 2] = pack_half2(p0, p1);
+                            if constexpr (kOneQ)
+                                split_bf162(p0, p1, pw[(i / 16) * 16 + (i % 16) / 2],
+                                            pw[(i / 16) * 16 + 8 + (i % 16) / 2]);
+                            else
+                                pw[i / 2] = pack_half2(p0, p1);
                         }
-                        tmem_st16u(s_base + 16 * c, pw);
+                        if constexpr (kOneQ)
+                            tmem_st32u(s_base + 32 * c, pw);
+                        else
+                            tmem_st16u(s_base + 16 * c, pw);
                         lsum = __fadd2_rn(lsum, __fadd2_rn(__fadd2_rn(ps[0], ps[1]),
                                                            __fadd2_rn(ps[2], ps[3])));
                     }
@@ -584,7 +689,10 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                         tmem_ld16(s_base + 16 * c, sv);
                         tmem_ld_wait();
                         reg_fence(sv);
-                        soft16_masked(sv, 16 * c, lim, cs, negm, lsum, s_base + 8 * c);
+                        if constexpr (kOneQ)
+                            soft16_masked_split(sv, 16 * c, lim, cs, negm, lsum, s_base + 16 * c);
+                        else
+                            soft16_masked(sv, 16 * c, lim, cs, negm, lsum, s_base + 8 * c);
                     }
                 }
                 l += lsum.x + lsum.y;
@@ -646,6 +754,23 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
                                                        abort_flag, P.wait_ns));
                 if (!ok) break;
                 uint8_t *tile = smem + Ly::kV + s * Ly::kOp;
+                if constexpr (kOneQ) {
+                    // ||v||^2 of the bf16 tile, read alongside the MMAs; then this
+                    // warp's share of the stage's release
+#pragma unroll 1
+                    for (int k0 = 0; k0 < 64; k0 += 16) {
+                        const int row = cw * 64 + k0 + (lane & 15);
+                        float q = row_half_sq<D>(tile, row, lane >> 4);
+                        q += __shfl_xor_sync(0xffffffffu, q, 16);
+                        const int j = (it.t0 + ti) * kTileKeys + row;
+                        if (lane < 16 && j < U.n &&
+                            in_range(U.kv_row0 + j, kv_rows_total(P), A.status))
+                            A.v2[U.kv_row0 + j] = q;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&v_empty[s]);
+                    continue;
+                }
                 bool bad = false;
                 uint32_t nz = 0, nrm = 0;
 #pragma unroll 1

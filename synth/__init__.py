@@ -444,6 +444,9 @@ PROFILE_CASES = [
                      num_kv_heads=2, num_q_heads=8),
     QWEN7B_128K.scaled(name="qwen7b_2L_2kv_14q_d128_n131072_ripple5", num_layers=2,
                        num_kv_heads=2, num_q_heads=14),
+    LLAMA8B_32K.scaled(name="llama8b_2L_8kv_32q_d128_n32768", num_layers=2),
+    RAGGED_MISTRAL.scaled(name="ragged8_mistral7b_2L_2kv_8q_d128_n16k-128k", num_layers=2,
+                          num_kv_heads=2, num_q_heads=8),
 ]
 BY_NAME = {c.name: c for c in CONFIGS + PROFILE_CASES}
 

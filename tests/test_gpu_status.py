@@ -152,13 +152,16 @@ def test_each_scoring_call_starts_a_new_status(cuda_lib):
 
 
 def test_tiny_value_block_reports_unsupported_and_zero_v_does_not(cuda_lib):
-    """fp16 keeps few bits of values below 2^-14: a block of 64 V rows whose values
-    are all that small (but not all zero) is refused; V that is exactly zero is
-    carried exactly and accepted."""
+    """fp16 keeps few bits of values below 2^-14: when P V runs in fp16 (window rows
+    over one 128-row chunk), a block of 64 V rows whose values are all that small
+    (but not all zero) is refused; V that is exactly zero is carried exactly and
+    accepted."""
     import torch
     from synth.device import DeviceWorkload
     kv = cuda_lib
-    wl = synth.small_variant(synth.LLAMA8B_32K, 1200, layers=1, kv_heads=2)
+    wl = synth.small_variant(synth.LONG_128K, 1200, layers=1, kv_heads=2).scaled(
+        budget_policy="uniform")
+    assert wl.rows > 128
     dw = DeviceWorkload(wl)
     prob = kv.Problem.for_workload(wl)
     ws = torch.zeros(kv.kv_score_workspace_size(prob), dtype=torch.uint8, device="cuda")
@@ -172,3 +175,32 @@ def test_tiny_value_block_reports_unsupported_and_zero_v_does_not(cuda_lib):
     kv.kv_score(prob, dw.q, dw.k, dw.v, scores, ws)
     assert kv.kv_check_status(ws) == kv.KV_OK
     assert float(scores[0, 1].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("scale", [1.0e5, 1.0e-6], ids=["huge", "tiny"])
+def test_single_chunk_form_takes_the_whole_bf16_range(cuda_lib, scale):
+    """With the window rows in one 128-row chunk, P V multiplies bf16 V by P as a
+    bf16 hi/lo pair: V values fp16 cannot hold (|v| >= 65504, or all below 2^-14)
+    are accepted and scored to the oracle's tolerance."""
+    from synth.device import DeviceWorkload
+    from tests import parity
+    kv = cuda_lib
+    wl = synth.small_variant(synth.LLAMA8B_32K, 1500, layers=1, kv_heads=2)
+    assert wl.rows <= 128
+    dw = DeviceWorkload(wl)
+    dw.v[0, 1, 100:400] *= scale          # a stretch of unit (0, 0, 1)
+    budgets = np.full((1, 1, 2), 200, dtype=np.int32)
+    run = parity.DeviceRun(kv, wl, budgets=budgets, dw=dw)
+    assert run.status_score == kv.KV_OK and run.status_select == kv.KV_OK
+    # the oracle's input: the host regeneration with the same scaling (an fp32
+    # product rounded to bf16, as torch's bf16 multiply does), checked against the
+    # device's bits
+    import torch
+    import oracle
+    q, k, v = dw.unit_host(0, 0, 1)
+    v = v.copy()
+    v[100:400] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(v[100:400]) * np.float32(scale))
+    dev = dw.v[0, 1].cpu().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(dev, v)
+    S = oracle.unit_scores_rule(q, k, v, wl.group, wl.window, 0)
+    parity.check_unit(run, 0, 0, 1, oracle_out=(q, k, v, S))
