@@ -672,11 +672,9 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
         out_bytes = bufs.total_rows * (4 + 2 * wl.head_dim * 2)
         host_ram = host_memory_bytes()
         pin_inputs = in_bytes + out_bytes <= 0.6 * host_ram
-        held = []
         try:
             if pin_inputs:
-                held = [kv.PinnedTensor(t.shape, t.dtype) for t in (dw.q, dw.k, dw.v)]
-                qh, kh, vh = (p.t for p in held)
+                qh, kh, vh = (kv.PinnedTensor(tuple(t.shape), t.dtype) for t in (dw.q, dw.k, dw.v))
             else:
                 qh, kh, vh = (torch.empty(t.shape, dtype=t.dtype) for t in (dw.q, dw.k, dw.v))
             qh.copy_(dw.q)
@@ -694,12 +692,11 @@ def e2e_measure(args, kv, torch, wl, dw, prob, bufs, stream, unit_tokens, bb=Non
                "steps": args.e2e_steps, "statistic": "median of per-step host wall times",
                "api": "kv_evict_host (C ABI), groups of 4 layers%s"
                       % (", fused launch per group" if pipe.fused else ""),
-               "host_inputs": "pinned (cudaHostRegister, exact size)" if pin_inputs else
+               "host_inputs": "pinned (cudaHostAlloc, exact size)" if pin_inputs else
                               "pageable: pinning %.0f GB would lock over 60%% of the %.0f GB "
                               "of host memory available" % ((in_bytes + out_bytes) / 1e9,
                                                             host_ram / 1e9)}
-        for p in held:
-            p.close()
+        del qh, kh, vh, pipe
         return out
     try:
         qh = torch.empty(dw.q.shape, dtype=dw.q.dtype, pin_memory=True)

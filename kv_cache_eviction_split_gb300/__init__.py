@@ -515,35 +515,64 @@ def kv_evict_host(prob: Problem, plan, q_host, k_host, v_host, budgets_host: np.
     return st.value
 
 
-class PinnedTensor:
-    """A host tensor page-locked at its exact size (cudaHostRegister on a plain CPU
-    allocation; torch's own pinned allocator rounds every block up to a power of
-    two, which at tens of GB doubles the locked host memory).  `.t` is the tensor;
-    close() (or garbage collection) unregisters it."""
+_cudart_lib = None
 
-    def __init__(self, shape, dtype):
-        import torch
-        self.t = torch.empty(shape, dtype=dtype)
-        self._ptr = self.t.data_ptr()
-        nbytes = self.t.numel() * self.t.element_size()
-        self._registered = False
-        if nbytes:
-            err = torch._C._cudart.cudaHostRegister(self._ptr, nbytes, 0)
-            if int(err) != 0:
-                raise RuntimeError("cudaHostRegister of %d bytes failed (%s)" % (nbytes, err))
-            self._registered = True
 
-    def close(self):
-        if self._registered:
-            import torch
-            torch._C._cudart.cudaHostUnregister(self._ptr)
-            self._registered = False
+def _cudart():
+    """The CUDA runtime library torch loaded (for cudaHostAlloc / cudaFreeHost)."""
+    global _cudart_lib
+    if _cudart_lib is None:
+        import torch  # noqa: F401  (loads the runtime)
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                lib = ctypes.CDLL(name)
+            except OSError:
+                continue
+            lib.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                                          ctypes.c_uint]
+            lib.cudaHostAlloc.restype = ctypes.c_int
+            lib.cudaFreeHost.argtypes = [ctypes.c_void_p]
+            lib.cudaFreeHost.restype = ctypes.c_int
+            _cudart_lib = lib
+            break
+    return _cudart_lib
+
+
+class _HostAllocation:
+    """One cudaHostAlloc block, freed when the last tensor viewing it is gone."""
+
+    def __init__(self, nbytes: int):
+        self.ptr = None
+        lib = _cudart()
+        if lib is None:
+            raise RuntimeError("no CUDA runtime library to page-lock host memory with")
+        p = ctypes.c_void_p()
+        err = lib.cudaHostAlloc(ctypes.byref(p), ctypes.c_size_t(nbytes), 0)
+        if err != 0 or not p.value:
+            raise RuntimeError("cudaHostAlloc of %d bytes failed (error %d)" % (nbytes, err))
+        self.ptr = p.value
+        self.lib = lib
 
     def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
+        if self.ptr:
+            self.lib.cudaFreeHost(ctypes.c_void_p(self.ptr))
+            self.ptr = None
+
+
+def PinnedTensor(shape, dtype):
+    """A page-locked host tensor of exactly its size (cudaHostAlloc; torch's own
+    pinned allocator rounds every block up to a power of two, which at tens of GB
+    nearly doubles the locked host memory).  The allocation lives as long as any
+    tensor that views it."""
+    import torch
+    numel = int(np.prod(shape)) if isinstance(shape, (tuple, list)) else int(shape)
+    elsize = torch.empty((), dtype=dtype).element_size()
+    nbytes = max(numel * elsize, elsize)
+    block = _HostAllocation(nbytes)
+    buf = (ctypes.c_uint8 * nbytes).from_address(block.ptr)
+    buf._owner = block                      # the buffer, hence every view, holds the block
+    arr = np.frombuffer(buf, dtype=np.uint8, count=nbytes)
+    return torch.from_numpy(arr).view(dtype)[:numel].view(shape)
 
 
 class HostPipeline:
@@ -565,8 +594,9 @@ class HostPipeline:
         dev = prob.cu_dev.device
         self.prob = prob
         self.fused = fused
-        self.group_layers = group_layers
         L = prob.num_layers
+        group_layers = max(1, min(int(group_layers), L))
+        self.group_layers = group_layers
         self.groups = [(l0, min(L, l0 + group_layers)) for l0 in range(0, L, group_layers)]
         self.plan = _KvHostPlan(int(group_layers), int(prob.pool_kernel), int(prob.head_budgets),
                                 int(fused))
@@ -576,9 +606,9 @@ class HostPipeline:
         nbytes = kv_evict_host_workspace_size(prob, self.plan, self.budgets_host)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         rows, d = max(self.total_rows, 1), prob.head_dim
-        self._pinned = [PinnedTensor(rows, torch.int32), PinnedTensor((rows, d), torch.bfloat16),
-                        PinnedTensor((rows, d), torch.bfloat16)]
-        self.sel_host, self.k_out_host, self.v_out_host = (b.t for b in self._pinned)
+        self.sel_host = PinnedTensor(rows, torch.int32)
+        self.k_out_host = PinnedTensor((rows, d), torch.bfloat16)
+        self.v_out_host = PinnedTensor((rows, d), torch.bfloat16)
 
     @property
     def h2d_bytes(self) -> int:
