@@ -274,11 +274,26 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
                  "blocks": "block_sum_kernel", "pool": "pool_kernel", "heads": "hb_hist_kernel",
                  "select": "select_kernel", "compact": "compact_range_kernel"}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a stage's
-# kernel at full size, keyed by (workload, score rule, pool kernel, fused).  Each
-# entry records the kernel sources it was measured on ("src": kernel_source_hash()
-# at capture time), the ncu case it came from and the factor that scales that
-# case to the full workload; bench reports traffic as null once the sources differ.
-TRAFFIC = {}
+# kernel at full size, keyed by (workload, score rule, pool kernel, fused): one ncu
+# launch of a reduced copy of the workload (the same per-unit shapes, fewer units)
+# scaled by the ratio of units.  Each entry records the kernel sources it was
+# measured on ("src": kernel_source_hash() at capture time), the reduced case and
+# the scale factor; bench reports traffic as null once the sources differ.
+TRAFFIC = {
+    ("long_32L_8kv_32q_d128_n131072_pyramid10", "dropkv", 1, False): {
+        "src": "8418bf39adb90461", "case": "long_2L_2kv_8q_d128_n131072_pyramid10", "scale": 64,
+        "bytes": {"attn_tc_kernel": 17510416384, "rescore_tc_kernel": 17570955264}},
+    ("llama8b_32L_8kv_32q_d128_n32768", "dropkv", 1, False): {
+        "src": "8418bf39adb90461", "case": "llama8b_2L_8kv_32q_d128_n32768", "scale": 16,
+        "bytes": {"attn_tc_kernel": 4378079232, "rescore_tc_kernel": 4378660864}},
+    ("qwen7b_28L_4kv_28q_d128_n131072_ripple5", "dropkv", 1, False): {
+        "src": "8418bf39adb90461", "case": "qwen7b_2L_2kv_14q_d128_n131072_ripple5", "scale": 28,
+        "bytes": {"attn_tc_kernel": 8149292032, "rescore_tc_kernel": 7809055744}},
+    ("ragged8_mistral7b_32L_8kv_32q_d128_n16k-128k", "dropkv", 1, False): {
+        "src": "8418bf39adb90461", "case": "ragged8_mistral7b_2L_2kv_8q_d128_n16k-128k",
+        "scale": 64,
+        "bytes": {"attn_tc_kernel": 91479998464, "rescore_tc_kernel": 88477859840}},
+}
 
 
 def kernel_source_hash() -> str:
