@@ -74,6 +74,9 @@ def parse_args(argv=None):
                          "(kv_evict_fused); no pooling, per-head budgets or blocks")
     ap.add_argument("--block-layers", type=int, default=0,
                     help="block eviction over blocks of this many layers (0: off)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step (every call of the path) in a CUDA graph after the "
+                         "warm-up and time its replays; stage times come from eager steps")
     return ap.parse_args(argv)
 
 
@@ -348,6 +351,8 @@ def bench_config_tag(wl, args):
     tag = {"workload": wl.name}
     if getattr(args, "fused", False):
         tag["launch"] = "fused: one cooperative kernel per step"
+    if getattr(args, "graph", False):
+        tag["graph"] = "one step captured in a CUDA graph, replayed per timed step"
     if args.score_rule != "dropkv" or args.pool > 1 or args.head_budgets or args.block_layers:
         tag.update(score_rule=args.score_rule, pool_kernel=args.pool,
                    head_budgets=bool(args.head_budgets))
@@ -485,7 +490,10 @@ def main(argv=None):
     prob = kv.Problem.for_workload(wl, device=dev, score_rule=rule, pool_kernel=pool,
                                    head_budgets=heads)
     bufs = kv.Buffers(prob, budgets)
-    stream = torch.cuda.current_stream(dev)
+    # a graph is captured on a side stream; everything else then runs there too
+    stream = torch.cuda.Stream(dev) if args.graph else torch.cuda.current_stream(dev)
+    if args.graph:
+        stream.wait_stream(torch.cuda.current_stream(dev))
     ranked = bufs.pooled if pool > 1 else bufs.scores
     bb = None
     if blk:
@@ -576,16 +584,45 @@ def main(argv=None):
            for _ in range(staged)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        step(evs[i] if i < staged else None)
-    t_end.record(stream)
+    graph = None
+    if args.graph:
+        # stage times from eager steps (a replay records no per-stage events), then
+        # one step captured and its replays timed
+        staged = min(args.steps, 50)
+        evs = evs[:staged]
+        for i in range(staged):
+            if flush is not None:
+                flush.zero_()
+            step(evs[i])
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                    for _ in range(args.steps)] if flush is not None else None
+        barrier()
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                if flush is not None:
+                    flush.zero_()
+                    step_evs[i][0].record(stream)
+                graph.replay()
+                if flush is not None:
+                    step_evs[i][1].record(stream)
+            t_end.record(stream)
+    else:
+        t_start.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            step(evs[i] if i < staged else None)
+        t_end.record(stream)
     barrier()
     clocks = sampler.stop()
     if flush is not None:
-        total_ms = sum(evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps))
+        total_ms = sum((step_evs[i][0].elapsed_time(step_evs[i][1]) for i in range(args.steps))
+                       if graph is not None else
+                       (evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)))
     else:
         total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, dist, dev)
