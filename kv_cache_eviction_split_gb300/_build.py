@@ -81,7 +81,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None,
         with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
             objs = list(ex.map(compile_one, _sources()))
         tmp = lib_path + ".%d.tmp" % os.getpid()
-        cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+        cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static", "-ldl"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("nvcc link failed:\n%s%s" % (res.stdout, res.stderr))

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "kv_internal.cuh"
+#include "kv_trace.cuh"
 
 using namespace kvevict;
 
@@ -166,6 +167,7 @@ static kv_status check_score_args(const kv_problem *p, DevProblem *P, const void
 
 kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void *k, const void *v,
                              void *workspace, size_t workspace_bytes, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
     if (st != KV_OK || P.units == 0) return st;
@@ -180,6 +182,7 @@ kv_status kv_score_attention(const kv_problem *p, const void *q_win, const void 
 
 kv_status kv_score_rescore(const kv_problem *p, const void *q_win, const void *k, const void *v,
                            float *scores, void *workspace, size_t workspace_bytes, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
     if (st != KV_OK || P.units == 0) return st;
@@ -191,6 +194,7 @@ kv_status kv_score_rescore(const kv_problem *p, const void *q_win, const void *k
 
 kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const void *v,
                    float *scores, void *workspace, size_t workspace_bytes, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
     if (st != KV_OK || P.units == 0) return st;
@@ -202,6 +206,7 @@ kv_status kv_score(const kv_problem *p, const void *q_win, const void *k, const 
 
 kv_status kv_pool_scores(const kv_problem *p, int32_t kernel, const float *scores_in,
                          float *scores_out, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = make_problem(p, &P);
     if (st != KV_OK) return st;
@@ -244,6 +249,7 @@ kv_status kv_select_workspace_size(const kv_problem *p, size_t *bytes) {
 kv_status kv_select_topk(const kv_problem *p, const float *scores, const int32_t *budgets_dev,
                          const int64_t *offsets_dev, int32_t *sel_idx, void *workspace,
                          size_t workspace_bytes, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = make_problem(p, &P);
     if (st != KV_OK || P.units == 0) return st;
@@ -263,6 +269,7 @@ kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_
                           const int64_t *offsets_dev, int32_t *budgets_out_dev,
                           int64_t *offsets_out_dev, void *workspace, size_t workspace_bytes,
                           void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = make_problem(p, &P);
     if (st != KV_OK || P.units == 0) return st;
@@ -290,6 +297,7 @@ kv_status kv_head_budgets(const kv_problem *p, const float *scores, const int32_
 
 kv_status kv_block_scores(const kv_problem *p, int32_t block_layers, const float *scores,
                           float *block_scores, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = make_problem(p, &P);
     if (st != KV_OK) return st;
@@ -304,6 +312,7 @@ kv_status kv_compact_blocks(const kv_problem *p, int32_t block_layers, const voi
                             const void *v, const int32_t *block_sel_idx,
                             const int64_t *block_offsets_dev, const int64_t *offsets_dev,
                             int64_t total_rows, void *k_out, void *v_out, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = make_problem(p, &P);
     if (st != KV_OK || P.units == 0) return st;
@@ -326,6 +335,7 @@ kv_status kv_evict_fused(const kv_problem *p, const void *q_win, const void *k, 
                          const int32_t *budgets_dev, const int64_t *offsets_dev,
                          int64_t total_rows, float *scores, int32_t *sel_idx, void *k_out,
                          void *v_out, void *workspace, size_t workspace_bytes, void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = check_score_args(p, &P, q_win, k, v, workspace, workspace_bytes);
     if (st != KV_OK || P.units == 0) return st;
@@ -345,6 +355,7 @@ kv_status kv_evict_fused(const kv_problem *p, const void *q_win, const void *k, 
 kv_status kv_compact(const kv_problem *p, const void *k, const void *v, const int32_t *sel_idx,
                      const int64_t *offsets_dev, int64_t total_rows, void *k_out, void *v_out,
                      void *stream) {
+    KV_API_RANGE();
     DevProblem P;
     kv_status st = make_problem(p, &P);
     if (st != KV_OK || P.units == 0) return st;
@@ -364,6 +375,7 @@ void kv_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_r
 uint64_t kv_get_wait_limit_ns(void) { return g_wait_ns.load(std::memory_order_relaxed); }
 
 kv_status kv_check_status(void *workspace, void *stream, int32_t *device_status) {
+    KV_API_RANGE();
     if (!workspace || !device_status) return KV_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "kv_internal.cuh"
+#include "kv_trace.cuh"
 
 using namespace kvevict;
 
@@ -192,6 +193,7 @@ kv_status kv_evict_host(const kv_problem *p, const kv_host_plan *plan, const voi
                         int64_t *offsets_host, int32_t *sel_idx_host, void *k_out_host,
                         void *v_out_host, void *workspace, size_t workspace_bytes, void *stream,
                         int32_t *device_status) {
+    KV_API_RANGE();
     if (!device_status) return KV_ERR_INVALID_ARG;
     *device_status = KV_OK;
     if (p && p->num_requests > 0 && !budgets_host) return KV_ERR_INVALID_ARG;
