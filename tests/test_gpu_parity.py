@@ -45,6 +45,8 @@ def test_product_budgets_equal_oracle_budgets(cuda_lib):
     synth.small_variant(synth.LLAMA8B_32K, 4999),
     synth.small_variant(synth.LONG_128K, 5003),
     synth.small_variant(synth.QWEN7B_128K, 10500, kv_heads=1),
+    # G w = 224 (G = 7, w = 32): a full 128-row chunk and a 96-row one
+    synth.small_variant(synth.QWEN7B_128K, 7001).scaled(name="qwen7b_rows224_w32_small", window=32),
     synth.small_variant(synth.RAGGED_MISTRAL, 0, requests=[1500, 4097, 2222]),
 ], ids=lambda w: w.name)
 def test_small_workloads_all_units(cuda_lib, wl):
