@@ -85,6 +85,19 @@ def test_window_row_edges_all_units(cuda_lib, wl):
     assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
 
 
+def test_short_last_chunk_over_several_grid_rounds(cuda_lib):
+    """448 window rows (chunks of 128, 128, 128, 64) with about two rounds of pass-2
+    work items on the grid, where the row chunk rotates by round: every unit
+    against the oracle."""
+    wl = synth.QWEN7B_128K.scaled(name="qwen7b_rows448_4L_4kv_n40000", num_layers=4,
+                                  num_kv_heads=4, num_q_heads=28, lengths=(40000,),
+                                  ragged_range=None, num_heavy=8)
+    assert wl.rows == 448 and wl.num_units == 16
+    run = _run(cuda_lib, wl)
+    res = parity.check_units(run, list(range(wl.num_units)))
+    assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
+
+
 @pytest.mark.parametrize("b_kind", ["minimum", "everything"])
 def test_budget_extremes(cuda_lib, b_kind):
     wl = synth.small_variant(synth.LLAMA8B_32K, 700, layers=1)
