@@ -49,16 +49,20 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
     P->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     P->units = (long long)P->R * P->L * P->H;
     P->max_n = 0;
+    P->uni_n = 0;
     P->N_tot = 0;
     if (P->R > 0) {
         if (!p->seq_offsets_host || !p->seq_offsets_dev) return KV_ERR_INVALID_ARG;
         if (p->seq_offsets_host[0] != 0) return KV_ERR_INVALID_ARG;
+        bool uniform = true;
         for (int r = 0; r < P->R; ++r) {
             const long long n = p->seq_offsets_host[r + 1] - p->seq_offsets_host[r];
             if (n < (long long)p->num_sinks + p->window || n < 1 || n >= (1LL << 31))
                 return KV_ERR_INVALID_ARG;
+            if (r > 0 && n != p->seq_offsets_host[1]) uniform = false;
             P->max_n = std::max<long long>(P->max_n, n);
         }
+        if (uniform) P->uni_n = P->max_n;
         P->N_tot = p->seq_offsets_host[P->R];
     }
     // TMA tile coordinates are 32-bit: the packed K/V rows, the window query rows

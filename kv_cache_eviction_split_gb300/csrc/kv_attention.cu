@@ -42,7 +42,7 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     if (!make_tile_map(&mq, q, q_rows, D) || !make_tile_map(&mk, k, kv_rows, D) ||
         !make_tile_map(&mv, v, kv_rows, D))
         return cudaErrorInvalidValue;
-    launch_plan(P, P.split_keys, ws.plan, st);
+    if (P.uni_n == 0) launch_plan(P, P.split_keys, ws.plan, st);   // ragged lengths only
     AttnArgs A;
     A.plan = ws.plan;
     A.part_ml = ws.part_ml;

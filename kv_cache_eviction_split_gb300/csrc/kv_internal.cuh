@@ -37,6 +37,8 @@ struct DevProblem {
     int rule;                 // kv_score_rule
     int rows;                 // G * w
     int max_n;                // longest request
+    int uni_n;                // the common length when every request has the same one, else 0:
+                              // the work items then decode without the plan tables
     int split_keys;           // keys per pass-1 split (a power of two, 4096..32768)
     int max_splits;           // ceil(max_n / split_keys)
     long long N_tot;          // packed tokens

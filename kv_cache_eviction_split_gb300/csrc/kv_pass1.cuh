@@ -110,15 +110,23 @@ __device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, c
     Item it;
     it.pair = (int)(item % A.pairs);
     const long long gs = item / A.pairs;
-    long long lo = 0, hi = P.units;
-    while (hi - lo > 1) {
-        const long long mid = (lo + hi) >> 1;
-        if (A.plan[mid] <= gs) lo = mid; else hi = mid;
+    long long lo = 0, first = 0;
+    if (P.uni_n > 0) {          // every unit has the same number of splits
+        const long long per = (P.uni_n + P.split_keys - 1) / P.split_keys;
+        lo = gs / per;
+        first = lo * per;
+    } else {                    // ragged: the plan holds each unit's first split
+        long long hi = P.units;
+        while (hi - lo > 1) {
+            const long long mid = (lo + hi) >> 1;
+            if (A.plan[mid] <= gs) lo = mid; else hi = mid;
+        }
+        first = A.plan[lo];
     }
     it.u = lo;
     const int r = (int)(lo / ((long long)P.L * P.H));
     const int n = (int)(P.cu[r + 1] - P.cu[r]);
-    it.split = (int)(gs - A.plan[lo]);
+    it.split = (int)(gs - first);
     const int k0 = it.split * P.split_keys;
     const int k1 = min(n, k0 + P.split_keys);
     it.t0 = k0 / kTileKeys;

@@ -116,16 +116,25 @@ __device__ __forceinline__ Item decode_item(long long item, long long ncta, cons
     if (P.rows % kChunkRows != 0 && ncta % A.chunks == 0)
         it.c = (int)((it.c + item / ncta) % A.chunks);
     const long long gb = item / A.chunks;
-    long long lo = 0, hi = P.units;            // plan[lo] <= gb < plan[hi]
-    while (hi - lo > 1) {
-        const long long mid = (lo + hi) >> 1;
-        if (A.plan[mid] <= gb) lo = mid; else hi = mid;
+    long long lo = 0, first = 0;
+    if (P.uni_n > 0) {          // every unit has the same number of key blocks
+        const long long tiles_u = (P.uni_n + kTileKeys - 1) / kTileKeys;
+        const long long per = (tiles_u + kTilesPerItem - 1) / kTilesPerItem;
+        lo = gb / per;
+        first = lo * per;
+    } else {                    // ragged: plan[lo] <= gb < plan[lo + 1]
+        long long hi = P.units;
+        while (hi - lo > 1) {
+            const long long mid = (lo + hi) >> 1;
+            if (A.plan[mid] <= gb) lo = mid; else hi = mid;
+        }
+        first = A.plan[lo];
     }
     it.u = lo;
     const int n = (int)(P.cu[(int)(lo / ((long long)P.L * P.H)) + 1] -
                         P.cu[(int)(lo / ((long long)P.L * P.H))]);
     const int tiles = (n + kTileKeys - 1) / kTileKeys;
-    it.t_begin = (int)(gb - A.plan[lo]) * kTilesPerItem;
+    it.t_begin = (int)(gb - first) * kTilesPerItem;
     it.t_end = min(it.t_begin + kTilesPerItem, tiles);
     return it;
 }

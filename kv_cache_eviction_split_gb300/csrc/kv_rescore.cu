@@ -46,7 +46,7 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
         !make_tile_map(&mv, v, kv_rows, D) || !make_tile_map(&mhi, ws.a_hi, a_rows, D) ||
         !make_tile_map(&mlo, ws.a_lo, a_rows, D))
         return cudaErrorInvalidValue;
-    launch_plan(P, kTileKeys * kTilesPerItem, ws.plan, st);
+    if (P.uni_n == 0) launch_plan(P, kTileKeys * kTilesPerItem, ws.plan, st);   // ragged only
     const long long blocks = total_blocks(P, kTileKeys * kTilesPerItem);
     const int chunks = ws.chunks;
     RescoreArgs A;
