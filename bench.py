@@ -266,8 +266,9 @@ def run_reference(args, wl, budgets):
 STAGES = ["attention", "rescore", "blocks", "pool", "heads", "select", "compact"]
 # attention: plan_kernel, attn_tc_kernel, attn_merge_kernel; rescore: plan_kernel,
 # rescore_tc_kernel and, when the window rows span more than one 128-row chunk,
-# chunk_sum_kernel.  The two plan_kernel launches happen only when the requests'
-# lengths differ (with equal lengths the work items decode without a plan).
+# chunk_sum_kernel.  The two plan_kernel launches happen only when the requests
+# form more than 32 runs of equal length (otherwise the work items decode from
+# tables passed as kernel parameters).
 # pool: pool_kernel, only with --pool > 1; heads: head_budget_kernel, only with
 # --head-budgets.
 # heads launches a memset and six kernels; blocks (block_sum_kernel) only with
@@ -658,9 +659,10 @@ def main(argv=None):
                  "all_stages": {s: stage_roofline(s, stage_ms[s], wl, budgets, peaks,
                                                   rule, blk)["frac"] for s in stages}})
 
-    uniform = len(set(wl.seq_lengths())) == 1
+    lens = wl.seq_lengths()
+    runs = 1 + sum(1 for a, b in zip(lens, lens[1:]) if a != b)
     launches = (1 if fused else sum(LAUNCHES_PER_STEP[s] for s in stages)
-                + (1 if wl.rows > 128 else 0) - (2 if uniform else 0))
+                + (1 if wl.rows > 128 else 0) - (2 if runs <= 32 else 0))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -21,6 +21,56 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+}  // namespace
+
+namespace kvevict {
+
+void build_item_order(const DevProblem &P, long long bk, ItemOrder *O) {
+    const long long *cu = P.host_cu;
+    std::memset(O, 0, sizeof *O);
+    if (P.R == 0) return;
+    const long long lh = (long long)P.L * P.H;
+    // runs of consecutive requests with one length
+    std::vector<int> first, count;
+    for (int r = 0; r < P.R; ++r) {
+        const long long n = cu[r + 1] - cu[r];
+        if (r > 0 && n == cu[r] - cu[r - 1]) {
+            ++count.back();
+        } else {
+            first.push_back(r);
+            count.push_back(1);
+        }
+    }
+    if ((int)first.size() > kMaxOrderRuns) return;
+    const int runs = (int)first.size();
+    long long acc = 0;
+    std::vector<int> part;
+    for (int i = 0; i < runs; ++i) {
+        const long long n = cu[first[i] + 1] - cu[first[i]];
+        O->unit0[i] = first[i] * lh;
+        O->full_first[i] = acc;
+        O->full_cnt[i] = (int)(n / bk);
+        acc += count[i] * lh * (n / bk);
+        if (n % bk) part.push_back(i);
+    }
+    O->full_end = acc;
+    auto part_len = [&](int i) { return (cu[first[i] + 1] - cu[first[i]]) % bk; };
+    std::stable_sort(part.begin(), part.end(),
+                     [&](int a, int b) { return part_len(a) > part_len(b); });
+    long long pacc = 0;
+    for (size_t k = 0; k < part.size(); ++k) {
+        O->part_run[k] = part[k];
+        O->part_first[k] = pacc;
+        pacc += count[part[k]] * lh;
+    }
+    O->n_part = (int)part.size();
+    O->nrun = runs;
+}
+
+}  // namespace kvevict
+
+namespace {
+
 // Validates the problem description and fills the device-side copy.
 kv_status make_problem(const kv_problem *p, DevProblem *P) {
     if (!p) return KV_ERR_INVALID_ARG;
@@ -49,20 +99,16 @@ kv_status make_problem(const kv_problem *p, DevProblem *P) {
     P->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     P->units = (long long)P->R * P->L * P->H;
     P->max_n = 0;
-    P->uni_n = 0;
     P->N_tot = 0;
     if (P->R > 0) {
         if (!p->seq_offsets_host || !p->seq_offsets_dev) return KV_ERR_INVALID_ARG;
         if (p->seq_offsets_host[0] != 0) return KV_ERR_INVALID_ARG;
-        bool uniform = true;
         for (int r = 0; r < P->R; ++r) {
             const long long n = p->seq_offsets_host[r + 1] - p->seq_offsets_host[r];
             if (n < (long long)p->num_sinks + p->window || n < 1 || n >= (1LL << 31))
                 return KV_ERR_INVALID_ARG;
-            if (r > 0 && n != p->seq_offsets_host[1]) uniform = false;
             P->max_n = std::max<long long>(P->max_n, n);
         }
-        if (uniform) P->uni_n = P->max_n;
         P->N_tot = p->seq_offsets_host[P->R];
     }
     // TMA tile coordinates are 32-bit: the packed K/V rows, the window query rows

@@ -14,22 +14,23 @@ template <int D, bool kOneQ>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-               const AttnArgs A) {
+               const AttnArgs A, const __grid_constant__ ItemOrder ord) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t tmem =
         tmem_acquire_all(reinterpret_cast<uint32_t *>(smem + Layout<D, kOneQ>::kMisc));
-    attn_tc_body<D, kOneQ>(P, &tm_q, &tm_k, &tm_v, A, smem, tmem, blockIdx.x, gridDim.x);
+    attn_tc_body<D, kOneQ>(P, &tm_q, &tm_k, &tm_v, A, ord, smem, tmem, blockIdx.x, gridDim.x);
     tmem_release_all(tmem);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kStatThreads, 1)
 attn_stats_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_k, const AttnArgs A) {
+                  const __grid_constant__ CUtensorMap tm_k, const AttnArgs A,
+                  const __grid_constant__ ItemOrder ord) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t tmem =
         tmem_acquire_all(reinterpret_cast<uint32_t *>(smem + StatLayout<D>::kMisc));
-    attn_stats_body<D>(P, &tm_q, &tm_k, A, smem, tmem, blockIdx.x, gridDim.x);
+    attn_stats_body<D>(P, &tm_q, &tm_k, A, ord, smem, tmem, blockIdx.x, gridDim.x);
     tmem_release_all(tmem);
 }
 
@@ -42,7 +43,10 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
     if (!make_tile_map(&mq, q, q_rows, D) || !make_tile_map(&mk, k, kv_rows, D) ||
         !make_tile_map(&mv, v, kv_rows, D))
         return cudaErrorInvalidValue;
-    if (P.uni_n == 0) launch_plan(P, P.split_keys, ws.plan, st);   // ragged lengths only
+    ItemOrder ord;
+    build_item_order(P, P.split_keys, &ord);
+    if (ord.nrun == 0)   // only with more runs of lengths than the order tables hold
+        launch_plan(P, P.split_keys, ws.plan, st);
     AttnArgs A;
     A.plan = ws.plan;
     A.part_ml = ws.part_ml;
@@ -62,7 +66,7 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
         cudaFuncSetAttribute(attn_stats_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
         if (grid > 0)
-            attn_stats_kernel<D><<<(unsigned)grid, kStatThreads, smem, st>>>(P, mq, mk, A);
+            attn_stats_kernel<D><<<(unsigned)grid, kStatThreads, smem, st>>>(P, mq, mk, A, ord);
         return cudaGetLastError();
     }
     // one row chunk (lanes on alternate tiles): one Q slot and a third V stage
@@ -71,13 +75,13 @@ cudaError_t attention_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_
         cudaFuncSetAttribute(attn_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
         if (grid > 0)
-            attn_tc_kernel<D, true><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
+            attn_tc_kernel<D, true><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A, ord);
     } else {
         const int smem = Layout<D, false>::kTotal;
         cudaFuncSetAttribute(attn_tc_kernel<D, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (grid > 0)
-            attn_tc_kernel<D, false><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A);
+            attn_tc_kernel<D, false><<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, A, ord);
     }
     return cudaGetLastError();
 }

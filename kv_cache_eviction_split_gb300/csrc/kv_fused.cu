@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 fused_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
              const __grid_constant__ CUtensorMap tm_ahi,
-             const __grid_constant__ CUtensorMap tm_alo, const FusedArgs F) {
+             const __grid_constant__ CUtensorMap tm_alo, const FusedArgs F,
+             const __grid_constant__ ItemOrder ord1, const __grid_constant__ ItemOrder ord2) {
     using Sm = FusedSmem<D, RULE>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const long long cta = blockIdx.x, ncta = gridDim.x;
@@ -209,11 +210,13 @@ fused_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     // 1. pass 1
     if (ok) {
         if constexpr (RULE == KV_SCORE_ATTN_SUM)
-            pass1::attn_stats_body<D>(P, &tm_q, &tm_k, F.a1, smem, tmem, cta, ncta);
+            pass1::attn_stats_body<D>(P, &tm_q, &tm_k, F.a1, ord1, smem, tmem, cta, ncta);
         else if (F.a1.parts == 2)   // one row chunk: one Q slot, a third V stage
-            pass1::attn_tc_body<D, true>(P, &tm_q, &tm_k, &tm_v, F.a1, smem, tmem, cta, ncta);
+            pass1::attn_tc_body<D, true>(P, &tm_q, &tm_k, &tm_v, F.a1, ord1, smem, tmem, cta,
+                                         ncta);
         else
-            pass1::attn_tc_body<D, false>(P, &tm_q, &tm_k, &tm_v, F.a1, smem, tmem, cta, ncta);
+            pass1::attn_tc_body<D, false>(P, &tm_q, &tm_k, &tm_v, F.a1, ord1, smem, tmem, cta,
+                                          ncta);
     }
     ok = barrier() && ok;
     // 2. merge: one warp per (unit, row)
@@ -226,8 +229,8 @@ fused_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
     ok = barrier() && ok;
     // 3. pass 2
     if (ok)
-        pass2::rescore_body<D, RULE, true>(P, &tm_q, &tm_k, &tm_v, &tm_ahi, &tm_alo, F.a2, smem,
-                                           tmem, cta, ncta);
+        pass2::rescore_body<D, RULE, true>(P, &tm_q, &tm_k, &tm_v, &tm_ahi, &tm_alo, F.a2, ord2,
+                                           smem, tmem, cta, ncta);
     ok = barrier() && ok;
     // 4. chunk partials -> scores, in chunk order
     if (F.ws.chunks > 1) {
@@ -273,6 +276,9 @@ cudaError_t fused_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bflo
         !make_tile_map(&mlo, ws.a_lo, a_rows, D))
         return cudaErrorInvalidValue;
     FusedArgs F{};
+    ItemOrder ord1, ord2;                // kernel parameters: the item decode reads them in place
+    build_item_order(P, P.split_keys, &ord1);
+    build_item_order(P, kPass2BlockKeys, &ord2);
     F.a1.plan = ws.plan;
     F.a1.part_ml = ws.part_ml;
     F.a1.part_o = ws.part_o;
@@ -320,7 +326,7 @@ cudaError_t fused_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bflo
     if (e != cudaSuccess) return e;
     if (!coop || per_sm != 1) return cudaErrorCooperativeLaunchTooLarge;
     DevProblem Pc = P;
-    void *args[] = {&Pc, &mq, &mk, &mv, &mhi, &mlo, &F};
+    void *args[] = {&Pc, &mq, &mk, &mv, &mhi, &mlo, &F, &ord1, &ord2};
     // one CTA per SM: each holds all 512 TMEM columns
     return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(kern), dim3((unsigned)sms),
                                        dim3(kFusedThreads), args, (size_t)smem, st);

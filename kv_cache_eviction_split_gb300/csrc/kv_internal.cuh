@@ -31,14 +31,38 @@ constexpr int kSplitSms = 152;
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kGridBarOffset = 64;
 
+// Keys per pass-2 work item (64 tiles of 128 keys).
+constexpr int kPass2BlockKeys = 8192;
+// Runs of equal-length requests the work-item order tables hold (more: the plan
+// tables in the workspace).
+constexpr int kMaxOrderRuns = 32;
+
+// Order of the work items of one pass, built on the host (build_item_order) and
+// passed to the kernels as a __grid_constant__ parameter, which the item decode
+// indexes in place.  An item is one key block (block_keys keys) of one unit.
+// Consecutive requests of one length form a run (one run when all lengths are
+// equal).  The full blocks come first, unit-major; then the partial last blocks,
+// run by run, the runs with the longest partial block first.  A persistent grid
+// takes items round-robin, so the equal full blocks fill whole rounds and the
+// short partial blocks even out the last ones (the plain unit-major order left
+// one SM in ten with 10% more pass-1 work on the ragged batch).
+struct ItemOrder {
+    int nrun;                            // runs in the tables; 0: not used (plan tables)
+    int n_part;                          // runs with a partial last block
+    long long full_end;                  // items [0, full_end) are full blocks
+    long long unit0[kMaxOrderRuns];      // first unit of run i
+    long long full_first[kMaxOrderRuns]; // first full item of run i
+    int full_cnt[kMaxOrderRuns];         // full blocks of each unit of run i
+    int part_run[kMaxOrderRuns];         // runs with a partial block, longest first
+    long long part_first[kMaxOrderRuns]; // first partial item (minus full_end) of part_run[k]
+};
+
 // Problem description passed by value to every kernel.
 struct DevProblem {
     int R, L, H, Hq, G, d, w, sinks;
     int rule;                 // kv_score_rule
     int rows;                 // G * w
     int max_n;                // longest request
-    int uni_n;                // the common length when every request has the same one, else 0:
-                              // the work items then decode without the plan tables
     int split_keys;           // keys per pass-1 split (a power of two, 4096..32768)
     int max_splits;           // ceil(max_n / split_keys)
     long long N_tot;          // packed tokens
@@ -72,6 +96,29 @@ __host__ __device__ inline UnitInfo unit_info(const DevProblem &P, long long u, 
     return U;
 }
 
+// Unit and block of item g of a pass ordered by O (O.nrun > 0).  Item counts stay
+// below 2^31 (the row limits of make_problem), so the arithmetic is 32-bit.  Not
+// inlined: it runs once per work item, and inlined into every role's item loop it
+// took registers from the kernels' tile loops.
+static __device__ __noinline__ void order_decode(const ItemOrder &O, long long g64, long long &u,
+                                                 int &blk) {
+    const int g = (int)g64;
+    if (g64 < O.full_end) {
+        int r = 0;
+        while (r + 1 < O.nrun && O.full_first[r + 1] <= g64) ++r;
+        const int off = g - (int)O.full_first[r];
+        u = O.unit0[r] + off / O.full_cnt[r];
+        blk = off % O.full_cnt[r];
+    } else {
+        const int j = g - (int)O.full_end;
+        int k = 0;
+        while (k + 1 < O.n_part && O.part_first[k + 1] <= j) ++k;
+        const int r = O.part_run[k];
+        u = O.unit0[r] + (j - (int)O.part_first[k]);
+        blk = O.full_cnt[r];
+    }
+}
+
 // Score workspace carve-up (all offsets 256-byte aligned).
 struct ScoreWs {
     int *status;
@@ -93,6 +140,9 @@ struct ScoreWs {
 
 ScoreWs score_ws_layout(const DevProblem &P, void *base);
 
+// The item order of a pass with key blocks of `block_keys` keys (from host_cu);
+// nrun = 0 when the requests form more than kMaxOrderRuns runs of one length.
+void build_item_order(const DevProblem &P, long long block_keys, ItemOrder *O);
 // plan[u] = sum over units u' < u of ceil(n_u' / keys_per_block); plan[units] = total.
 void launch_plan(const DevProblem &P, int keys_per_block, int32_t *plan, cudaStream_t s);
 // 2-D TMA map over a row-major [rows][D] bf16 tensor: box 128 rows x 64 columns,

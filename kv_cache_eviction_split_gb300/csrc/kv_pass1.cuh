@@ -106,27 +106,26 @@ struct Item {
     int split, pair, t0, t1;   // tiles [t0, t1) of the split (unit-local tile index)
 };
 
-__device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, const DevProblem &P) {
+// `O` is the kernel's item-order parameter (used when O.nrun > 0).
+__device__ __forceinline__ Item decode_item(long long item, const AttnArgs &A, const DevProblem &P,
+                                            const ItemOrder &O) {
     Item it;
     it.pair = (int)(item % A.pairs);
     const long long gs = item / A.pairs;
-    long long lo = 0, first = 0;
-    if (P.uni_n > 0) {          // every unit has the same number of splits
-        const long long per = (P.uni_n + P.split_keys - 1) / P.split_keys;
-        lo = gs / per;
-        first = lo * per;
-    } else {                    // ragged: the plan holds each unit's first split
+    long long lo = 0;
+    if (O.nrun > 0) {           // full splits first, then partial ones
+        order_decode(O, gs, lo, it.split);
+    } else {                    // many runs of lengths: the plan holds each unit's first split
         long long hi = P.units;
         while (hi - lo > 1) {
             const long long mid = (lo + hi) >> 1;
             if (A.plan[mid] <= gs) lo = mid; else hi = mid;
         }
-        first = A.plan[lo];
+        it.split = (int)(gs - A.plan[lo]);
     }
     it.u = lo;
     const int r = (int)(lo / ((long long)P.L * P.H));
     const int n = (int)(P.cu[r + 1] - P.cu[r]);
-    it.split = (int)(gs - first);
     const int k0 = it.split * P.split_keys;
     const int k1 = min(n, k0 + P.split_keys);
     it.t0 = k0 / kTileKeys;
@@ -306,8 +305,8 @@ __device__ __forceinline__ float row_half_sq(const uint8_t *tile, int row, int h
 template <int D, bool kOneQ = false>
 __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorMap *tm_q,
                                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                             const AttnArgs A, uint8_t *smem, uint32_t tmem,
-                                             long long cta, long long ncta) {
+                                             const AttnArgs A, const ItemOrder &ord, uint8_t *smem,
+                                             uint32_t tmem, long long cta, long long ncta) {
     using Ly = Layout<D, kOneQ>;
     constexpr int kKStages = Ly::kKSt;
     constexpr int kVStages = Ly::kVSt;
@@ -372,7 +371,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
             long long qcount = 0, kiss = 0;     // Q and K loads issued
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, A, P);
+                const Item it = decode_item(item, A, P, ord);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
                 const LaneWork w0 = lane_work(A, it, 0), w1 = lane_work(A, it, 1);
                 const bool two_q = A.parts == 1 && w1.steps > 0;
@@ -423,7 +422,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
             long long tcount = 0, viss = 0;     // V tiles loaded (= issued)
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, A, P);
+                const Item it = decode_item(item, A, P, ord);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
                 const int ntiles = it.t1 - it.t0;
                 for (int i = 0; ok && i < ntiles; ++i) {
@@ -464,7 +463,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
             long long oc[2] = {0, 0};   // items in which the lane took part
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, A, P);
+                const Item it = decode_item(item, A, P, ord);
                 const LaneWork w[2] = {lane_work(A, it, 0), lane_work(A, it, 1)};
                 // the lane whose MMAs are the last to read a tile frees its K/V stage
                 const int releaser = (A.parts == 1 && w[1].steps > 0) ? 1 : -1;
@@ -577,7 +576,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
         long long sc = 0, oc = 0;
         bool ok = true;
         for (long long item = cta; ok && item < A.total_items; item += ncta) {
-            const Item it = decode_item(item, A, P);
+            const Item it = decode_item(item, A, P, ord);
             const LaneWork w = lane_work(A, it, L);
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const int row = w.chunk * kChunkRows + rr;
@@ -752,7 +751,7 @@ __device__ __forceinline__ void attn_tc_body(const DevProblem P, const CUtensorM
         long long tbase = 0;   // tiles of this CTA's earlier items (V stage and parity)
         bool ok = true;
         for (long long item = cta; ok && item < A.total_items; item += ncta) {
-            const Item it = decode_item(item, A, P);
+            const Item it = decode_item(item, A, P, ord);
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const int item_tiles = it.t1 - it.t0;
             for (int ti = 0; ok && ti < item_tiles; ++ti) {
@@ -844,8 +843,8 @@ struct StatLayout {
 template <int D>
 __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtensorMap *tm_q,
                                                 const CUtensorMap *tm_k, const AttnArgs A,
-                                                uint8_t *smem, uint32_t tmem, long long cta,
-                                                long long ncta) {
+                                                const ItemOrder &ord, uint8_t *smem, uint32_t tmem,
+                                                long long cta, long long ncta) {
     using Ly = StatLayout<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -889,7 +888,7 @@ __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtens
             long long tcount = 0, icount = 0, qcount = 0, kiss = 0;
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, A, P);
+                const Item it = decode_item(item, A, P, ord);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
                 const LaneWork w0 = lane_work(A, it, 0), w1 = lane_work(A, it, 1);
                 const bool two_q = A.parts == 1 && w1.steps > 0;
@@ -943,7 +942,7 @@ __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtens
             long long sc[2] = {0, 0};   // S tiles issued per lane (buffer and parity)
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, A, P);
+                const Item it = decode_item(item, A, P, ord);
                 const LaneWork w[2] = {lane_work(A, it, 0), lane_work(A, it, 1)};
                 const int releaser = (A.parts == 1 && w[1].steps > 0) ? 1 : -1;
                 ok = mbar_wait(q_full, (uint32_t)(icount & 1), abort_flag, P.wait_ns);
@@ -1005,7 +1004,7 @@ __device__ __forceinline__ void attn_stats_body(const DevProblem P, const CUtens
         long long sc = 0;
         bool ok = true;
         for (long long item = cta; ok && item < A.total_items; item += ncta) {
-            const Item it = decode_item(item, A, P);
+            const Item it = decode_item(item, A, P, ord);
             const LaneWork w = lane_work(A, it, L);
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const int row = w.chunk * kChunkRows + rr;

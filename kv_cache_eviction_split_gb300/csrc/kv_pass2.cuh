@@ -64,6 +64,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBlockBytes = kChunkRows * 128;   // one [128 rows][64 bf16] swizzled box
+static_assert(kTileKeys * kTilesPerItem == kPass2BlockKeys, "pass-2 item order tables");
 
 template <int D, int RULE>
 struct Layout {
@@ -110,31 +111,29 @@ struct Item {
 // rotation is the same for all chunks of a block) and gives every CTA every chunk
 // in turn (448 rows: pass 2 4.61 -> 4.53 ms; with equal chunks it is not applied).
 __device__ __forceinline__ Item decode_item(long long item, long long ncta, const RescoreArgs &A,
-                                            const DevProblem &P) {
+                                            const DevProblem &P, const ItemOrder &O) {
     Item it;
     it.c = (int)(item % A.chunks);
     if (P.rows % kChunkRows != 0 && ncta % A.chunks == 0)
         it.c = (int)((it.c + item / ncta) % A.chunks);
     const long long gb = item / A.chunks;
-    long long lo = 0, first = 0;
-    if (P.uni_n > 0) {          // every unit has the same number of key blocks
-        const long long tiles_u = (P.uni_n + kTileKeys - 1) / kTileKeys;
-        const long long per = (tiles_u + kTilesPerItem - 1) / kTilesPerItem;
-        lo = gb / per;
-        first = lo * per;
-    } else {                    // ragged: plan[lo] <= gb < plan[lo + 1]
+    long long lo = 0;
+    int blk = 0;
+    if (O.nrun > 0) {           // full blocks first, then partial ones
+        order_decode(O, gb, lo, blk);
+    } else {                    // many runs of lengths: plan[lo] <= gb < plan[lo + 1]
         long long hi = P.units;
         while (hi - lo > 1) {
             const long long mid = (lo + hi) >> 1;
             if (A.plan[mid] <= gb) lo = mid; else hi = mid;
         }
-        first = A.plan[lo];
+        blk = (int)(gb - A.plan[lo]);
     }
     it.u = lo;
     const int n = (int)(P.cu[(int)(lo / ((long long)P.L * P.H)) + 1] -
                         P.cu[(int)(lo / ((long long)P.L * P.H))]);
     const int tiles = (n + kTileKeys - 1) / kTileKeys;
-    it.t_begin = (int)(gb - first) * kTilesPerItem;
+    it.t_begin = blk * kTilesPerItem;
     it.t_end = min(it.t_begin + kTilesPerItem, tiles);
     return it;
 }
@@ -254,8 +253,9 @@ template <int D, int RULE, bool kCoherent = false>
 __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorMap *tm_q,
                                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                              const CUtensorMap *tm_ahi, const CUtensorMap *tm_alo,
-                                             const RescoreArgs A, uint8_t *smem, uint32_t tmem,
-                                             long long cta, long long ncta) {
+                                             const RescoreArgs A, const ItemOrder &ord,
+                                             uint8_t *smem, uint32_t tmem, long long cta,
+                                             long long ncta) {
     using Ly = Layout<D, RULE>;
     constexpr bool kX = Ly::kX;
     constexpr int kKSt = Ly::kKSt;
@@ -319,7 +319,7 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
             int pf_t = 0, pf_end = 0;
             auto pf_open = [&]() {
                 if (pf_item < A.total_items) {
-                    const Item pi = decode_item(pf_item, ncta, A, P);
+                    const Item pi = decode_item(pf_item, ncta, A, P, ord);
                     pf_row0 = unit_info(P, pi.u, P.cu).kv_row0;
                     pf_t = pi.t_begin;
                     pf_end = pi.t_end;
@@ -345,7 +345,7 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
             pf_open();
             for (int i = 0; i < kPrefetchTiles; ++i) pf_step();
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, ncta, A, P);
+                const Item it = decode_item(item, ncta, A, P, ord);
                 const UnitInfo U = unit_info(P, it.u, P.cu);
                 ok = mbar_wait(qa_empty, (uint32_t)(icount & 1) ^ 1u, abort_flag, P.wait_ns);
                 if (!ok) break;
@@ -418,7 +418,7 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
             long long tcount = 0, icount = 0;
             bool ok = true;
             for (long long item = cta; ok && item < A.total_items; item += ncta) {
-                const Item it = decode_item(item, ncta, A, P);
+                const Item it = decode_item(item, ncta, A, P, ord);
                 const uint32_t idesc = idesc_bf16_f32(128, chunk_rows_n(P, it.c));
                 ok = mbar_wait(qa_full, (uint32_t)(icount & 1), abort_flag, P.wait_ns);
                 if (!ok) break;
@@ -500,7 +500,7 @@ __device__ __forceinline__ void rescore_body(const DevProblem P, const CUtensorM
         long long tcount = 0;
         bool ok = true;
         for (long long item = cta; ok && item < A.total_items; item += ncta) {
-            const Item it = decode_item(item, ncta, A, P);
+            const Item it = decode_item(item, ncta, A, P, ord);
             const UnitInfo U = unit_info(P, it.u, P.cu);
             const int groups = chunk_rows_n(P, it.c) / 32;
             const int row_first = it.c * kChunkRows + 2 * part;   // unit-local row of pair 0

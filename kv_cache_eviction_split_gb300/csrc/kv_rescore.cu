@@ -15,11 +15,12 @@ rescore_tc_kernel(const DevProblem P, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_ahi,
-                  const __grid_constant__ CUtensorMap tm_alo, const RescoreArgs A) {
+                  const __grid_constant__ CUtensorMap tm_alo, const RescoreArgs A,
+                  const __grid_constant__ ItemOrder ord) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t tmem =
         tmem_acquire_all(reinterpret_cast<uint32_t *>(smem + Layout<D, RULE>::kMisc));
-    rescore_body<D, RULE>(P, &tm_q, &tm_k, &tm_v, &tm_ahi, &tm_alo, A, smem, tmem, blockIdx.x,
+    rescore_body<D, RULE>(P, &tm_q, &tm_k, &tm_v, &tm_ahi, &tm_alo, A, ord, smem, tmem, blockIdx.x,
                           gridDim.x);
     tmem_release_all(tmem);
 }
@@ -46,7 +47,10 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
         !make_tile_map(&mv, v, kv_rows, D) || !make_tile_map(&mhi, ws.a_hi, a_rows, D) ||
         !make_tile_map(&mlo, ws.a_lo, a_rows, D))
         return cudaErrorInvalidValue;
-    if (P.uni_n == 0) launch_plan(P, kTileKeys * kTilesPerItem, ws.plan, st);   // ragged only
+    ItemOrder ord;
+    build_item_order(P, kPass2BlockKeys, &ord);
+    if (ord.nrun == 0)   // only with more runs of lengths than the order tables hold
+        launch_plan(P, kTileKeys * kTilesPerItem, ws.plan, st);
     const long long blocks = total_blocks(P, kTileKeys * kTilesPerItem);
     const int chunks = ws.chunks;
     RescoreArgs A;
@@ -69,7 +73,7 @@ cudaError_t rescore_d(const DevProblem &P, const __nv_bfloat16 *q, const __nv_bf
     const long long grid = std::min<long long>(sms, A.total_items);
     if (grid > 0)
         rescore_tc_kernel<D, RULE>
-            <<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, mhi, mlo, A);
+            <<<(unsigned)grid, kThreads, smem, st>>>(P, mq, mk, mv, mhi, mlo, A, ord);
     if (chunks > 1)
         chunk_sum_kernel<<<sms * 8, 256, 0, st>>>(ws.part_scores, kv_rows, chunks, scores);
     return cudaGetLastError();
