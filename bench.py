@@ -286,18 +286,18 @@ STAGE_KERNELS = {"attention": "attn_tc_kernel", "rescore": "rescore_tc_kernel",
 # the scale factor; bench reports traffic as null once the sources differ.
 TRAFFIC = {
     ("long_32L_8kv_32q_d128_n131072_pyramid10", "dropkv", 1, False): {
-        "src": "f9421826a1723375", "case": "long_2L_2kv_8q_d128_n131072_pyramid10", "scale": 64,
-        "bytes": {"attn_tc_kernel": 17497522176, "rescore_tc_kernel": 17558700032}},
+        "src": "42267627bf73f97c", "case": "long_2L_2kv_8q_d128_n131072_pyramid10", "scale": 64,
+        "bytes": {"attn_tc_kernel": 17546493952, "rescore_tc_kernel": 17584996352}},
     ("llama8b_32L_8kv_32q_d128_n32768", "dropkv", 1, False): {
-        "src": "f9421826a1723375", "case": "llama8b_2L_8kv_32q_d128_n32768", "scale": 16,
-        "bytes": {"attn_tc_kernel": 4378284032, "rescore_tc_kernel": 4379897856}},
+        "src": "42267627bf73f97c", "case": "llama8b_2L_8kv_32q_d128_n32768", "scale": 16,
+        "bytes": {"attn_tc_kernel": 4389621760, "rescore_tc_kernel": 4383350784}},
     ("qwen7b_28L_4kv_28q_d128_n131072_ripple5", "dropkv", 1, False): {
-        "src": "f9421826a1723375", "case": "qwen7b_2L_2kv_14q_d128_n131072_ripple5", "scale": 28,
-        "bytes": {"attn_tc_kernel": 8145320960, "rescore_tc_kernel": 7806761984}},
+        "src": "42267627bf73f97c", "case": "qwen7b_2L_2kv_14q_d128_n131072_ripple5", "scale": 28,
+        "bytes": {"attn_tc_kernel": 8184501248, "rescore_tc_kernel": 7831118848}},
     ("ragged8_mistral7b_32L_8kv_32q_d128_n16k-128k", "dropkv", 1, False): {
-        "src": "f9421826a1723375", "case": "ragged8_mistral7b_2L_2kv_8q_d128_n16k-128k",
+        "src": "42267627bf73f97c", "case": "ragged8_mistral7b_2L_2kv_8q_d128_n16k-128k",
         "scale": 64,
-        "bytes": {"attn_tc_kernel": 91514109952, "rescore_tc_kernel": 88520704000}},
+        "bytes": {"attn_tc_kernel": 91530002432, "rescore_tc_kernel": 88923734016}},
 }
 
 

@@ -98,6 +98,27 @@ def test_short_last_chunk_over_several_grid_rounds(cuda_lib):
     assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
 
 
+def test_more_length_runs_than_the_order_tables(cuda_lib):
+    """34 requests of distinct lengths: more runs of equal length than the work-item
+    order tables hold, so both passes decode their items from the plan tables that
+    a kernel computes in the workspace; every unit against the oracle, and the
+    fused launch bit for bit against the separate calls."""
+    lengths = tuple(300 + 97 * i for i in range(34))
+    wl = synth.TINY.scaled(name="runs34_d64_g4_w8", num_kv_heads=1, num_q_heads=4, window=8,
+                           lengths=lengths, ragged_range=None, num_heavy=0,
+                           budget_tokens=None, budget_ratio=0.3)
+    assert len(set(lengths)) == 34
+    run = _run(cuda_lib, wl)
+    res = parity.check_units(run, list(range(wl.num_units)))
+    assert max(r["max_rel"] for r in res.values()) <= parity.SCORE_RTOL
+    import torch
+    fused = _run(cuda_lib, wl, dw=run.dw, fused=True)
+    for name in ("scores", "sel", "k_out", "v_out"):
+        a, b = getattr(run.bufs, name), getattr(fused.bufs, name)
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)), name
+
+
 @pytest.mark.parametrize("b_kind", ["minimum", "everything"])
 def test_budget_extremes(cuda_lib, b_kind):
     wl = synth.small_variant(synth.LLAMA8B_32K, 700, layers=1)
